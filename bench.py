@@ -1,0 +1,379 @@
+#!/usr/bin/env python
+"""Throughput of the Mamba2 mixer block on GB300.
+
+One step = one paged decode of 64 rows from a 256-slot state pool plus one
+prefill of 4 x 2048 tokens (chunk 256, zero initial state), i.e. every stage
+of the block's hot path.  Inputs are synthetic (seeded), resident in HBM; L2
+is flushed (256 MiB write) before every timed step and the flush is outside
+the per-step CUDA-event interval.  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the only reference this path has) on
+a bounded sample of the same workload on the host cores.
+Multi-GPU: replicas only (each rank runs the whole workload on its GPU; no
+exchange); value is the sum over ranks of tokens / the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEC_B, N_SLOTS = 64, 256
+SEQLENS = [2048] * 4
+T_PF = sum(SEQLENS)
+TOKENS_PER_STEP = DEC_B + T_PF
+H, Z, I, CONV = 2688, 10304, 4096, 6144
+WORKLOAD = "mamba2 mixer block: paged decode B=64 (256-slot pool) + prefill 4x2048 (chunk 256, zero state)"
+METRIC = "Mamba2 mixer tokens/s (decode B=64, prefill 4x2048); HBM GB/s & FP8 TC %"
+
+
+def peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+def stage_work():
+    """Algorithmic work per launch of each stage of one step: (kind, amount).
+    kind 'flop' counts 2 per multiply-add; 'byte' counts each operand read or
+    written once (intermediates counted where a stage must move them)."""
+    T, B = T_PF, DEC_B
+    state = 64 * 64 * 128 * 4
+    return {
+        "quant_in": ("byte", T * H * 3),
+        "in_proj": ("flop", 2.0 * T * Z * H),
+        "conv": ("byte", T * CONV * 2 * 2),
+        "conv_state": ("byte", 4 * CONV * 3 * 2),
+        "ssd_cumsum": ("byte", T * 64 * (2 + 8)),
+        "ssd_chunk_state": ("flop", 2.0 * T * 64 * 64 * 128),
+        "ssd_state_pass": ("byte", (T // 256) * 64 * state * 2 + 4 * 64 * state),
+        # causal C.B per group, (C.B o decay) x per head, C S_in per head
+        "ssd_chunk_scan": ("flop", T * (8 * 257 * 128 + 64 * 257 * 64 + 64 * 2 * 64 * 128)),
+        "norm_quant": ("byte", T * I * 5),
+        "out_proj": ("flop", 2.0 * T * H * I),
+        "decode_fused": ("byte", B * (2 * 64 * state + 2 * CONV * 3 * 2 + Z * 2 + I)),
+        "dec_quant_in": ("byte", B * H * 3),
+        "dec_in_proj": ("byte", Z * H + B * H + B * Z * 2),
+        "dec_out_proj": ("byte", H * I + B * I + B * H * 2),
+    }
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(stage):
+    """dram bytes per launch from a committed ncu summary, or None when no
+    capture exists or the kernel's source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path)).get(stage)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    if source_digest(rec["sources"]) != rec["digest"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+
+_ORACLE_W = {}
+
+
+def oracle_sample():
+    """Time the CPU oracle on a bounded sample of the step: decode rows and
+    prefill tokens timed separately, then combined for the step's token mix."""
+    import numpy as np
+
+    import oracle
+    import synth
+    if "w" not in _ORACLE_W:
+        _ORACLE_W["w"] = synth.make_weights(0)
+    Wt = _ORACLE_W["w"]
+    conv = synth.make_conv_state(2, 8)
+    ssm = synth.make_ssm_state(2, 8)
+    h = synth.make_hidden(2, 8)
+    t0 = time.perf_counter()
+    oracle.block_decode(Wt, h[:8], conv, ssm, np.arange(8))
+    t_dec = (time.perf_counter() - t0) / 8
+    tp = 256
+    hp = synth.make_hidden(3, tp)
+    t0 = time.perf_counter()
+    oracle.block_prefill(Wt, hp, [tp])
+    t_pf = (time.perf_counter() - t0) / tp
+    step_s = DEC_B * t_dec + T_PF * t_pf
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        cores = os.cpu_count()
+    return dict(value=TOKENS_PER_STEP / step_s, unit="tokens/s", cores=cores, kind="oracle",
+                sample=f"oracle (numpy float64, sequential recurrence) on 8 decode rows of the 256-slot pool and "
+                       f"one 256-token prefill; per-token costs {t_dec * 1e3:.1f} ms (decode) and "
+                       f"{t_pf * 1e3:.2f} ms (prefill) combined for the step's 64 + 8192 tokens"), step_s
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    samples = []
+    for _ in range(args.warmup):
+        oracle_sample()
+    for _ in range(args.steps):
+        cb, step_s = oracle_sample()
+        samples.append(step_s)
+    step_s = statistics.mean(samples)
+    val = TOKENS_PER_STEP / step_s
+    cb["value"] = val
+    line = dict(metric=METRIC, value=val, unit="tokens/s", n_gpus=args.gpus, steps=args.steps, warmup=args.warmup,
+                ms_per_step=step_s * 1e3, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64",
+                data="synthetic", impl="reference",
+                config=dict(workload=WORKLOAD, sample="bounded sample per step (see cpu_baseline)"),
+                cpu_baseline=cb,
+                e2e=dict(value=val, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- ours (GPU)
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import mamba2_ssm_mixer_gb300 as m2
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    Wt = synth.make_weights(0)
+    w = dict(in_proj=torch.from_numpy(Wt["in_proj"]).to(dev), s_w1=Wt["s_w1"],
+             out_proj=torch.from_numpy(Wt["out_proj"]).to(dev), s_w2=Wt["s_w2"],
+             conv_w=torch.from_numpy(Wt["conv_w"]).to(torch.bfloat16).to(dev), conv_b=None,
+             A_log=torch.from_numpy(Wt["A_log"]).to(dev), D=torch.from_numpy(Wt["D"]).to(dev),
+             dt_bias=torch.from_numpy(Wt["dt_bias"]).to(dev),
+             norm_w=torch.from_numpy(Wt["norm_w"]).to(torch.bfloat16).to(dev),
+             s_x=Wt["s_x"], s_y=Wt["s_y"], eps=Wt["eps"])
+    blk = m2.Mamba2Mixer(w, device=dev)
+    conv_pool = torch.from_numpy(synth.make_conv_state(2, N_SLOTS)).to(torch.bfloat16).to(dev)
+    ssm_pool = torch.from_numpy(synth.make_ssm_state(2, N_SLOTS)).to(dev)
+    slots = torch.from_numpy(synth.make_slot_idx(2, N_SLOTS, DEC_B)).to(dev)
+    h_dec_np = synth.make_hidden(2, DEC_B)
+    h_pf_np = synth.make_hidden(3, T_PF)
+    h_dec = torch.from_numpy(h_dec_np).to(torch.bfloat16).to(dev)
+    h_pf = torch.from_numpy(h_pf_np).to(torch.bfloat16).to(dev)
+    out_dec = torch.empty((DEC_B, H), dtype=torch.bfloat16, device=dev)
+    out_pf = torch.empty((T_PF, H), dtype=torch.bfloat16, device=dev)
+    conv_st = torch.zeros((len(SEQLENS), CONV, 3), dtype=torch.bfloat16, device=dev)
+    ssm_st = torch.zeros((len(SEQLENS), 64, 64, 128), dtype=torch.float32, device=dev)
+    ws_dec = torch.empty(blk.decode_workspace_size(DEC_B), dtype=torch.uint8, device=dev)
+    ws_pf = torch.empty(blk.prefill_workspace_size(SEQLENS), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        blk.decode(h_dec, conv_pool, ssm_pool, slots, out=out_dec, workspace=ws_dec, stream=stream)
+        blk.prefill(h_pf, SEQLENS, conv_st, ssm_st, out=out_pf, workspace=ws_pf, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    blk.check()
+
+    # ---- timed region: device-resident inputs
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    launches0 = blk.stats()["kernel_launches"]
+    blk.profile(True)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    prof = blk.profile_read()
+    blk.profile(False)
+    launches = blk.stats()["kernel_launches"] - launches0
+    blk.check()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # ---- end to end: host buffers, copies inside the timed interval
+    hd_pin = torch.from_numpy(h_dec_np).to(torch.bfloat16).pin_memory()
+    hp_pin = torch.from_numpy(h_pf_np).to(torch.bfloat16).pin_memory()
+    od_pin = torch.empty((DEC_B, H), dtype=torch.bfloat16).pin_memory()
+    op_pin = torch.empty((T_PF, H), dtype=torch.bfloat16).pin_memory()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e2e_ev[i][0].record(stream)
+        h_dec.copy_(hd_pin, non_blocking=True)
+        h_pf.copy_(hp_pin, non_blocking=True)
+        step()
+        od_pin.copy_(out_dec, non_blocking=True)
+        op_pin.copy_(out_pf, non_blocking=True)
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = hd_pin.numel() * 2 + hp_pin.numel() * 2
+    d2h = od_pin.numel() * 2 + op_pin.numel() * 2
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    pk = peaks() or {}
+    hbm = pk.get("hbm_gbs")
+    fp8_sus = 2.0 * pk["bf16_tflops_sustained"] if pk.get("bf16_tflops_sustained") else None
+    bf16_sus = pk.get("bf16_tflops_sustained")
+    peak_src = "of measured" if pk else "of fallback"
+    if not pk:
+        hbm, fp8_sus, bf16_sus = 6800.0, 3400.0, 1700.0
+    work = stage_work()
+    stages = {}
+    for name, (tot_ms, n) in prof.items():
+        per_launch_ms = tot_ms / args.steps
+        kind, amt = work.get(name, ("byte", 0))
+        if kind == "flop":
+            ach = amt / (per_launch_ms * 1e-3) / 1e12
+            peak = fp8_sus if name in ("in_proj", "out_proj") else bf16_sus
+            stages[name] = dict(ms=per_launch_ms, achieved=ach, unit="TFLOP/s", peak=peak, frac=ach / peak)
+        else:
+            ach = amt / (per_launch_ms * 1e-3) / 1e9
+            stages[name] = dict(ms=per_launch_ms, achieved=ach, unit="GB/s", peak=hbm, frac=ach / hbm)
+    dom = max(stages, key=lambda k: stages[k]["ms"])
+    d = stages[dom]
+    roof = dict(kernel=dom, bound="tensor" if d["unit"] == "TFLOP/s" else "hbm", achieved=d["achieved"],
+                peak=d["peak"], unit=d["unit"], frac=d["frac"], traffic=traffic_for(dom),
+                peak_note=f"{peak_src} (fp8 = 2 x measured bf16 sustained; hbm = measured copy)")
+    cb = None
+    if world == 1 and not args.no_cpu_baseline:
+        cb, _ = oracle_sample()
+    value = TOKENS_PER_STEP * world / (ms * 1e-3)
+    line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+                ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="fp8",
+                data="synthetic",
+                config=dict(workload=WORKLOAD, tokens_per_step=TOKENS_PER_STEP, decode_rows=DEC_B,
+                            prefill_tokens=T_PF, l2="flushed before each step (256 MiB write), outside the interval",
+                            parallelism="replicas" if world > 1 else "single GPU"),
+                clocks=clocks,
+                e2e=dict(value=TOKENS_PER_STEP * world / (e2e_ms * 1e-3), unit="tokens/s",
+                         h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
+                gpu_launches=launches, roofline=roof, cpu_baseline=cb,
+                stages={k: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
+                        for k, v in stages.items()})
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

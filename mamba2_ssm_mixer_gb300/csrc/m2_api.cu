@@ -1,0 +1,544 @@
+// The C ABI of libm2 (declared in include/m2.h): argument validation, the
+// handle that owns the block's device weights, workspace carving, and the
+// launch sequence of prefill and decode.  All compute runs in the kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/m2.h"
+#include "m2_kernels.h"
+#include "gemm.h"
+
+using namespace m2;
+
+namespace {
+
+thread_local std::string g_err;
+
+m2_status fail(m2_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define M2_CUDA(call)                                                                          \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess) return fail(M2_ECUDA, "%s: %s", #call, cudaGetErrorString(e_));     \
+  } while (0)
+
+// Launch one kernel stage: optional event bracket, error check, launch count.
+#define M2_STAGE(h, st, stage, nlaunch, call)                                                  \
+  do {                                                                                         \
+    cudaEvent_t a_ = nullptr;                                                                  \
+    if ((h)->prof_on) {                                                                        \
+      a_ = (h)->take_event();                                                                  \
+      cudaEventRecord(a_, st);                                                                 \
+    }                                                                                          \
+    M2_CUDA(call);                                                                             \
+    (h)->stats.kernel_launches += (uint64_t)(nlaunch);                                         \
+    if (a_) {                                                                                  \
+      cudaEvent_t b_ = (h)->take_event();                                                      \
+      cudaEventRecord(b_, st);                                                                 \
+      (h)->recs.push_back({(stage), (int)(nlaunch), a_, b_});                                  \
+    }                                                                                          \
+  } while (0)
+
+m2_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(M2_EDEVICE, "no CUDA device");
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (major != 10 || minor != 3)
+    return fail(M2_EDEVICE, "device %d is sm_%d%d; libm2 is built for sm_103a only", dev, major, minor);
+  return M2_OK;
+}
+
+inline size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Bump allocator over a caller-provided workspace.
+struct Carve {
+  char* base;
+  size_t off = 0;
+  template <class T>
+  T* take(size_t count) {
+    T* p = reinterpret_cast<T*>(base ? base + off : nullptr);
+    off = align256(off + count * sizeof(T));
+    return p;
+  }
+};
+
+}  // namespace
+
+struct m2_handle {
+  int device;
+  m2_config cfg;
+  uint8_t* in_proj = nullptr;
+  uint8_t* out_proj = nullptr;
+  float s_w1 = 0, s_w2 = 0;
+  uint16_t* conv_w = nullptr;
+  uint16_t* conv_b = nullptr;
+  float* A_log = nullptr;
+  float* D = nullptr;
+  float* dt_bias = nullptr;
+  uint16_t* norm_w = nullptr;
+  int* err = nullptr;
+  m2_stats stats;
+  bool taps_on = false;
+  m2_taps taps;
+  // stage timing
+  struct StageRec {
+    int stage, launches;
+    cudaEvent_t a, b;
+  };
+  bool prof_on = false;
+  std::vector<cudaEvent_t> ev_free;
+  std::vector<StageRec> recs;
+  cudaEvent_t take_event() {
+    if (!ev_free.empty()) {
+      cudaEvent_t e = ev_free.back();
+      ev_free.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+
+  BlockParams params() const {
+    BlockParams bp;
+    bp.conv_w = conv_w;
+    bp.conv_b = conv_b;
+    bp.A_log = A_log;
+    bp.D = D;
+    bp.dt_bias = dt_bias;
+    bp.norm_w = norm_w;
+    bp.eps = cfg.eps;
+    bp.s_x = cfg.s_x;
+    bp.s_y = cfg.s_y;
+    return bp;
+  }
+};
+
+extern "C" {
+
+const char* m2_last_error(void) { return g_err.c_str(); }
+
+static m2_status upload(m2_handle* h, void** dst, const void* src, size_t bytes) {
+  M2_CUDA(cudaMalloc(dst, bytes));
+  M2_CUDA(cudaMemcpy(*dst, src, bytes, cudaMemcpyDefault));
+  h->stats.bytes_uploaded += bytes;
+  return M2_OK;
+}
+
+m2_status m2_create(const m2_config* cfg, const m2_weights* w, m2_handle** out) {
+  g_err.clear();
+  if (!cfg || !w || !out) return fail(M2_EINVAL, "m2_create: null argument");
+  *out = nullptr;
+  if (cfg->hidden != kH || cfg->d_inner != kI || cfg->nheads != kNH || cfg->headdim != kP ||
+      cfg->n_groups != kG || cfg->d_state != kN || cfg->conv_width != kW)
+    return fail(M2_ESHAPE,
+                "m2_create: geometry (hidden %d, d_inner %d, nheads %d, headdim %d, n_groups %d, d_state %d, "
+                "conv %d) is not the supported (2688, 4096, 64, 64, 8, 128, 4)",
+                cfg->hidden, cfg->d_inner, cfg->nheads, cfg->headdim, cfg->n_groups, cfg->d_state,
+                cfg->conv_width);
+  if (cfg->chunk_size != kChunk) return fail(M2_ESHAPE, "m2_create: chunk_size %d is not 256", cfg->chunk_size);
+  if (cfg->ssm_dtype != M2_DTYPE_F32)
+    return fail(M2_EINVAL, "m2_create: ssm_dtype must be f32 (the recurrent rows are f32 working state)");
+  if (!(cfg->eps > 0.f) || !(cfg->s_x > 0.f) || !(cfg->s_y > 0.f) || !(cfg->s_x < 3.0e38f) ||
+      !(cfg->s_y < 3.0e38f))
+    return fail(M2_EINVAL, "m2_create: eps and activation scales must be positive and finite");
+  if (!(w->s_w1 > 0.f) || !(w->s_w2 > 0.f) || !(w->s_w1 < 3.0e38f) || !(w->s_w2 < 3.0e38f))
+    return fail(M2_EINVAL, "m2_create: weight scales must be positive and finite");
+  if (w->layout != M2_LAYOUT_OUT_IN)
+    return fail(M2_EINVAL, "m2_create: projection weights must be stored [out, in]");
+  if (!w->in_proj || !w->out_proj || !w->conv_w || !w->A_log || !w->D || !w->dt_bias || !w->norm_w)
+    return fail(M2_EINVAL, "m2_create: a required weight pointer is null");
+  m2_status st = check_device();
+  if (st) return st;
+
+  m2_handle* h = new m2_handle();
+  memset(&h->stats, 0, sizeof h->stats);
+  memset(&h->taps, 0, sizeof h->taps);
+  cudaGetDevice(&h->device);
+  h->cfg = *cfg;
+  h->s_w1 = w->s_w1;
+  h->s_w2 = w->s_w2;
+  m2_status s = M2_OK;
+  if (!s) s = upload(h, (void**)&h->in_proj, w->in_proj, (size_t)kZ * kH);
+  if (!s) s = upload(h, (void**)&h->out_proj, w->out_proj, (size_t)kH * kI);
+  if (!s) s = upload(h, (void**)&h->conv_w, w->conv_w, (size_t)kConv * kW * 2);
+  if (!s && w->conv_b) s = upload(h, (void**)&h->conv_b, w->conv_b, (size_t)kConv * 2);
+  if (!s) s = upload(h, (void**)&h->A_log, w->A_log, kNH * 4);
+  if (!s) s = upload(h, (void**)&h->D, w->D, kNH * 4);
+  if (!s) s = upload(h, (void**)&h->dt_bias, w->dt_bias, kNH * 4);
+  if (!s) s = upload(h, (void**)&h->norm_w, w->norm_w, (size_t)kI * 2);
+  if (!s) {
+    cudaError_t e = cudaMalloc((void**)&h->err, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) s = fail(M2_ECUDA, "m2_create: %s", cudaGetErrorString(e));
+  }
+  if (s) {
+    m2_destroy(h);
+    return s;
+  }
+  *out = h;
+  return M2_OK;
+}
+
+void m2_destroy(m2_handle* h) {
+  if (!h) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(h->device);
+  cudaDeviceSynchronize();
+  cudaFree(h->in_proj);
+  cudaFree(h->out_proj);
+  cudaFree(h->conv_w);
+  cudaFree(h->conv_b);
+  cudaFree(h->A_log);
+  cudaFree(h->D);
+  cudaFree(h->dt_bias);
+  cudaFree(h->norm_w);
+  cudaFree(h->err);
+  for (auto& r : h->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : h->ev_free) cudaEventDestroy(e);
+  cudaSetDevice(prev);
+  delete h;
+}
+
+m2_status m2_get_stats(const m2_handle* h, m2_stats* out) {
+  if (!h || !out) return fail(M2_EINVAL, "m2_get_stats: null argument");
+  *out = h->stats;
+  return M2_OK;
+}
+
+m2_status m2_set_taps(m2_handle* h, const m2_taps* taps) {
+  if (!h) return fail(M2_EINVAL, "m2_set_taps: null handle");
+  if (taps) {
+    h->taps = *taps;
+    h->taps_on = true;
+  } else {
+    memset(&h->taps, 0, sizeof h->taps);
+    h->taps_on = false;
+  }
+  return M2_OK;
+}
+
+m2_status m2_profile_enable(m2_handle* h, int on) {
+  if (!h) return fail(M2_EINVAL, "m2_profile_enable: null handle");
+  h->prof_on = on != 0;
+  if (!h->prof_on) {
+    for (auto& r : h->recs) {
+      h->ev_free.push_back(r.a);
+      h->ev_free.push_back(r.b);
+    }
+    h->recs.clear();
+  }
+  return M2_OK;
+}
+
+m2_status m2_profile_read(m2_handle* h, double* ms, uint64_t* launches) {
+  if (!h) return fail(M2_EINVAL, "m2_profile_read: null handle");
+  for (auto& r : h->recs) {
+    M2_CUDA(cudaEventSynchronize(r.b));
+    float t = 0.f;
+    M2_CUDA(cudaEventElapsedTime(&t, r.a, r.b));
+    if (r.stage >= 0 && r.stage < M2_NSTAGES) {
+      if (ms) ms[r.stage] += t;
+      if (launches) launches[r.stage] += (uint64_t)r.launches;
+    }
+    h->ev_free.push_back(r.a);
+    h->ev_free.push_back(r.b);
+  }
+  h->recs.clear();
+  return M2_OK;
+}
+
+m2_status m2_check(m2_handle* h) {
+  if (!h) return fail(M2_EINVAL, "m2_check: null handle");
+  int v = 0;
+  M2_CUDA(cudaDeviceSynchronize());
+  M2_CUDA(cudaMemcpy(&v, h->err, sizeof v, cudaMemcpyDeviceToHost));
+  M2_CUDA(cudaMemset(h->err, 0, sizeof(int)));
+  if (v & kErrTimeout) return fail(M2_ETIMEOUT, "m2_check: a bounded device wait ran out");
+  if (v & kErrSlot) return fail(M2_EINVAL, "m2_check: a decode row named a slot outside [0, n_slots)");
+  return M2_OK;
+}
+
+// ---------------------------------------------------------------- prefill
+
+static m2_status build_seqinfo(const int32_t* seqlens, int nseq, const uint8_t* has_initial, SeqInfo* si) {
+  if (nseq < 1 || nseq > kMaxSeq) return fail(M2_ESHAPE, "m2_prefill: nseq %d not in [1, %d]", nseq, kMaxSeq);
+  if (!seqlens) return fail(M2_EINVAL, "m2_prefill: seqlens is null");
+  memset(si, 0, sizeof *si);
+  si->nseq = nseq;
+  long long tok = 0, ch = 0;
+  for (int s = 0; s < nseq; ++s) {
+    if (seqlens[s] < 1) return fail(M2_ESHAPE, "m2_prefill: seqlens[%d] = %d < 1", s, seqlens[s]);
+    si->cu_seqlens[s] = (int)tok;
+    si->cu_chunks[s] = (int)ch;
+    tok += seqlens[s];
+    ch += (seqlens[s] + kChunk - 1) / kChunk;
+    if (tok > (1 << 24)) return fail(M2_ESHAPE, "m2_prefill: more than 2^24 tokens in one call");
+    if (has_initial && has_initial[s]) si->has_init[s >> 5] |= 1u << (s & 31);
+  }
+  si->cu_seqlens[nseq] = (int)tok;
+  si->cu_chunks[nseq] = (int)ch;
+  si->total_tokens = (int)tok;
+  si->total_chunks = (int)ch;
+  return M2_OK;
+}
+
+struct PrefillWs {
+  uint8_t* q;
+  uint16_t* zx;
+  uint16_t* u;
+  float* dt;
+  float* cum;
+  float* states;
+  uint16_t* y;
+  uint8_t* q2;
+  void* gemm_ws;
+  size_t gemm_ws_bytes;
+  size_t total;
+};
+
+static PrefillWs carve_prefill(void* base, int T, int chunks) {
+  Carve c{static_cast<char*>(base)};
+  PrefillWs w;
+  w.q = c.take<uint8_t>((size_t)T * kH);
+  w.zx = c.take<uint16_t>((size_t)T * kZ);
+  w.u = c.take<uint16_t>((size_t)T * kConv);
+  w.dt = c.take<float>((size_t)T * kNH);
+  w.cum = c.take<float>((size_t)T * kNH);
+  w.states = c.take<float>((size_t)chunks * kNH * kP * kN);
+  w.y = c.take<uint16_t>((size_t)T * kI);
+  w.q2 = c.take<uint8_t>((size_t)T * kI);
+  size_t g1 = gemm_workspace_bytes(T, kZ, kH), g2 = gemm_workspace_bytes(T, kH, kI);
+  w.gemm_ws_bytes = g1 > g2 ? g1 : g2;
+  w.gemm_ws = c.take<char>(w.gemm_ws_bytes);
+  w.total = c.off;
+  return w;
+}
+
+m2_status m2_prefill_workspace_size(const m2_handle* h, const int32_t* seqlens_host, int nseq, size_t* bytes) {
+  if (!h || !bytes) return fail(M2_EINVAL, "m2_prefill_workspace_size: null argument");
+  SeqInfo si;
+  m2_status s = build_seqinfo(seqlens_host, nseq, nullptr, &si);
+  if (s) return s;
+  *bytes = carve_prefill(nullptr, si.total_tokens, si.total_chunks).total;
+  return M2_OK;
+}
+
+static m2_status copy_tap(void* dst, const void* src, size_t bytes, cudaStream_t st) {
+  if (!dst) return M2_OK;
+  M2_CUDA(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st));
+  return M2_OK;
+}
+
+m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlens_host, int nseq,
+                     const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state, uint16_t* out,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  if (!h || !hidden || !conv_state || !ssm_state || !out || !workspace)
+    return fail(M2_EINVAL, "m2_prefill: null argument");
+  if ((uintptr_t)workspace % 256) return fail(M2_EINVAL, "m2_prefill: workspace must be 256-byte aligned");
+  if ((uintptr_t)hidden % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_state % 16)
+    return fail(M2_EINVAL, "m2_prefill: hidden, out and ssm_state must be 16-byte aligned");
+  SeqInfo local;
+  m2_status s = build_seqinfo(seqlens_host, nseq, has_initial, &local);
+  if (s) return s;
+  const int T = local.total_tokens;
+  PrefillWs w = carve_prefill(workspace, T, local.total_chunks);
+  if (ws_bytes < w.total)
+    return fail(M2_ENOMEM, "m2_prefill: workspace %zu bytes < %zu needed", ws_bytes, w.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const BlockParams bp = h->params();
+  const float sc1 = h->cfg.s_x * h->s_w1, sc2 = h->cfg.s_y * h->s_w2;
+
+  int nl = 0;
+  M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
+  M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, st, &nl));
+  M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(w.zx, bp, conv_state, local, w.u, st));
+  M2_STAGE(h, st, M2_STAGE_CONV_STATE, 1, launch_conv_state_update(w.zx, conv_state, local, st));
+  M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(w.zx, bp, local, w.dt, w.cum, st));
+  M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1, launch_ssd_chunk_state(w.u, w.dt, w.cum, local, w.states, st));
+  M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1, launch_ssd_state_pass(w.states, w.cum, local, ssm_state, st));
+  M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1, launch_ssd_chunk_scan(w.u, w.dt, w.cum, w.states, bp, local, w.y, st));
+  M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
+           launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, h->taps_on ? h->taps.o : nullptr, st));
+  M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, st, &nl));
+  if (h->taps_on) {
+    if ((s = copy_tap(h->taps.q, w.q, (size_t)T * kH, st))) return s;
+    if ((s = copy_tap(h->taps.zx, w.zx, (size_t)T * kZ * 2, st))) return s;
+    if ((s = copy_tap(h->taps.u, w.u, (size_t)T * kConv * 2, st))) return s;
+    if ((s = copy_tap(h->taps.dt, w.dt, (size_t)T * kNH * 4, st))) return s;
+    if ((s = copy_tap(h->taps.y, w.y, (size_t)T * kI * 2, st))) return s;
+    if ((s = copy_tap(h->taps.q2, w.q2, (size_t)T * kI, st))) return s;
+  }
+  h->stats.prefill_calls += 1;
+  h->stats.conv_fwd_calls += 1;
+  h->stats.chunk_scan_calls += 1;
+  return M2_OK;
+}
+
+// ---------------------------------------------------------------- decode
+
+struct DecodeWs {
+  uint8_t* q;
+  uint16_t* zx;
+  uint8_t* q2;
+  void* gemm_ws;
+  size_t gemm_ws_bytes;
+  size_t total;
+};
+
+static DecodeWs carve_decode(void* base, int Bt) {
+  Carve c{static_cast<char*>(base)};
+  DecodeWs w;
+  w.q = c.take<uint8_t>((size_t)Bt * kH);
+  w.zx = c.take<uint16_t>((size_t)Bt * kZ);
+  w.q2 = c.take<uint8_t>((size_t)Bt * kI);
+  size_t g1 = gemm_workspace_bytes(Bt, kZ, kH), g2 = gemm_workspace_bytes(Bt, kH, kI);
+  w.gemm_ws_bytes = g1 > g2 ? g1 : g2;
+  w.gemm_ws = c.take<char>(w.gemm_ws_bytes);
+  w.total = c.off;
+  return w;
+}
+
+m2_status m2_decode_workspace_size(const m2_handle* h, int Bt, size_t* bytes) {
+  if (!h || !bytes) return fail(M2_EINVAL, "m2_decode_workspace_size: null argument");
+  if (Bt < 1 || Bt > 4096) return fail(M2_ESHAPE, "m2_decode: Bt %d not in [1, 4096]", Bt);
+  *bytes = carve_decode(nullptr, Bt).total;
+  return M2_OK;
+}
+
+m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, float* ssm_pool,
+                    int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  g_err.clear();
+  if (!h || !hidden || !conv_pool || !ssm_pool || !slot_idx || !out || !workspace)
+    return fail(M2_EINVAL, "m2_decode: null argument");
+  if (Bt < 1 || Bt > 4096) return fail(M2_ESHAPE, "m2_decode: Bt %d not in [1, 4096]", Bt);
+  if (n_slots < 1) return fail(M2_EINVAL, "m2_decode: n_slots %d < 1", n_slots);
+  if ((uintptr_t)workspace % 256) return fail(M2_EINVAL, "m2_decode: workspace must be 256-byte aligned");
+  if ((uintptr_t)hidden % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_pool % 16)
+    return fail(M2_EINVAL, "m2_decode: hidden, out and ssm_pool must be 16-byte aligned");
+  DecodeWs w = carve_decode(workspace, Bt);
+  if (ws_bytes < w.total) return fail(M2_ENOMEM, "m2_decode: workspace %zu bytes < %zu needed", ws_bytes, w.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const BlockParams bp = h->params();
+  const float sc1 = h->cfg.s_x * h->s_w1, sc2 = h->cfg.s_y * h->s_w2;
+  DecodeTaps dt{};
+  if (h->taps_on) {
+    dt.u = h->taps.u;
+    dt.dt = h->taps.dt;
+    dt.y = h->taps.y;
+    dt.o = h->taps.o;
+  }
+  int nl = 0;
+  M2_STAGE(h, st, M2_STAGE_DEC_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)Bt * kH, h->cfg.s_x, w.q, st));
+  M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, st, &nl));
+  M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
+           launch_decode_fused(w.zx, bp, conv_pool, ssm_pool, n_slots, slot_idx, Bt, w.q2, h->err, dt, st));
+  M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, st, &nl));
+  if (h->taps_on) {
+    m2_status s;
+    if ((s = copy_tap(h->taps.q, w.q, (size_t)Bt * kH, st))) return s;
+    if ((s = copy_tap(h->taps.zx, w.zx, (size_t)Bt * kZ * 2, st))) return s;
+    if ((s = copy_tap(h->taps.q2, w.q2, (size_t)Bt * kI, st))) return s;
+  }
+  h->stats.decode_calls += 1;
+  h->stats.conv_update_rows += (uint64_t)Bt;
+  h->stats.state_update_rows += (uint64_t)Bt;
+  return M2_OK;
+}
+
+// ---------------------------------------------------------------- standalone ops
+
+m2_status fp8_quant(const uint16_t* x, size_t n, float scale, uint8_t* q, void* stream) {
+  g_err.clear();
+  if ((!x || !q) && n) return fail(M2_EINVAL, "fp8_quant: null pointer");
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return fail(M2_EINVAL, "fp8_quant: scale must be positive and finite");
+  m2_status s = check_device();
+  if (s) return s;
+  M2_CUDA(launch_quant_e4m3(x, n, scale, q, static_cast<cudaStream_t>(stream)));
+  return M2_OK;
+}
+
+static m2_status check_linear(const void* a, const uint8_t* w, const uint16_t* y, int M, int N, int K, float s_a,
+                              float s_w, const char* who) {
+  if (M < 0 || N < 1 || K < 16) return fail(M2_ESHAPE, "%s: M %d, N %d, K %d out of range", who, M, N, K);
+  if (K % 16) return fail(M2_ESHAPE, "%s: K %d must be a multiple of 16", who, K);
+  if (M && (!a || !w || !y)) return fail(M2_EINVAL, "%s: null pointer", who);
+  if ((uintptr_t)a % 16 || (uintptr_t)w % 16 || (uintptr_t)y % 16)
+    return fail(M2_EINVAL, "%s: pointers must be 16-byte aligned", who);
+  if (!(s_a > 0.f) || !(s_w > 0.f) || !(s_a < 3.0e38f) || !(s_w < 3.0e38f))
+    return fail(M2_EINVAL, "%s: scales must be positive and finite", who);
+  return check_device();
+}
+
+m2_status fp8_linear_workspace_size(int M, int N, int K, size_t* bytes) {
+  if (!bytes) return fail(M2_EINVAL, "fp8_linear_workspace_size: null argument");
+  if (M < 0 || N < 1 || K < 16 || K % 16) return fail(M2_ESHAPE, "fp8_linear_workspace_size: bad shape");
+  *bytes = gemm_workspace_bytes(M, N, K);
+  return M2_OK;
+}
+
+m2_status fp8_linear(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_w, uint16_t* y, int M, int N, int K,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  m2_status s = check_linear(a_q, w_q, y, M, N, K, s_a, s_w, "fp8_linear");
+  if (s) return s;
+  size_t need = gemm_workspace_bytes(M, N, K);
+  if (ws_bytes < need || (need && !workspace))
+    return fail(M2_ENOMEM, "fp8_linear: workspace %zu bytes < %zu needed", ws_bytes, need);
+  int nl = 0;
+  M2_CUDA(gemm_fp8(a_q, w_q, y, M, N, K, s_a * s_w, workspace, ws_bytes, static_cast<cudaStream_t>(stream), &nl));
+  return M2_OK;
+}
+
+m2_status fp8_linear_bf16(const uint16_t* x, float s_a, const uint8_t* w_q, float s_w, uint16_t* y, int M, int N,
+                          int K, void* workspace, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  m2_status s = check_linear(x, w_q, y, M, N, K, s_a, s_w, "fp8_linear_bf16");
+  if (s) return s;
+  if (!workspace || (uintptr_t)workspace % 256) return fail(M2_EINVAL, "fp8_linear_bf16: workspace must be 256-byte aligned");
+  size_t qbytes = align256((size_t)M * K);
+  size_t need = qbytes + gemm_workspace_bytes(M, N, K);
+  if (ws_bytes < need) return fail(M2_ENOMEM, "fp8_linear_bf16: workspace %zu bytes < %zu needed", ws_bytes, need);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* q = static_cast<uint8_t*>(workspace);
+  M2_CUDA(launch_quant_e4m3(x, (size_t)M * K, s_a, q, st));
+  int nl = 0;
+  M2_CUDA(gemm_fp8(q, w_q, y, M, N, K, s_a * s_w, static_cast<char*>(workspace) + qbytes, ws_bytes - qbytes, st, &nl));
+  return M2_OK;
+}
+
+m2_status m2_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps, uint16_t* normed, int T,
+                              int n, void* stream) {
+  g_err.clear();
+  if (T < 0 || n < 8 || n % 8) return fail(M2_ESHAPE, "m2_rmsnorm_residual: T %d, n %d (n must be a multiple of 8)", T, n);
+  if (T && (!h || !w || !normed)) return fail(M2_EINVAL, "m2_rmsnorm_residual: null pointer");
+  if ((uintptr_t)h % 16 || (uintptr_t)add % 16 || (uintptr_t)w % 16 || (uintptr_t)normed % 16)
+    return fail(M2_EINVAL, "m2_rmsnorm_residual: pointers must be 16-byte aligned");
+  if (!(eps > 0.f)) return fail(M2_EINVAL, "m2_rmsnorm_residual: eps must be positive");
+  m2_status s = check_device();
+  if (s) return s;
+  M2_CUDA(launch_rmsnorm_residual(h, add, w, eps, normed, T, n, static_cast<cudaStream_t>(stream)));
+  return M2_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+"""Shared test helpers: moving synthetic inputs to the device and comparing
+device results with the oracle.  Holds none of the block's arithmetic."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+
+# Tolerances of the block (the benchmark spec of this path):
+OUT_MAX_ABS = 2e-2        # bf16 block output, max abs
+OUT_REL_L2 = 1e-2         # bf16 block output, relative L2
+STATE_REL_L2 = 1e-3       # f32 SSM state, relative L2
+
+
+def bf16_dev(a: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).to(device)
+
+
+def f32_dev(a: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+
+
+def u8_dev(a: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).to(device)
+
+
+def to_np(t: torch.Tensor) -> np.ndarray:
+    t = t.detach().cpu()
+    if t.dtype == torch.bfloat16:
+        t = t.to(torch.float32)
+    return t.numpy().astype(np.float64) if t.dtype != torch.uint8 else t.numpy()
+
+
+def device_weights(Wt: dict, device="cuda") -> dict:
+    return dict(in_proj=u8_dev(Wt["in_proj"], device), s_w1=Wt["s_w1"],
+                out_proj=u8_dev(Wt["out_proj"], device), s_w2=Wt["s_w2"],
+                conv_w=bf16_dev(Wt["conv_w"], device),
+                conv_b=None if Wt["conv_b"] is None else bf16_dev(Wt["conv_b"], device),
+                A_log=f32_dev(Wt["A_log"], device), D=f32_dev(Wt["D"], device),
+                dt_bias=f32_dev(Wt["dt_bias"], device), norm_w=bf16_dev(Wt["norm_w"], device),
+                s_x=Wt["s_x"], s_y=Wt["s_y"], eps=Wt["eps"])
+
+
+def rel_l2(got, ref) -> float:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert got.size > 0          # a maximum over zero elements would also be 0.0
+    den = np.linalg.norm(ref.ravel())
+    return float(np.linalg.norm((got - ref).ravel()) / (den if den > 0 else 1.0))
+
+
+def max_abs(got, ref) -> float:
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape and got.size > 0
+    return float(np.abs(got - ref).max())
+
+
+def assert_block_out(got, ref, what="out"):
+    ma, rl = max_abs(got, ref), rel_l2(got, ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    assert ma <= OUT_MAX_ABS and rl <= OUT_REL_L2, f"{what}: max abs {ma:.3e}, rel L2 {rl:.3e}"
+    return ma, rl
+
+
+def assert_state(got, ref, what="ssm_state"):
+    rl = rel_l2(got, ref)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    assert rl <= STATE_REL_L2, f"{what}: rel L2 {rl:.3e}"
+    return rl
+
+
+def assert_e4m3_close(got_codes, ref_codes, max_frac=2e-3, what="q2"):
+    """Codes of an e4m3 quant whose bf16 input may differ by rounding between
+    the two sides: equal almost everywhere, and at most one code apart."""
+    g = np.asarray(got_codes).astype(np.int64)
+    r = np.asarray(ref_codes).astype(np.int64)
+    assert g.shape == r.shape and g.size > 0
+    diff = g != r
+    frac = diff.mean()
+    assert frac <= max_frac, f"{what}: {frac:.2e} of codes differ"
+    if diff.any():
+        # same sign, adjacent magnitude codes (or +-0)
+        gs, rs = g[diff], r[diff]
+        mag_g, mag_r = gs & 0x7F, rs & 0x7F
+        assert np.all(np.abs(mag_g - mag_r) <= 1), f"{what}: codes more than one step apart"
+
+
+def assert_bf16_close(got, ref, max_frac=5e-3, what="bf16"):
+    """bf16 tensors rounded from slightly different fp32/fp64 values: equal
+    almost everywhere and otherwise within one bf16 ulp."""
+    g = np.asarray(got, np.float64)
+    r = np.asarray(ref, np.float64)
+    assert g.shape == r.shape and g.size > 0
+    diff = g != r
+    frac = diff.mean()
+    assert frac <= max_frac, f"{what}: {frac:.2e} of values differ"
+    if diff.any():
+        ulp = np.abs(r[diff]) * 2.0 ** -7 + 1e-30
+        assert np.all(np.abs(g[diff] - r[diff]) <= ulp * 1.01), f"{what}: difference above one bf16 ulp"
+
+
+def make_block(config: int, layer: int = 0):
+    return synth.make_weights(config, layer)

@@ -1,0 +1,113 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function include/m2.h declares, and refuses bad arguments before touching a
+device.  No kernel is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "m2.h")
+
+
+@pytest.fixture(scope="module")
+def m2():
+    lib = os.path.join(ROOT, "mamba2_ssm_mixer_gb300", "libm2.so")
+    if not os.path.exists(lib):
+        from mamba2_ssm_mixer_gb300 import _build
+        _build.build()
+    import mamba2_ssm_mixer_gb300 as pkg
+    return pkg
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[\w\s\*]+?\b(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "defined")))
+
+
+def test_header_declares_expected_entry_points():
+    names = declared_functions()
+    for n in ["m2_create", "m2_destroy", "m2_prefill", "m2_decode", "fp8_quant", "fp8_linear",
+              "fp8_linear_bf16", "m2_get_stats", "m2_rmsnorm_residual", "m2_check", "m2_last_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(m2):
+    lib = ctypes.CDLL(m2.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(m2.EXPORTED) == set(declared_functions())
+
+
+def _cfg(m2, **kw):
+    c = m2.make_config(1 / 64, 1 / 32)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def _weights(m2, **kw):
+    buf = (ctypes.c_uint8 * 16)()
+    p = ctypes.cast(buf, ctypes.c_void_p).value
+    w = m2.m2_weights(p, 0.01, p, 0.01, p, None, p, p, p, p, m2.M2_LAYOUT_OUT_IN)
+    for k, v in kw.items():
+        setattr(w, k, v)
+    return w, buf
+
+
+@pytest.mark.parametrize("field,value", [("hidden", 2048), ("d_state", 64), ("nheads", 32), ("conv_width", 3)])
+def test_create_refuses_other_geometry(m2, field, value):
+    w, _keep = _weights(m2)
+    h = ctypes.c_void_p()
+    st = m2._lib.m2_create(ctypes.byref(_cfg(m2, **{field: value})), ctypes.byref(w), ctypes.byref(h))
+    assert st == m2.M2_ESHAPE and not h.value
+    assert "geometry" in m2.last_error()
+
+
+def test_create_refuses_non_f32_ssm_state(m2):
+    """The paged arm needs f32 recurrent rows (the ssm_dtype == f32 term)."""
+    w, _keep = _weights(m2)
+    h = ctypes.c_void_p()
+    st = m2._lib.m2_create(ctypes.byref(_cfg(m2, ssm_dtype=m2.M2_DTYPE_BF16)), ctypes.byref(w), ctypes.byref(h))
+    assert st == m2.M2_EINVAL and "ssm_dtype" in m2.last_error()
+
+
+def test_create_refuses_other_orientation(m2):
+    w, _keep = _weights(m2, layout=1)
+    h = ctypes.c_void_p()
+    st = m2._lib.m2_create(ctypes.byref(_cfg(m2)), ctypes.byref(w), ctypes.byref(h))
+    assert st == m2.M2_EINVAL and "[out, in]" in m2.last_error()
+
+
+def test_create_refuses_bad_scales_and_nulls(m2):
+    w, _keep = _weights(m2, s_w1=0.0)
+    h = ctypes.c_void_p()
+    assert m2._lib.m2_create(ctypes.byref(_cfg(m2)), ctypes.byref(w), ctypes.byref(h)) == m2.M2_EINVAL
+    w, _keep = _weights(m2, in_proj=None)
+    assert m2._lib.m2_create(ctypes.byref(_cfg(m2)), ctypes.byref(w), ctypes.byref(h)) == m2.M2_EINVAL
+    assert m2._lib.m2_create(ctypes.byref(_cfg(m2, s_x=0.0)), ctypes.byref(w), ctypes.byref(h)) == m2.M2_EINVAL
+    assert m2._lib.m2_create(ctypes.byref(_cfg(m2, chunk_size=128)), ctypes.byref(w), ctypes.byref(h)) == m2.M2_ESHAPE
+    assert m2._lib.m2_create(None, None, None) == m2.M2_EINVAL
+
+
+def test_calls_refuse_null_handle(m2):
+    assert m2._lib.m2_prefill(None, None, None, 0, None, None, None, None, None, 0, None) == m2.M2_EINVAL
+    assert m2._lib.m2_decode(None, None, 1, None, None, 1, None, None, None, 0, None) == m2.M2_EINVAL
+    assert m2._lib.m2_check(None) == m2.M2_EINVAL
+    assert m2._lib.m2_set_taps(None, None) == m2.M2_EINVAL
+    m2._lib.m2_destroy(None)
+
+
+def test_standalone_ops_refuse_bad_arguments(m2):
+    assert m2._lib.fp8_quant(None, 16, 1.0, None, None) == m2.M2_EINVAL
+    assert m2._lib.fp8_quant(None, 0, 0.0, None, None) == m2.M2_EINVAL
+    assert m2._lib.fp8_linear(None, 1.0, None, 1.0, None, 4, 4, 24, None, 0, None) == m2.M2_ESHAPE
+    assert m2._lib.fp8_linear(None, 1.0, None, 1.0, None, 4, 4, 32, None, 0, None) == m2.M2_EINVAL
+    assert m2._lib.fp8_linear(16, 1.0, 16, -1.0, 16, 4, 4, 32, None, 0, None) == m2.M2_EINVAL
+    assert m2._lib.m2_rmsnorm_residual(None, None, None, 1e-5, None, 4, 12, None) == m2.M2_ESHAPE
+    n = ctypes.c_size_t()
+    assert m2._lib.fp8_linear_workspace_size(8, 8, 20, ctypes.byref(n)) == m2.M2_ESHAPE
+    assert m2._lib.fp8_linear_workspace_size(8, 10304, 2688, ctypes.byref(n)) == m2.M2_OK
