@@ -205,20 +205,13 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- ours (GPU)
 
-def run_ours(args, rank, world, local_rank):
-    import numpy as np
+def build_workload(dev):
+    """The bench workload on `dev`: one block, the 256-slot decode pool and the
+    4 x 2048 prefill inputs, resident in HBM, plus the step closures."""
     import torch
 
     import mamba2_ssm_mixer_gb300 as m2
     import synth
-
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
     Wt = synth.make_weights(0)
     w = dict(in_proj=torch.from_numpy(Wt["in_proj"]).to(dev), s_w1=Wt["s_w1"],
              out_proj=torch.from_numpy(Wt["out_proj"]).to(dev), s_w2=Wt["s_w2"],
@@ -247,6 +240,35 @@ def run_ours(args, rank, world, local_rank):
     def step():
         blk.decode(h_dec, conv_pool, ssm_pool, slots, out=out_dec, workspace=ws_dec, stream=stream)
         blk.prefill(h_pf, SEQLENS, conv_st, ssm_st, out=out_pf, workspace=ws_pf, stream=stream)
+
+    def decode():
+        blk.decode(h_dec, conv_pool, ssm_pool, slots, out=out_dec, workspace=ws_dec, stream=stream)
+
+    def prefill():
+        blk.prefill(h_pf, SEQLENS, conv_st, ssm_st, out=out_pf, workspace=ws_pf, stream=stream)
+
+    return dict(blk=blk, step=step, decode=decode, prefill=prefill, flush=flush, stream=stream, h_dec=h_dec,
+                h_pf=h_pf, out_dec=out_dec, out_pf=out_pf, h_dec_np=h_dec_np, h_pf_np=h_pf_np)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import mamba2_ssm_mixer_gb300 as m2
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    ctx = build_workload(dev)
+    blk, step, flush, stream = ctx["blk"], ctx["step"], ctx["flush"], ctx["stream"]
+    h_dec, h_pf, out_dec, out_pf = ctx["h_dec"], ctx["h_pf"], ctx["out_dec"], ctx["out_pf"]
+    h_dec_np, h_pf_np = ctx["h_dec_np"], ctx["h_pf_np"]
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -356,6 +378,33 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+def run_case(args):
+    """One kernel family at its bench-workload shape, for profiler captures
+    (ncu -k <kernel> -c <n>): --case in_proj | out_proj | decode | prefill."""
+    import torch
+
+    import mamba2_ssm_mixer_gb300 as m2
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.case in ("in_proj", "out_proj"):
+        rng = torch.Generator(device=dev)
+        rng.manual_seed(1)
+        M, N, K = (T_PF, Z, H) if args.case == "in_proj" else (T_PF, H, I)
+        a = torch.randint(0, 0x7E, (M, K), generator=rng, device=dev, dtype=torch.int32).to(torch.uint8)
+        w = torch.randint(0, 0x7E, (N, K), generator=rng, device=dev, dtype=torch.int32).to(torch.uint8)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        for _ in range(args.steps):
+            m2.fp8_linear(a, 1.0 / 64, w, 0.01, y=y)
+    else:
+        ctx = build_workload(dev)
+        for _ in range(args.steps):
+            if args.case == "decode":
+                ctx["decode"]()
+            else:
+                ctx["prefill"]()
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -363,13 +412,17 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill"], default=None,
+                    help="run one kernel family at the workload shape (for profiler captures); prints nothing")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)

@@ -252,10 +252,11 @@ m2_status fp8_linear_bf16(const uint16_t* x, float s_a, const uint8_t* w_q, floa
 
 /*
  * Between stacked blocks (pre-norm residual stack):
- *   if add != NULL:  h[t, :] = bf16(h[t, :] + add[t, :])     (in place)
- *   normed[t, :] = bf16( h[t, :] / sqrt(mean(h[t, :]^2) + eps) * w )
- * h bf16 [T, n] in/out, add bf16 [T, n] or NULL, w bf16 [n], normed bf16
- * [T, n]; all device.  n must be a multiple of 8.
+ *   if add != NULL:     h[t, :] = bf16(h[t, :] + add[t, :])     (in place)
+ *   if normed != NULL:  normed[t, :] = bf16( h[t, :] / sqrt(mean(h[t, :]^2) + eps) * w )
+ * h bf16 [T, n] in/out, add bf16 [T, n] or NULL, w bf16 [n] (may be NULL when
+ * normed is NULL), normed bf16 [T, n] or NULL; all device, 16-byte aligned.
+ * n must be a multiple of 8.
  */
 m2_status m2_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps,
                               uint16_t* normed, int T, int n, void* stream);

@@ -304,14 +304,51 @@ def fp8_linear_bf16(x: torch.Tensor, s_a: float, w_q: torch.Tensor, s_w: float, 
     return y
 
 
-def m2_rmsnorm_residual(h: torch.Tensor, add: torch.Tensor | None, w: torch.Tensor, eps: float,
-                        normed: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+def m2_rmsnorm_residual(h: torch.Tensor, add: torch.Tensor | None, w: torch.Tensor | None, eps: float,
+                        normed: torch.Tensor | None = None, stream=None, norm: bool = True):
+    """h += add (if given); returns rmsnorm(h) * w (or None with norm=False)."""
     T, n = h.shape
     _need(h, "h", torch.bfloat16)
     if add is not None:
         _need(add, "add", torch.bfloat16, (T, n))
-    _need(w, "w", torch.bfloat16, (n,))
-    if normed is None:
-        normed = torch.empty_like(h)
+    if norm:
+        _need(w, "w", torch.bfloat16, (n,))
+        if normed is None:
+            normed = torch.empty_like(h)
+    else:
+        normed = None
     _check(_lib.m2_rmsnorm_residual(_ptr(h), _ptr(add), _ptr(w), eps, _ptr(normed), T, n, _stream(stream)))
     return normed
+
+
+class Mamba2Stack:
+    """Pre-norm residual stack of mixer blocks: for each layer l,
+    h <- h + block_l(rmsnorm(h) * norm_w[l]).  Host-side composition of the
+    C ABI calls (one rmsnorm_residual and one block call per layer)."""
+
+    def __init__(self, blocks: list, norm_ws: list, eps: float = 1e-5):
+        assert len(blocks) == len(norm_ws) and blocks
+        self.blocks, self.norm_ws, self.eps = blocks, norm_ws, eps
+
+    def _run(self, hidden, call, stream):
+        h = hidden.clone()
+        normed = torch.empty_like(h)
+        out = torch.empty_like(h)
+        for l, blk in enumerate(self.blocks):
+            m2_rmsnorm_residual(h, out if l else None, self.norm_ws[l], self.eps, normed, stream=stream)
+            call(l, blk, normed, out)
+        m2_rmsnorm_residual(h, out, None, self.eps, stream=stream, norm=False)
+        return h
+
+    def decode(self, hidden, conv_pools, ssm_pools, slot_idx, workspace=None, stream=None):
+        ws = workspace if workspace is not None else torch.empty(
+            self.blocks[0].decode_workspace_size(hidden.shape[0]), dtype=torch.uint8, device=hidden.device)
+        return self._run(hidden, lambda l, blk, x, out: blk.decode(x, conv_pools[l], ssm_pools[l], slot_idx, out=out,
+                                                                    workspace=ws, stream=stream), stream)
+
+    def prefill(self, hidden, seqlens, conv_states, ssm_states, has_initial=None, workspace=None, stream=None):
+        ws = workspace if workspace is not None else torch.empty(
+            self.blocks[0].prefill_workspace_size(seqlens), dtype=torch.uint8, device=hidden.device)
+        return self._run(hidden, lambda l, blk, x, out: blk.prefill(x, seqlens, conv_states[l], ssm_states[l],
+                                                                     has_initial=has_initial, out=out, workspace=ws,
+                                                                     stream=stream), stream)

@@ -207,6 +207,18 @@ __global__ void __launch_bounds__(256) k_rmsnorm_residual(uint16_t* __restrict__
   uint16_t* hr = h + (size_t)t * n;
   const int nv = n / 8;
   float ss = 0.f;
+  if (!normed) {   // residual add only
+    for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+      uint4 hv = reinterpret_cast<uint4*>(hr)[v];
+      uint16_t* hb = reinterpret_cast<uint16_t*>(&hv);
+      uint4 av = reinterpret_cast<const uint4*>(add + (size_t)t * n)[v];
+      const uint16_t* ab = reinterpret_cast<const uint16_t*>(&av);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) hb[e] = f2bfbits(bfbits2f(hb[e]) + bfbits2f(ab[e]));
+      reinterpret_cast<uint4*>(hr)[v] = hv;
+    }
+    return;
+  }
   for (int v = threadIdx.x; v < nv; v += blockDim.x) {
     uint4 hv = reinterpret_cast<uint4*>(hr)[v];
     uint16_t* hb = reinterpret_cast<uint16_t*>(&hv);

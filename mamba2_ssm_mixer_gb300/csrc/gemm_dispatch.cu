@@ -1,19 +1,24 @@
-// Chooses the GEMM kernel for a W8A8 problem.
+// Chooses the W8A8 GEMM kernel for a problem shape: the tensor-core skinny
+// split-K kernel for up to 256 activation rows (decode), the persistent
+// tensor-core kernel above that (prefill).
 #include "gemm.h"
 #include "m2_kernels.h"
 
 namespace m2 {
 
 size_t gemm_workspace_bytes(int M, int N, int K) {
-  (void)M; (void)N; (void)K;
+  if (M <= 0) return 0;
+  if (M <= kSkinnyMaxRows) return gemm_tc_skinny_workspace(M, N, K);
   return 0;
 }
 
 cudaError_t gemm_fp8(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, void* ws,
-                     size_t ws_bytes, cudaStream_t st, int* launches) {
-  (void)ws; (void)ws_bytes;
-  *launches = (M > 0) ? 1 : 0;
-  return launch_gemm_fp8_simt(A, B, y, M, N, K, scale, st);
+                     size_t ws_bytes, int* err, cudaStream_t st, int* launches) {
+  *launches = 0;
+  if (M <= 0) return cudaSuccess;
+  if (M <= kSkinnyMaxRows) return gemm_tc_skinny(A, B, y, M, N, K, scale, ws, ws_bytes, err, st, launches);
+  *launches = 1;
+  return gemm_tc_big(A, B, y, M, N, K, scale, err, st);
 }
 
 }  // namespace m2

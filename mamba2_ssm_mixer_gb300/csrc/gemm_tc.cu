@@ -1,0 +1,533 @@
+// Tensor-core W8A8 GEMMs for sm_103a: y = bf16(scale * A . B^T) with e4m3
+// operands stored K-major ([rows, K] row-major), f32 accumulation in TMEM.
+//
+// k_gemm_fp8_tc  (prefill, many rows): persistent CTAs, one per SM, each
+//   walking 128 x BN output tiles.  Warp roles: warp 0 issues TMA loads of
+//   128-byte-swizzled K-slices into a STAGES-deep shared-memory ring, warp 1
+//   issues tcgen05.mma (128 x BN x 32 per instruction) into one of two TMEM
+//   accumulators, warps 2-5 drain the other accumulator (tcgen05.ld), scale,
+//   round to bf16 and store, so the epilogue of tile i overlaps the MMAs of
+//   tile i+1.
+// k_gemm_fp8_tc_skinny (decode, few rows): the weight matrix is the MMA's
+//   128-row A operand and the few activation rows are its N operand
+//   (D^T = W . X^T), with the K dimension split across CTAs so every SM
+//   streams weights; f32 partials are summed by k_splitk_reduce.
+// Every mbarrier wait is bounded: a wait that runs out raises the CTA's abort
+// flag and the device error word, the roles leave their loops, outstanding
+// copies and MMAs are drained with bounded waits, and TMEM is freed.
+#include <cudaTypedefs.h>
+
+#include "gemm.h"
+#include "m2_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace m2 {
+
+using namespace tc;
+
+namespace {
+
+constexpr int kBM = 128;        // MMA M (rows of the A operand per tile)
+constexpr int kBK = 128;        // K bytes per pipeline stage (one 128-byte swizzle row)
+constexpr int kThreads = 192;   // 6 warps: producer, MMA, 4 x epilogue
+
+struct __align__(8) Ctl {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void raise_abort(Ctl* ctl, int* err) {
+  *reinterpret_cast<volatile int*>(&ctl->abort) = 1;
+  if (err) atomicOr(err, kErrTimeout);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  return (uint32_t)f2bfbits(a) | ((uint32_t)f2bfbits(b) << 16);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Persistent prefill GEMM.
+// ---------------------------------------------------------------------------
+template <int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_fp8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  uint16_t* __restrict__ C, int M, int N, int K, float scale, int* err) {
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+  static_assert(STAGES <= 8, "STAGES");
+  constexpr uint32_t A_BYTES = kBM * kBK;
+  constexpr uint32_t B_BYTES = BN * kBK;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                 : (2 * BN <= 256) ? 256 : 512;
+  constexpr uint32_t IDESC = idesc_f32acc(kBM, BN, 0u);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  volatile int* abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + BN - 1) / BN;
+  const int num_tiles = tiles_m * tiles_n;
+  const int kblocks = (K + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->tfull[i], 1);
+      mbar_init(&ctl->tempty[i], 4 * 32);
+    }
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch(&tmA);
+    tma_prefetch(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * BN;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort)) {
+            raise_abort(ctl, err);
+            ok = false;
+            break;
+          }
+          uint8_t* sA = smem + stage * STAGE_BYTES;
+          mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
+          tma_load_2d(sA, &tmA, &ctl->full[stage], kb * kBK, m0);
+          tma_load_2d(sA + A_BYTES, &tmB, &ctl->full[stage], kb * kBK, n0);
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+      }
+      if (*abort) {
+        // let copies already in flight land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) mbar_wait(&ctl->full[s], issued_phase[s], nullptr, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, abort)) {
+          raise_abort(ctl, err);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&ctl->full[stage], phase, abort)) {
+            raise_abort(ctl, err);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+          const uint64_t adesc = desc_kmajor_sw128(a_addr);
+          const uint64_t bdesc = desc_kmajor_sw128(a_addr + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k)   // 32 e4m3 per MMA: +32 bytes = +2 in the address field
+            mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+          mma_commit(&ctl->empty[stage]);
+          if (++stage == STAGES) stage = 0, phase ^= 1u;
+        }
+        if (!ok) break;
+        mma_commit(&ctl->tfull[acc]);
+        if (++acc == 2) acc = 0, acc_phase ^= 1u;
+      }
+      if (*abort) {
+        mma_commit(&ctl->drain);
+        mbar_wait(&ctl->drain, 0, nullptr, 100000000ull);
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 own TMEM lane quarters (warp % 4)
+    const int quarter = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const bool vec_ok = (N % 8) == 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * BN;
+      if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort)) {
+        raise_abort(ctl, err);
+        break;
+      }
+      tc_fence_after();
+      const int row = m0 + quarter * 32 + lane;
+      uint16_t* crow = C + (size_t)row * N;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c), r);
+        tmem_ld_wait();
+        const int n = n0 + c;
+        if (row < M && n < N) {
+          if (vec_ok && n + 32 <= N) {
+            uint4* dst = reinterpret_cast<uint4*>(crow + n);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint4 v;
+              v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * scale, __uint_as_float(r[8 * q + 1]) * scale);
+              v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * scale, __uint_as_float(r[8 * q + 3]) * scale);
+              v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * scale, __uint_as_float(r[8 * q + 5]) * scale);
+              v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * scale, __uint_as_float(r[8 * q + 7]) * scale);
+              dst[q] = v;
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (n + j < N) crow[n + j] = f2bfbits(__uint_as_float(r[j]) * scale);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&ctl->tempty[acc]);
+      if (++acc == 2) acc = 0, acc_phase ^= 1u;
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Skinny (few-row) GEMM, weights as the MMA's A operand, split over K.
+//   D^T[n, m] = sum_k W[n, k] X[m, k] for one 128-row block of W and the
+//   k-blocks [kb0, kb1) of this split.  splits == 1: bf16 y[m, n] directly;
+//   else f32 partial[split][m][n].
+// ---------------------------------------------------------------------------
+template <int BNT, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_fp8_tc_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                         uint16_t* __restrict__ y, float* __restrict__ partial, int Mtok, int N, int K,
+                         int kb_per_split, float scale, int* err) {
+  static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= 256, "BNT");
+  constexpr uint32_t A_BYTES = kBM * kBK;
+  constexpr uint32_t B_BYTES = BNT * kBK;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = (BNT <= 32) ? 32 : (BNT <= 64) ? 64 : (BNT <= 128) ? 128 : 256;
+  constexpr uint32_t IDESC = idesc_f32acc(kBM, BNT, 0u);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  volatile int* abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBM;
+  const int split = blockIdx.y;
+  const int kblocks = (K + kBK - 1) / kBK;
+  const int kb0 = split * kb_per_split;
+  const int kb1 = min(kblocks, kb0 + kb_per_split);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    mbar_init(&ctl->tfull[0], 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch(&tmW);
+    tma_prefetch(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool issued[STAGES];
+      uint32_t issued_phase[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort)) {
+          raise_abort(ctl, err);
+          break;
+        }
+        uint8_t* sA = smem + stage * STAGE_BYTES;
+        mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
+        tma_load_2d(sA, &tmW, &ctl->full[stage], kb * kBK, n0);
+        tma_load_2d(sA + A_BYTES, &tmX, &ctl->full[stage], kb * kBK, 0);
+        issued[stage] = true;
+        issued_phase[stage] = phase;
+        if (++stage == STAGES) stage = 0, phase ^= 1u;
+      }
+      if (*abort)
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) mbar_wait(&ctl->full[s], issued_phase[s], nullptr, 100000000ull);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        if (!mbar_wait(&ctl->full[stage], phase, abort)) {
+          raise_abort(ctl, err);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + stage * STAGE_BYTES);
+        const uint64_t adesc = desc_kmajor_sw128(a_addr);
+        const uint64_t bdesc = desc_kmajor_sw128(a_addr + A_BYTES);
+#pragma unroll
+        for (int k = 0; k < kBK / 32; ++k)
+          mma_f8f6f4(tmem_base, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb != kb0) || (k != 0));
+        mma_commit(&ctl->empty[stage]);
+        if (++stage == STAGES) stage = 0, phase ^= 1u;
+      }
+      if (ok) {
+        mma_commit(&ctl->tfull[0]);
+      } else {
+        mma_commit(&ctl->drain);
+        mbar_wait(&ctl->drain, 0, nullptr, 100000000ull);
+      }
+    }
+  } else {
+    const int quarter = warp & 3;
+    if (kb1 > kb0 && mbar_wait(&ctl->tfull[0], 0, abort)) {
+      tc_fence_after();
+      const int n = n0 + quarter * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < BNT; c += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, r);
+        tmem_ld_wait();
+        if (n < N) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int m = c + j;
+            if (m < Mtok) {
+              const float v = __uint_as_float(r[j]);
+              if (partial)
+                partial[((size_t)split * Mtok + m) * N + n] = v;
+              else
+                y[(size_t)m * N + n] = f2bfbits(v * scale);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+    } else if (kb1 > kb0) {
+      raise_abort(ctl, err);
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// y[m, n] = bf16(scale * sum_s partial[s][m][n]); 4 columns per thread, or
+// one when the sizes or y's alignment do not allow vectors.
+__global__ void __launch_bounds__(256) k_splitk_reduce(const float* __restrict__ partial, int splits, int Mtok, int N,
+                                                       float scale, uint16_t* __restrict__ y, int vec) {
+  const size_t plane = (size_t)Mtok * N;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  if (vec) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < plane / 4; i += stride) {
+      float4 acc = reinterpret_cast<const float4*>(partial)[i];
+      for (int s = 1; s < splits; ++s) {
+        float4 v = reinterpret_cast<const float4*>(partial + s * plane)[i];
+        acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+      }
+      uint2 o;
+      o.x = pack_bf16x2(acc.x * scale, acc.y * scale);
+      o.y = pack_bf16x2(acc.z * scale, acc.w * scale);
+      reinterpret_cast<uint2*>(y)[i] = o;
+    }
+  } else {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < plane; i += stride) {
+      float acc = partial[i];
+      for (int s = 1; s < splits; ++s) acc += partial[s * plane + i];
+      y[i] = f2bfbits(acc * scale);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// Row-major [rows, K] e4m3 matrix, box of box_rows x 128 bytes, 128B swizzle.
+cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+template <class Kern>
+cudaError_t set_smem(Kern k, size_t bytes) {
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+template <int BN, int STAGES>
+cudaError_t launch_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
+                       cudaStream_t st) {
+  CUtensorMap ta, tb;
+  cudaError_t e;
+  if ((e = make_map(&ta, A, M, K, kBM)) != cudaSuccess) return e;
+  if ((e = make_map(&tb, B, N, K, BN)) != cudaSuccess) return e;
+  const size_t smem = 1024 + (size_t)STAGES * (kBM + BN) * kBK + sizeof(Ctl);
+  auto k = k_gemm_fp8_tc<BN, STAGES>;
+  if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+  const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  k<<<grid, kThreads, smem, st>>>(ta, tb, y, M, N, K, scale, err);
+  return cudaGetLastError();
+}
+
+template <int BNT, int STAGES>
+cudaError_t launch_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, float* partial, int Mtok, int N, int K,
+                          int splits, int kps, float scale, int* err, cudaStream_t st) {
+  CUtensorMap tw, tx;
+  cudaError_t e;
+  if ((e = make_map(&tw, W, N, K, kBM)) != cudaSuccess) return e;
+  if ((e = make_map(&tx, X, Mtok, K, BNT)) != cudaSuccess) return e;
+  const size_t smem = 1024 + (size_t)STAGES * (kBM + BNT) * kBK + sizeof(Ctl);
+  auto k = k_gemm_fp8_tc_skinny<BNT, STAGES>;
+  if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+  dim3 grid((N + kBM - 1) / kBM, splits);
+  k<<<grid, kThreads, smem, st>>>(tw, tx, y, splits > 1 ? partial : nullptr, Mtok, N, K, kps, scale, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Split plan of the skinny GEMM for (Mtok, N, K): splits and k-blocks each.
+void skinny_plan(int Mtok, int N, int K, int* splits, int* kps) {
+  (void)Mtok;
+  const int kblocks = (K + kBK - 1) / kBK;
+  const int nt = (N + kBM - 1) / kBM;
+  int target = 2 * num_sms();
+  int s = (target + nt - 1) / nt;
+  if (s > kblocks) s = kblocks;
+  if (s < 1) s = 1;
+  int per = (kblocks + s - 1) / s;
+  s = (kblocks + per - 1) / per;
+  *splits = s;
+  *kps = per;
+}
+
+size_t gemm_tc_skinny_workspace(int Mtok, int N, int K) {
+  int s, kps;
+  skinny_plan(Mtok, N, K, &s, &kps);
+  return s > 1 ? (size_t)s * Mtok * N * sizeof(float) : 0;
+}
+
+cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
+                           void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches) {
+  int splits, kps;
+  skinny_plan(Mtok, N, K, &splits, &kps);
+  float* partial = static_cast<float*>(ws);
+  if (splits > 1 && (!ws || ws_bytes < (size_t)splits * Mtok * N * sizeof(float))) return cudaErrorInvalidValue;
+  const int bnt = (Mtok + 15) / 16 * 16;
+  cudaError_t e;
+  if (bnt <= 16) e = launch_skinny<16, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 32) e = launch_skinny<32, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 64) e = launch_skinny<64, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 128) e = launch_skinny<128, 6>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 256) e = launch_skinny<256, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else return cudaErrorInvalidValue;
+  if (e != cudaSuccess) return e;
+  *launches = 1;
+  if (splits > 1) {
+    const int vec = (((size_t)Mtok * N) % 4 == 0) && ((uintptr_t)y % 8 == 0) && ((uintptr_t)partial % 16 == 0);
+    const size_t items = vec ? (size_t)Mtok * N / 4 : (size_t)Mtok * N;
+    int blocks = (int)((items + 255) / 256);
+    if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
+    k_splitk_reduce<<<blocks, 256, 0, st>>>(partial, splits, Mtok, N, scale, y, vec);
+    *launches = 2;
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
+                        cudaStream_t st) {
+  // Tile width: full 256-column tiles unless a narrower tile fills the last
+  // wave better (N = 2688 = 14 x 192).
+  if (N % 192 == 0 && N % 256 != 0) return launch_big<192, 5>(A, B, y, M, N, K, scale, err, st);
+  return launch_big<256, 4>(A, B, y, M, N, K, scale, err, st);
+}
+
+}  // namespace m2

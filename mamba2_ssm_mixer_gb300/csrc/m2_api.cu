@@ -370,16 +370,18 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
 
   int nl = 0;
   M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
-  M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, st, &nl));
+  M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(w.zx, bp, conv_state, local, w.u, st));
   M2_STAGE(h, st, M2_STAGE_CONV_STATE, 1, launch_conv_state_update(w.zx, conv_state, local, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(w.zx, bp, local, w.dt, w.cum, st));
-  M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1, launch_ssd_chunk_state(w.u, w.dt, w.cum, local, w.states, st));
+  M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
+           launch_ssd_chunk_state_tc(w.u, w.dt, w.cum, local, w.states, h->err, st));
   M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1, launch_ssd_state_pass(w.states, w.cum, local, ssm_state, st));
-  M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1, launch_ssd_chunk_scan(w.u, w.dt, w.cum, w.states, bp, local, w.y, st));
+  M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
+           launch_ssd_chunk_scan_tc(w.u, w.dt, w.cum, w.states, bp, local, w.y, h->err, st));
   M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
            launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, h->taps_on ? h->taps.o : nullptr, st));
-  M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, st, &nl));
+  M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   if (h->taps_on) {
     if ((s = copy_tap(h->taps.q, w.q, (size_t)T * kH, st))) return s;
     if ((s = copy_tap(h->taps.zx, w.zx, (size_t)T * kZ * 2, st))) return s;
@@ -450,10 +452,10 @@ m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv
   }
   int nl = 0;
   M2_STAGE(h, st, M2_STAGE_DEC_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)Bt * kH, h->cfg.s_x, w.q, st));
-  M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, st, &nl));
+  M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
-           launch_decode_fused(w.zx, bp, conv_pool, ssm_pool, n_slots, slot_idx, Bt, w.q2, h->err, dt, st));
-  M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, st, &nl));
+           launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, n_slots, slot_idx, Bt, w.q2, h->err, dt, st));
+  M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   if (h->taps_on) {
     m2_status s;
     if ((s = copy_tap(h->taps.q, w.q, (size_t)Bt * kH, st))) return s;
@@ -506,7 +508,7 @@ m2_status fp8_linear(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_
   if (ws_bytes < need || (need && !workspace))
     return fail(M2_ENOMEM, "fp8_linear: workspace %zu bytes < %zu needed", ws_bytes, need);
   int nl = 0;
-  M2_CUDA(gemm_fp8(a_q, w_q, y, M, N, K, s_a * s_w, workspace, ws_bytes, static_cast<cudaStream_t>(stream), &nl));
+  M2_CUDA(gemm_fp8(a_q, w_q, y, M, N, K, s_a * s_w, workspace, ws_bytes, nullptr, static_cast<cudaStream_t>(stream), &nl));
   return M2_OK;
 }
 
@@ -523,7 +525,7 @@ m2_status fp8_linear_bf16(const uint16_t* x, float s_a, const uint8_t* w_q, floa
   uint8_t* q = static_cast<uint8_t*>(workspace);
   M2_CUDA(launch_quant_e4m3(x, (size_t)M * K, s_a, q, st));
   int nl = 0;
-  M2_CUDA(gemm_fp8(q, w_q, y, M, N, K, s_a * s_w, static_cast<char*>(workspace) + qbytes, ws_bytes - qbytes, st, &nl));
+  M2_CUDA(gemm_fp8(q, w_q, y, M, N, K, s_a * s_w, static_cast<char*>(workspace) + qbytes, ws_bytes - qbytes, nullptr, st, &nl));
   return M2_OK;
 }
 
@@ -531,7 +533,8 @@ m2_status m2_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* 
                               int n, void* stream) {
   g_err.clear();
   if (T < 0 || n < 8 || n % 8) return fail(M2_ESHAPE, "m2_rmsnorm_residual: T %d, n %d (n must be a multiple of 8)", T, n);
-  if (T && (!h || !w || !normed)) return fail(M2_EINVAL, "m2_rmsnorm_residual: null pointer");
+  if (T && (!h || (normed && !w) || (!normed && !add)))
+    return fail(M2_EINVAL, "m2_rmsnorm_residual: null pointer");
   if ((uintptr_t)h % 16 || (uintptr_t)add % 16 || (uintptr_t)w % 16 || (uintptr_t)normed % 16)
     return fail(M2_EINVAL, "m2_rmsnorm_residual: pointers must be 16-byte aligned");
   if (!(eps > 0.f)) return fail(M2_EINVAL, "m2_rmsnorm_residual: eps must be positive");

@@ -50,9 +50,20 @@ cudaError_t launch_ssd_state_pass(float* states, const float* cum, const SeqInfo
 cudaError_t launch_ssd_chunk_scan(const uint16_t* u, const float* dt, const float* cum, const float* states,
                                   const BlockParams& bp, const SeqInfo& si, uint16_t* y, cudaStream_t st);
 
+// ssd_tc.cu (tensor-core chunk states and chunk scan)
+cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const float* dt, const float* cum, const SeqInfo& si,
+                                      float* states, int* err, cudaStream_t st);
+cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const float* dt, const float* cum, const float* states,
+                                     const BlockParams& bp, const SeqInfo& si, uint16_t* y, int* err,
+                                     cudaStream_t st);
+
 // decode.cu
 cudaError_t launch_decode_fused(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,
                                 int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
                                 const DecodeTaps& taps, cudaStream_t st);
+// decode_tma.cu (persistent, TMA-streamed state)
+cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,
+                                 int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
+                                 const DecodeTaps& taps, cudaStream_t st);
 
 }  // namespace m2

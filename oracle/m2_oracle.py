@@ -209,6 +209,29 @@ def ssd_sequential(x, dt, A, B, C, D, S0):
     return y, S
 
 
+def _ssd_group_job(args):
+    return ssd_sequential(*args)
+
+
+def ssd_by_group(x, dt, A, B, C, D, S0, map_fn=map):
+    """ssd_sequential evaluated group by group: the heads of different groups
+    share nothing, so this is the same function; map_fn may be a process
+    pool's map to spread the groups over host cores."""
+    x = np.asarray(x, np.float64)
+    T, nh, P = x.shape
+    G = np.asarray(B).shape[1]
+    hpg = nh // G
+    jobs = []
+    for g in range(G):
+        hs = slice(g * hpg, (g + 1) * hpg)
+        jobs.append((x[:, hs], np.asarray(dt)[:, hs], np.asarray(A)[hs], np.asarray(B)[:, g:g + 1],
+                     np.asarray(C)[:, g:g + 1], np.asarray(D)[hs], np.asarray(S0)[hs]))
+    res = list(map_fn(_ssd_group_job, jobs))
+    y = np.concatenate([r[0] for r in res], axis=1)
+    S = np.concatenate([r[1] for r in res], axis=0)
+    return y, S
+
+
 def gated_rmsnorm_group(y, z, w, n_groups: int, eps: float):
     """RmsNormGatedGroup(n_groups).
 
@@ -241,7 +264,7 @@ def _dims(Wt):
     return g.hidden, g.d_inner, g.nheads, g.headdim, g.n_groups, g.d_state, g.conv_width
 
 
-def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False):
+def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False, map_fn=None):
     """Run the mixer block over packed sequences with carried states.
 
     hidden: [sum(T), H] bf16 values.  conv_state: [nseq, conv_dim, W-1];
@@ -249,7 +272,8 @@ def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False):
     for a fresh sequence, PR #1288 "What it does": rows are gathered and
     zeroed).  Sequences never share a chunk or a state.
     Returns dict with out [sum(T), H] (bf16 values), conv_state, ssm_state
-    (final, per sequence) and, when keep=True, the intermediates.
+    (final, per sequence) and, when keep=True, the intermediates.  map_fn, if
+    given, runs the recurrence group by group through it (ssd_by_group).
     """
     H, I, nh, P, G, N, W = _dims(Wt)
     conv_dim = I + 2 * G * N
@@ -270,9 +294,12 @@ def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False):
         sl = slice(start, start + T)
         u[sl], conv_out[s] = causal_conv1d_silu(xbc[sl], Wt["conv_w"], Wt["conv_b"], conv_state[s])
         xs, Bs, Cs = split_xbc(u[sl], I, G, N)
-        ys, ssm_out[s] = ssd_sequential(xs.reshape(T, nh, P), dt[sl], A,
-                                        Bs.reshape(T, G, N), Cs.reshape(T, G, N),
-                                        Wt["D"], ssm_state[s])
+        args = (xs.reshape(T, nh, P), dt[sl], A, Bs.reshape(T, G, N), Cs.reshape(T, G, N),
+                Wt["D"], ssm_state[s])
+        if map_fn is None:
+            ys, ssm_out[s] = ssd_sequential(*args)
+        else:
+            ys, ssm_out[s] = ssd_by_group(*args, map_fn=map_fn)
         y[sl] = bf16_round(ys.reshape(T, I))
         start += T
     o = bf16_round(gated_rmsnorm_group(y, z, Wt["norm_w"], G, Wt["eps"]))
@@ -284,7 +311,7 @@ def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False):
     return res
 
 
-def block_prefill(Wt, hidden, seqlens, conv_state=None, ssm_state=None, keep=False):
+def block_prefill(Wt, hidden, seqlens, conv_state=None, ssm_state=None, keep=False, map_fn=None):
     """Prefill of packed sequences; missing states mean fresh sequences."""
     H, I, nh, P, G, N, W = _dims(Wt)
     nseq = len(seqlens)
@@ -292,7 +319,7 @@ def block_prefill(Wt, hidden, seqlens, conv_state=None, ssm_state=None, keep=Fal
         conv_state = np.zeros((nseq, I + 2 * G * N, W - 1))
     if ssm_state is None:
         ssm_state = np.zeros((nseq, nh, P, N))
-    return block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=keep)
+    return block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=keep, map_fn=map_fn)
 
 
 def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False):
@@ -325,13 +352,15 @@ def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False):
     return res
 
 
-def stack_prefill(layers, norm_ws, hidden, seqlens, eps: float):
+def stack_prefill(layers, norm_ws, hidden, seqlens, eps: float, map_fn=None):
     """Pre-norm residual stack: h <- h + block_l(rmsnorm(h) * w_l), all bf16.
+    `layers` may be a list or a callable l -> weights (generated on demand).
     Returns (h_out, final conv states per layer, final ssm states per layer)."""
     h = np.asarray(hidden, np.float64)
     convs, ssms = [], []
-    for Wt, nw in zip(layers, norm_ws):
-        r = block_prefill(Wt, rmsnorm(h, nw, eps), seqlens)
+    for l, nw in enumerate(norm_ws):
+        Wt = layers(l) if callable(layers) else layers[l]
+        r = block_prefill(Wt, rmsnorm(h, nw, eps), seqlens, map_fn=map_fn)
         h = bf16_round(h + r["out"])
         convs.append(r["conv_state"])
         ssms.append(r["ssm_state"])

@@ -145,3 +145,14 @@ WORKLOADS = {
     3: dict(kind="prefill", seqlens=[2048] * 4, zero_state=True, chunk=256),
     4: dict(kind="stack", layers=23, batch=128, n_slots=512, seqlens=[4096, 1024, 512, 37]),
 }
+
+
+def device_normal(shape, config: int, layer: int, tensor_id: int, std: float, dtype, device):
+    """Seeded normal tensor generated on a CUDA device with PyTorch's Philox
+    generator (for state pools too large to draw on the host)."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed_for(config, layer, tensor_id))
+    t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+    if std != 1.0:
+        t.mul_(std)
+    return t.to(dtype)

@@ -15,8 +15,8 @@ HEADER = os.path.join(ROOT, "include", "m2.h")
 def m2():
     lib = os.path.join(ROOT, "mamba2_ssm_mixer_gb300", "libm2.so")
     if not os.path.exists(lib):
-        from mamba2_ssm_mixer_gb300 import _build
-        _build.build()
+        import __graft_entry__
+        __graft_entry__.build()
     import mamba2_ssm_mixer_gb300 as pkg
     return pkg
 

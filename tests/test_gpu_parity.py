@@ -13,7 +13,7 @@ import torch
 import oracle
 import synth
 from helpers import (assert_bf16_close, assert_block_out, assert_e4m3_close, assert_state, bf16_dev,
-                     device_weights, f32_dev, max_abs, rel_l2, to_np, u8_dev)
+                     device_weights, f32_dev, gemm_atol, max_abs, rel_l2, to_np, u8_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,14 +59,20 @@ def test_fp8_quant_ragged_sizes_and_offsets(n):
 # ---------------------------------------------------------------- fp8 linear
 
 def _int_codes(rng, shape, lo=-8, hi=8):
+    """Random integers in [lo, hi] and their (exact) e4m3 codes."""
     ints = rng.integers(lo, hi + 1, shape)
-    table = {v: int(oracle.e4m3_encode(np.array([float(v)]))[0]) for v in range(lo, hi + 1)}
-    return ints, np.vectorize(table.get)(ints).astype(np.uint8)
+    lut = oracle.e4m3_encode(np.arange(lo, hi + 1, dtype=np.float64))
+    return ints, lut[ints - lo]
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 10304, 2688), (64, 10304, 2688), (37, 2688, 4096), (300, 200, 160),
-                                   (128, 2688, 4096)])
+                                   (128, 2688, 4096), (256, 2688, 4096), (5, 7, 2688), (257, 300, 2688),
+                                   (1000, 2688, 4096), (8192, 10304, 2688)])
 def test_fp8_linear_integer_exact(M, N, K):
+    """Integer-valued e4m3 operands: every partial sum is an exact integer
+    below 2^24, so any summation order gives the same f32 value and the bf16
+    result must be bit-exact.  Shapes cover the skinny split-K path (M <= 256),
+    the persistent path (256- and 192-wide tiles), ragged M, N and K tails."""
     rng = np.random.default_rng(M * 7 + N)
     _, a = _int_codes(rng, (M, K))
     _, w = _int_codes(rng, (N, K))
@@ -83,7 +89,7 @@ def test_fp8_linear_random_vs_oracle(M):
     q = oracle.quant_static_e4m3(h, Wt["s_x"])
     y = to_np(m2.fp8_linear(u8_dev(q), Wt["s_x"], u8_dev(Wt["in_proj"]), Wt["s_w1"]))
     ref = oracle.fp8_linear(q, Wt["s_x"], Wt["in_proj"], Wt["s_w1"])
-    assert_bf16_close(y, ref, what="in_proj")
+    assert_bf16_close(y, ref, atol=gemm_atol(q, Wt["in_proj"], Wt["s_x"] * Wt["s_w1"]), what="in_proj")
     y2 = to_np(m2.fp8_linear_bf16(bf16_dev(h), Wt["s_x"], u8_dev(Wt["in_proj"]), Wt["s_w1"]))
     assert np.array_equal(y, y2)
 
@@ -127,15 +133,16 @@ def test_config0_prefill_32_tokens_all_stages(block0):
     out, conv, ssm, tp = _run_prefill(blk, h, [32], taps=True)
     ref = oracle.block_prefill(Wt, h, [32], keep=True)
     assert np.array_equal(to_np(tp["q"]), ref["q"])                       # bit-exact quant
-    assert_bf16_close(to_np(tp["zx"]), ref["zx"], what="zx")
-    assert_bf16_close(to_np(tp["u"]), ref["u"], what="u")
-    assert rel_l2(to_np(tp["dt"]), ref["dt"]) < 1e-5
+    assert_bf16_close(to_np(tp["zx"]), ref["zx"], atol=gemm_atol(ref["q"], Wt["in_proj"], Wt["s_x"] * Wt["s_w1"]),
+                      what="zx")
+    assert rel_l2(to_np(tp["u"]), ref["u"]) < 1e-3
+    assert rel_l2(to_np(tp["dt"]), ref["dt"]) < 1e-4
     assert rel_l2(to_np(tp["y"]), ref["y"]) < 1e-2
     assert rel_l2(to_np(tp["o"]), ref["o"]) < 1e-2
     assert_e4m3_close(to_np(tp["q2"]), ref["q2"])
     assert_block_out(to_np(out), ref["out"])
     assert_state(to_np(ssm), ref["ssm_state"])
-    assert_bf16_close(to_np(conv), ref["conv_state"], what="conv_state")
+    assert_bf16_close(to_np(conv), ref["conv_state"], atol=1e-3, what="conv_state")
 
 
 def test_prefill_integer_exact_split_and_conv_state():
@@ -158,7 +165,7 @@ def test_prefill_integer_exact_split_and_conv_state():
     assert np.array_equal(to_np(tp["q"]), ref["q"])
     assert np.array_equal(to_np(tp["zx"]), ref["zx"])
     assert np.array_equal(to_np(conv), ref["conv_state"])
-    assert_bf16_close(to_np(tp["u"]), ref["u"], what="u")
+    assert_bf16_close(to_np(tp["u"]), ref["u"], atol=1e-5, what="u")
     assert_block_out(to_np(out), ref["out"])
     blk.close()
 
@@ -177,13 +184,14 @@ def test_config1_decode_batch1(block0):
     blk.check()
     ref = oracle.block_decode(Wt, h, conv0, ssm0, np.array([0]), keep=True)
     assert np.array_equal(to_np(tp["q"]), ref["q"])
-    assert_bf16_close(to_np(tp["zx"]), ref["zx"], what="zx")
-    assert_bf16_close(to_np(tp["u"]), ref["u"], what="u")
+    assert_bf16_close(to_np(tp["zx"]), ref["zx"], atol=gemm_atol(ref["q"], Wt["in_proj"], Wt["s_x"] * Wt["s_w1"]),
+                      what="zx")
+    assert rel_l2(to_np(tp["u"]), ref["u"]) < 1e-3
     assert_block_out(to_np(out), ref["out"])
     assert_state(to_np(ssm)[0], ref["ssm_rows"][0])
     c = to_np(conv)[0]
     assert np.array_equal(c[:, :2], conv0[0][:, 1:])                      # shifted taps: exact copies
-    assert_bf16_close(c[:, 2], ref["conv_rows"][0][:, 2], what="conv tap")
+    assert_bf16_close(c[:, 2], ref["conv_rows"][0][:, 2], atol=1e-3, what="conv tap")
 
 
 def test_config2_paged_decode_batch64(block0):
@@ -206,7 +214,7 @@ def test_config2_paged_decode_batch64(block0):
     assert np.array_equal(ssm_np[untouched], ssm0[untouched])                 # byte-identical
     assert np.array_equal(conv_np[untouched], conv0[untouched])
     assert np.array_equal(conv_np[slots][:, :, :2], conv0[slots][:, :, 1:])
-    assert_bf16_close(conv_np[slots][:, :, 2], ref["conv_rows"][:, :, 2], what="conv tap")
+    assert_bf16_close(conv_np[slots][:, :, 2], ref["conv_rows"][:, :, 2], atol=1e-3, what="conv tap")
     st = blk.stats()
     assert st["state_update_rows"] >= Bt and st["decode_calls"] >= 1
 
@@ -250,7 +258,7 @@ def test_varlen_prefill_ragged_with_initial_states(block0):
     ref = oracle.block_prefill(Wt, h, lens, rng_conv * mask[:, None, None], rng_ssm * mask[:, None, None, None])
     assert_block_out(to_np(out), ref["out"])
     assert_state(to_np(ssm), ref["ssm_state"])
-    assert_bf16_close(to_np(conv), ref["conv_state"], what="conv_state")
+    assert_bf16_close(to_np(conv), ref["conv_state"], atol=1e-3, what="conv_state")
 
 
 def test_decode_after_prefill_carry(block0):
@@ -277,7 +285,7 @@ def test_config3_prefill_4x2048(block0):
     ref = oracle.block_prefill(Wt, h, lens)
     assert_block_out(to_np(out), ref["out"])
     assert_state(to_np(ssm), ref["ssm_state"])
-    assert_bf16_close(to_np(conv), ref["conv_state"], what="conv_state")
+    assert_bf16_close(to_np(conv), ref["conv_state"], atol=1e-3, what="conv_state")
 
 
 def test_rmsnorm_residual_vs_oracle():

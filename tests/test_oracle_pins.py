@@ -519,3 +519,11 @@ def test_mutation_decay_sign_is_caught():
     y_bad, _ = oracle.ssd_sequential(x, dt, -A, B, C, D, S0)
     y_ref, _ = _ssd_chunked(x, dt, A, B, C, D, S0, L=4)
     assert not np.allclose(y_bad, y_ref, rtol=1e-6)
+
+
+def test_ssd_by_group_equals_sequential():
+    rng = np.random.default_rng(26)
+    args = _ssd_inputs(rng, 13)
+    y1, S1 = oracle.ssd_sequential(*args)
+    y2, S2 = oracle.ssd_by_group(*args)
+    assert np.array_equal(y1, y2) and np.array_equal(S1, S2)
