@@ -50,7 +50,7 @@ def stage_work():
     kind 'flop' counts 2 per multiply-add; 'byte' counts each operand read or
     written once (intermediates counted where a stage must move them)."""
     T, B = T_PF, DEC_B
-    state = 64 * 64 * 128 * 4
+    state = 64 * 64 * 128 * 4          # one f32 SSM state row (all heads): 2 MiB
     return {
         "quant_in": ("byte", T * H * 3),
         "in_proj": ("flop", 2.0 * T * Z * H),
@@ -58,12 +58,12 @@ def stage_work():
         "conv_state": ("byte", 4 * CONV * 3 * 2),
         "ssd_cumsum": ("byte", T * 64 * (2 + 8)),
         "ssd_chunk_state": ("flop", 2.0 * T * 64 * 64 * 128),
-        "ssd_state_pass": ("byte", (T // 256) * 64 * state * 2 + 4 * 64 * state),
+        "ssd_state_pass": ("byte", (T // 256) * state * 2 + 4 * state),
         # causal C.B per group, (C.B o decay) x per head, C S_in per head
         "ssd_chunk_scan": ("flop", T * (8 * 257 * 128 + 64 * 257 * 64 + 64 * 2 * 64 * 128)),
         "norm_quant": ("byte", T * I * 5),
         "out_proj": ("flop", 2.0 * T * H * I),
-        "decode_fused": ("byte", B * (2 * 64 * state + 2 * CONV * 3 * 2 + Z * 2 + I)),
+        "decode_fused": ("byte", B * (2 * state + 2 * CONV * 3 * 2 + Z * 2 + I)),
         "dec_quant_in": ("byte", B * H * 3),
         "dec_in_proj": ("byte", Z * H + B * H + B * Z * 2),
         "dec_out_proj": ("byte", H * I + B * I + B * H * 2),
@@ -237,15 +237,17 @@ def build_workload(dev):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
-        blk.decode(h_dec, conv_pool, ssm_pool, slots, out=out_dec, workspace=ws_dec, stream=stream)
-        blk.prefill(h_pf, SEQLENS, conv_st, ssm_st, out=out_pf, workspace=ws_pf, stream=stream)
-
+    # the calls run on the caller's current stream (so a CUDA graph capture
+    # records them)
     def decode():
-        blk.decode(h_dec, conv_pool, ssm_pool, slots, out=out_dec, workspace=ws_dec, stream=stream)
+        blk.decode(h_dec, conv_pool, ssm_pool, slots, out=out_dec, workspace=ws_dec)
 
     def prefill():
-        blk.prefill(h_pf, SEQLENS, conv_st, ssm_st, out=out_pf, workspace=ws_pf, stream=stream)
+        blk.prefill(h_pf, SEQLENS, conv_st, ssm_st, out=out_pf, workspace=ws_pf)
+
+    def step():
+        decode()
+        prefill()
 
     return dict(blk=blk, step=step, decode=decode, prefill=prefill, flush=flush, stream=stream, h_dec=h_dec,
                 h_pf=h_pf, out_dec=out_dec, out_pf=out_pf, h_dec_np=h_dec_np, h_pf_np=h_pf_np)
@@ -276,29 +278,62 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     blk.check()
 
-    # ---- timed region: device-resident inputs
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    def timed(run, steps, profile=False):
+        """Per-step CUDA-event intervals on the current stream, L2 flushed
+        before each step outside the interval; returns mean ms per step."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        if profile:
+            blk.profile(True)
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record()
+            run()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    # ---- timed region: device-resident inputs.  Headline: the step replayed
+    # from a CUDA graph (how a serving loop runs it); also timed eagerly.
+    graph = None
+    try:
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            step()                       # one eager step on the capture stream first
+        torch.cuda.current_stream(dev).wait_stream(cs)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cs):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+    except Exception as exc:  # pragma: no cover - reported in the JSON line
+        graph = None
+        graph_error = f"{type(exc).__name__}: {exc}"
     sampler = ClockSampler(local_rank)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
     launches0 = blk.stats()["kernel_launches"]
-    blk.profile(True)
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
+    ms_eager = timed(step, args.steps)
+    launches_per_step = (blk.stats()["kernel_launches"] - launches0) / args.steps
+    ms_graph = timed(graph.replay, args.steps) if graph is not None else None
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clocks = sampler.stop()
+    blk.check()
+    # per-stage times (events between kernels; a separate pass so the
+    # brackets do not perturb the headline numbers)
+    timed(step, args.steps, profile=True)
     prof = blk.profile_read()
     blk.profile(False)
-    launches = blk.stats()["kernel_launches"] - launches0
     blk.check()
-    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    ms = ms_graph if ms_graph is not None else ms_eager
+    launches = int(round(launches_per_step * args.steps))
     if dist:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -312,13 +347,13 @@ def run_ours(args, rank, world, local_rank):
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
-        e2e_ev[i][0].record(stream)
+        e2e_ev[i][0].record()
         h_dec.copy_(hd_pin, non_blocking=True)
         h_pf.copy_(hp_pin, non_blocking=True)
         step()
         od_pin.copy_(out_dec, non_blocking=True)
         op_pin.copy_(out_pf, non_blocking=True)
-        e2e_ev[i][1].record(stream)
+        e2e_ev[i][1].record()
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
     if dist:
@@ -366,7 +401,16 @@ def run_ours(args, rank, world, local_rank):
                 data="synthetic",
                 config=dict(workload=WORKLOAD, tokens_per_step=TOKENS_PER_STEP, decode_rows=DEC_B,
                             prefill_tokens=T_PF, l2="flushed before each step (256 MiB write), outside the interval",
-                            parallelism="replicas" if world > 1 else "single GPU"),
+                            parallelism="replicas" if world > 1 else "single GPU",
+                            launch="cuda_graph" if ms_graph is not None else "eager",
+                            ms_per_step_eager=ms_eager, ms_per_step_graph=ms_graph,
+                            decode_stage_ms=sum(v[0] for k, v in prof.items()
+                                                if k in ("dec_quant_in", "dec_in_proj", "decode_fused",
+                                                         "dec_out_proj")) / args.steps,
+                            prefill_stage_ms=sum(v[0] for k, v in prof.items()
+                                                 if k not in ("dec_quant_in", "dec_in_proj", "decode_fused",
+                                                              "dec_out_proj")) / args.steps,
+                            graph_error=None if graph is not None else graph_error),
                 clocks=clocks,
                 e2e=dict(value=TOKENS_PER_STEP * world / (e2e_ms * 1e-3), unit="tokens/s",
                          h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),

@@ -3,7 +3,8 @@
 // from and written back to pool[slot] in place, y = S C + D x, gated group
 // RMSNorm and e4m3 quant), organised for HBM bandwidth:
 //
-//  - persistent CTAs (one per SM) walk the (row, group) work items;
+//  - persistent CTAs (two per SM, so one streams while the other is in its
+//    conv or norm phase) walk the (row, group) work items;
 //  - a producer thread streams every head's f32 state (64 x 128 = 32 KB,
 //    contiguous in the pool) into a shared-memory ring with cp.async.bulk
 //    (TMA, 1-D) several heads ahead, so loads are always in flight;
@@ -16,6 +17,7 @@
 // bounded; a wait that runs out sets the device error word and the CTA stops
 // issuing work, drains its copies and returns.
 #include "m2_kernels.h"
+#include "launch_util.h"
 #include "tc_ptx.cuh"
 
 namespace m2 {
@@ -24,7 +26,7 @@ using namespace tc;
 
 namespace {
 
-constexpr int kStages = 5;                  // 5 x 32 KB ring
+constexpr int kStages = 3;                  // 3 x 32 KB ring per CTA, 2 CTAs per SM
 constexpr int kHeadBytes = kP * kN * 4;     // 32768
 constexpr int kConsumers = 256;             // 8 warps
 constexpr int kThreadsT = kConsumers + 32;  // + producer warp
@@ -46,7 +48,7 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
 struct __align__(16) Smem {
-  float state[kStages][kP * kN];   // 160 KB ring
+  float state[kStages][kP * kN];   // 96 KB ring
   float ux[kGroupCh];
   float4 ub[kN / 4];
   float4 uc[kN / 4];
@@ -59,7 +61,7 @@ struct __align__(16) Smem {
 
 }  // namespace
 
-__global__ void __launch_bounds__(kThreadsT, 1)
+__global__ void __launch_bounds__(kThreadsT, 2)
     k_decode_stream(const uint16_t* __restrict__ zx, const uint16_t* __restrict__ conv_w,
                     const uint16_t* __restrict__ conv_b, const float* __restrict__ A_log, const float* __restrict__ Dp,
                     const float* __restrict__ dt_bias, const uint16_t* __restrict__ norm_w, float eps, float s_y,
@@ -81,6 +83,8 @@ __global__ void __launch_bounds__(kThreadsT, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_trigger();
 
   if (warp == kConsumers / 32) {
     // ------------------------------------------------ producer warp
@@ -256,21 +260,14 @@ __global__ void __launch_bounds__(kThreadsT, 1)
 cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,
                                  int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
                                  const DecodeTaps& taps, cudaStream_t st) {
-  static int sms = 0;
-  if (!sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaError_t e = cudaFuncSetAttribute(k_decode_stream, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(sizeof(Smem) + 128));
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k_decode_stream), (int)(sizeof(Smem) + 128));
+  if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
   const int items = Bt * kG;
-  const int grid = items < sms ? items : sms;
-  k_decode_stream<<<grid, kThreadsT, sizeof(Smem) + 128, st>>>(zx, bp.conv_w, bp.conv_b, bp.A_log, bp.D, bp.dt_bias,
-                                                              bp.norm_w, bp.eps, bp.s_y, conv_pool, ssm_pool, n_slots,
-                                                              slot_idx, Bt, q2, err, taps);
-  return cudaGetLastError();
+  const int grid = items < 2 * sms ? items : 2 * sms;
+  return launch_pdl(k_decode_stream, dim3(grid), dim3(kThreadsT), sizeof(Smem) + 128, st, zx, bp.conv_w, bp.conv_b,
+                    bp.A_log, bp.D, bp.dt_bias, bp.norm_w, bp.eps, bp.s_y, conv_pool, ssm_pool, n_slots, slot_idx, Bt,
+                    q2, err, taps);
 }
 
 }  // namespace m2

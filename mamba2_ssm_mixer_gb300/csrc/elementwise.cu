@@ -2,6 +2,7 @@
 // causal conv1d + SiLU (prefill) and its state hand-off, gated group RMSNorm
 // with the out_proj quant fused into its epilogue, and the residual RMSNorm
 // used between stacked blocks.
+#include "launch_util.h"
 #include "m2_kernels.h"
 
 namespace m2 {
@@ -13,6 +14,8 @@ namespace m2 {
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_quant_e4m3_vec(const uint4* __restrict__ x, size_t nvec, float scale,
                                                         uint2* __restrict__ q) {
+  pdl_wait();
+  pdl_trigger();
   size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
     uint4 v = x[i];
@@ -30,6 +33,8 @@ __global__ void __launch_bounds__(256) k_quant_e4m3_vec(const uint4* __restrict_
 
 __global__ void k_quant_e4m3_scalar(const uint16_t* __restrict__ x, size_t begin, size_t n, float scale,
                                     uint8_t* __restrict__ q) {
+  pdl_wait();
+  pdl_trigger();
   size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = begin + (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride)
     q[i] = quant_e4m3(bfbits2f(x[i]), scale);
@@ -42,14 +47,16 @@ cudaError_t launch_quant_e4m3(const uint16_t* x, size_t n, float scale, uint8_t*
   if (nvec) {
     size_t blocks = (nvec + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    k_quant_e4m3_vec<<<(unsigned)blocks, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), nvec, scale,
-                                                         reinterpret_cast<uint2*>(q));
+    cudaError_t e = launch_pdl(k_quant_e4m3_vec, dim3((unsigned)blocks), dim3(256), 0, st,
+                               reinterpret_cast<const uint4*>(x), nvec, scale, reinterpret_cast<uint2*>(q));
+    if (e != cudaSuccess) return e;
   }
   size_t rest = n - nvec * 8;
   if (rest) {
     size_t blocks = (rest + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
-    k_quant_e4m3_scalar<<<(unsigned)blocks, 256, 0, st>>>(x, nvec * 8, n, scale, q);
+    cudaError_t e = launch_pdl(k_quant_e4m3_scalar, dim3((unsigned)blocks), dim3(256), 0, st, x, nvec * 8, n, scale, q);
+    if (e != cudaSuccess) return e;
   }
   return cudaGetLastError();
 }
@@ -60,43 +67,78 @@ cudaError_t launch_quant_e4m3(const uint16_t* x, size_t n, float scale, uint8_t*
 // read in place from the in_proj row (the split is addressing).  Taps before a
 // sequence's first token come from conv_state (has_initial) or are zero.
 //   u[t, c] = bf16(silu(b[c] + sum_j w[c, j] * x[t - 3 + j, c]))
-// One thread per (token, channel pair).
+// One thread per channel pair and 16 consecutive tokens, the 3 previous
+// inputs kept in registers (a sliding window reset at sequence starts).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_conv_silu_prefill(const uint16_t* __restrict__ zx,
+constexpr int kConvTokens = 16;
+
+__device__ __forceinline__ float2 ld_bf2(const uint16_t* p) {
+  const uint32_t v = *reinterpret_cast<const uint32_t*>(p);
+  return make_float2(bfbits2f((uint16_t)(v & 0xFFFFu)), bfbits2f((uint16_t)(v >> 16)));
+}
+
+__global__ void __launch_bounds__(128) k_conv_silu_prefill(const uint16_t* __restrict__ zx,
                                                            const uint16_t* __restrict__ conv_w,
                                                            const uint16_t* __restrict__ conv_b,
                                                            const uint16_t* __restrict__ conv_state,
                                                            const SeqInfo si, uint16_t* __restrict__ u) {
-  const int t = blockIdx.y;
+  pdl_wait();
+  pdl_trigger();
   const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
-  if (c >= kConv || t >= si.total_tokens) return;
-  const int s = seq_of_token(si, t);
-  const int tl = t - si.cu_seqlens[s];
-  const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
-  float xv[2][kW];
-#pragma unroll
-  for (int j = 0; j < kW; ++j) {
-    int tt = tl - (kW - 1) + j;   // local time of tap j
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float v = 0.f;
-      if (tt >= 0) {
-        v = bfbits2f(zx[(size_t)(t - (kW - 1) + j) * kZ + kOffXBC + c + e]);
-      } else if (init) {
-        v = bfbits2f(conv_state[((size_t)s * kConv + c + e) * (kW - 1) + (kW - 1) + tt]);
-      }
-      xv[e][j] = v;
-    }
-  }
-  uint32_t packed = 0;
+  const int t_begin = blockIdx.y * kConvTokens;
+  if (c >= kConv || t_begin >= si.total_tokens) return;
+  const int t_end = min(t_begin + kConvTokens, si.total_tokens);
+  float w[2][kW], bias[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
-    float acc = conv_b ? bfbits2f(conv_b[c + e]) : 0.f;
+    bias[e] = conv_b ? bfbits2f(conv_b[c + e]) : 0.f;
 #pragma unroll
-    for (int j = 0; j < kW; ++j) acc = fmaf(bfbits2f(conv_w[(c + e) * kW + j]), xv[e][j], acc);
-    packed |= (uint32_t)f2bfbits(silu_f(acc)) << (16 * e);
+    for (int j = 0; j < kW; ++j) w[e][j] = bfbits2f(conv_w[(c + e) * kW + j]);
   }
-  *reinterpret_cast<uint32_t*>(u + (size_t)t * kConv + c) = packed;
+  int s = seq_of_token(si, t_begin);
+  int seq_start = si.cu_seqlens[s], seq_end = si.cu_seqlens[s + 1];
+  // window[k] = input at time t - 3 + k (k = 0, 1, 2) for the next token t
+  float2 win[kW - 1];
+  auto load_window = [&](int t) {
+    const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
+#pragma unroll
+    for (int k = 0; k < kW - 1; ++k) {
+      const int tt = t - (kW - 1) + k;
+      if (tt >= seq_start) {
+        win[k] = ld_bf2(zx + (size_t)tt * kZ + kOffXBC + c);
+      } else if (init) {
+        const int tap = (kW - 1) + (tt - seq_start);   // 0..2
+        const uint16_t* st = conv_state + ((size_t)s * kConv + c) * (kW - 1);
+        win[k] = make_float2(bfbits2f(st[tap]), bfbits2f(st[(kW - 1) + tap]));
+      } else {
+        win[k] = make_float2(0.f, 0.f);
+      }
+    }
+  };
+  load_window(t_begin);
+  for (int t = t_begin; t < t_end; ++t) {
+    if (t == seq_end) {   // first token of the next sequence
+      ++s;
+      seq_start = seq_end;
+      seq_end = si.cu_seqlens[s + 1];
+      load_window(t);
+    }
+    const float2 x = ld_bf2(zx + (size_t)t * kZ + kOffXBC + c);
+    float a0 = bias[0], a1 = bias[1];
+    a0 = fmaf(w[0][0], win[0].x, a0);
+    a1 = fmaf(w[1][0], win[0].y, a1);
+    a0 = fmaf(w[0][1], win[1].x, a0);
+    a1 = fmaf(w[1][1], win[1].y, a1);
+    a0 = fmaf(w[0][2], win[2].x, a0);
+    a1 = fmaf(w[1][2], win[2].y, a1);
+    a0 = fmaf(w[0][3], x.x, a0);
+    a1 = fmaf(w[1][3], x.y, a1);
+    *reinterpret_cast<uint32_t*>(u + (size_t)t * kConv + c) =
+        (uint32_t)f2bfbits(silu_f(a0)) | ((uint32_t)f2bfbits(silu_f(a1)) << 16);
+    win[0] = win[1];
+    win[1] = win[2];
+    win[2] = x;
+  }
 }
 
 // New conv window of each sequence: the last 3 raw xBC inputs of
@@ -104,6 +146,8 @@ __global__ void __launch_bounds__(256) k_conv_silu_prefill(const uint16_t* __res
 // state never race with this write; one thread owns one channel's 3 taps.
 __global__ void __launch_bounds__(256) k_conv_state_update(const uint16_t* __restrict__ zx,
                                                            uint16_t* __restrict__ conv_state, const SeqInfo si) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.y;
   const int c = blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= kConv) return;
@@ -126,16 +170,14 @@ __global__ void __launch_bounds__(256) k_conv_state_update(const uint16_t* __res
 
 cudaError_t launch_conv_silu_prefill(const uint16_t* zx, const BlockParams& bp, const uint16_t* conv_state,
                                      const SeqInfo& si, uint16_t* u, cudaStream_t st) {
-  dim3 grid((kConv / 2 + 255) / 256, si.total_tokens);
-  k_conv_silu_prefill<<<grid, 256, 0, st>>>(zx, bp.conv_w, bp.conv_b, conv_state, si, u);
-  return cudaGetLastError();
+  dim3 grid((kConv / 2 + 127) / 128, (si.total_tokens + kConvTokens - 1) / kConvTokens);
+  return launch_pdl(k_conv_silu_prefill, grid, dim3(128), 0, st, zx, bp.conv_w, bp.conv_b, conv_state, si, u);
 }
 
 cudaError_t launch_conv_state_update(const uint16_t* zx, uint16_t* conv_state, const SeqInfo& si,
                                      cudaStream_t st) {
   dim3 grid((kConv + 255) / 256, si.nseq);
-  k_conv_state_update<<<grid, 256, 0, st>>>(zx, conv_state, si);
-  return cudaGetLastError();
+  return launch_pdl(k_conv_state_update, grid, dim3(256), 0, st, zx, conv_state, si);
 }
 
 // ---------------------------------------------------------------------------
@@ -143,57 +185,54 @@ cudaError_t launch_conv_state_update(const uint16_t* zx, uint16_t* conv_state, c
 // out_proj activation quant in its epilogue:
 //   g = y * silu(z);  o = bf16(g / sqrt(mean_group(g^2) + eps) * w);
 //   q2 = e4m3(o / s_y)
-// One CTA of 128 threads per (token, group of 512 channels), 4 per thread.
+// One CTA of 8 warps per token; warp g owns group g (512 channels, 16 per
+// lane), so the group reduction is a warp shuffle.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ float block_sum_128(float v, float* red) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float s = red[0] + red[1] + red[2] + red[3];
-  return s;
-}
-
-__global__ void __launch_bounds__(128) k_gated_norm_quant(const uint16_t* __restrict__ y,
+__global__ void __launch_bounds__(256) k_gated_norm_quant(const uint16_t* __restrict__ y,
                                                           const uint16_t* __restrict__ zx,
                                                           const uint16_t* __restrict__ norm_w, float eps,
                                                           float s_y, uint8_t* __restrict__ q2,
                                                           uint16_t* __restrict__ o_tap) {
-  __shared__ float red[4];
-  const int t = blockIdx.x, g = blockIdx.y;
-  const int c = g * kGroupCh + threadIdx.x * 4;
-  uint2 yv = *reinterpret_cast<const uint2*>(y + (size_t)t * kI + c);
-  uint2 zv = *reinterpret_cast<const uint2*>(zx + (size_t)t * kZ + c);
-  uint2 wv = *reinterpret_cast<const uint2*>(norm_w + c);
-  const uint16_t* yb = reinterpret_cast<const uint16_t*>(&yv);
-  const uint16_t* zb = reinterpret_cast<const uint16_t*>(&zv);
-  const uint16_t* wb = reinterpret_cast<const uint16_t*>(&wv);
-  float gv[4];
+  pdl_wait();
+  pdl_trigger();
+  const int t = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = g * kGroupCh + lane * 16;
+  const uint4* yp = reinterpret_cast<const uint4*>(y + (size_t)t * kI + c);
+  const uint4* zp = reinterpret_cast<const uint4*>(zx + (size_t)t * kZ + c);
+  const uint4* wp = reinterpret_cast<const uint4*>(norm_w + c);
+  uint4 yv[2] = {yp[0], yp[1]}, zv[2] = {zp[0], zp[1]}, wv[2] = {wp[0], wp[1]};
+  const uint16_t* yb = reinterpret_cast<const uint16_t*>(yv);
+  const uint16_t* zb = reinterpret_cast<const uint16_t*>(zv);
+  const uint16_t* wb = reinterpret_cast<const uint16_t*>(wv);
+  float gv[16];
   float ss = 0.f;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < 16; ++e) {
     gv[e] = bfbits2f(yb[e]) * silu_f(bfbits2f(zb[e]));
     ss = fmaf(gv[e], gv[e], ss);
   }
-  ss = block_sum_128(ss, red);
-  const float r = 1.0f / sqrtf(ss / (float)kGroupCh + eps);
-  uint32_t qq = 0;
-  uint16_t ob[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float r = 1.0f / sqrtf(ss / (float)kGroupCh + eps);
+  uint32_t qq[4] = {0u, 0u, 0u, 0u};
+  uint16_t ob[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
     ob[e] = f2bfbits(gv[e] * r * bfbits2f(wb[e]));
-    qq |= (uint32_t)quant_e4m3(bfbits2f(ob[e]), s_y) << (8 * e);
+    qq[e >> 2] |= (uint32_t)quant_e4m3(bfbits2f(ob[e]), s_y) << (8 * (e & 3));
   }
-  *reinterpret_cast<uint32_t*>(q2 + (size_t)t * kI + c) = qq;
-  if (o_tap) *reinterpret_cast<uint2*>(o_tap + (size_t)t * kI + c) = *reinterpret_cast<uint2*>(ob);
+  *reinterpret_cast<uint4*>(q2 + (size_t)t * kI + c) = make_uint4(qq[0], qq[1], qq[2], qq[3]);
+  if (o_tap) {
+    uint4* op = reinterpret_cast<uint4*>(o_tap + (size_t)t * kI + c);
+    op[0] = reinterpret_cast<const uint4*>(ob)[0];
+    op[1] = reinterpret_cast<const uint4*>(ob)[1];
+  }
 }
 
 cudaError_t launch_gated_norm_quant(const uint16_t* y, const uint16_t* zx, const BlockParams& bp, int T,
                                     uint8_t* q2, uint16_t* o_tap, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  dim3 grid(T, kG);
-  k_gated_norm_quant<<<grid, 128, 0, st>>>(y, zx, bp.norm_w, bp.eps, bp.s_y, q2, o_tap);
-  return cudaGetLastError();
+  return launch_pdl(k_gated_norm_quant, dim3(T), dim3(256), 0, st, y, zx, bp.norm_w, bp.eps, bp.s_y, q2, o_tap);
 }
 
 // ---------------------------------------------------------------------------
@@ -203,6 +242,8 @@ __global__ void __launch_bounds__(256) k_rmsnorm_residual(uint16_t* __restrict__
                                                           const uint16_t* __restrict__ w, float eps,
                                                           uint16_t* __restrict__ normed, int n) {
   __shared__ float red[8];
+  pdl_wait();
+  pdl_trigger();
   const int t = blockIdx.x;
   uint16_t* hr = h + (size_t)t * n;
   const int nv = n / 8;
@@ -255,8 +296,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_residual(uint16_t* __restrict__
 cudaError_t launch_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps,
                                     uint16_t* normed, int T, int n, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  k_rmsnorm_residual<<<T, 256, 0, st>>>(h, add, w, eps, normed, n);
-  return cudaGetLastError();
+  return launch_pdl(k_rmsnorm_residual, dim3(T), dim3(256), 0, st, h, add, w, eps, normed, n);
 }
 
 }  // namespace m2

@@ -18,6 +18,7 @@
 #include <cudaTypedefs.h>
 
 #include "gemm.h"
+#include "launch_util.h"
 #include "m2_common.cuh"
 #include "tc_ptx.cuh"
 
@@ -100,6 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  pdl_wait();      // operands are produced by the previous kernel
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -275,6 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
+  pdl_wait();      // operands are produced by the previous kernel
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -369,6 +374,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // one when the sizes or y's alignment do not allow vectors.
 __global__ void __launch_bounds__(256) k_splitk_reduce(const float* __restrict__ partial, int splits, int Mtok, int N,
                                                        float scale, uint16_t* __restrict__ y, int vec) {
+  pdl_wait();
+  pdl_trigger();
   const size_t plane = (size_t)Mtok * N;
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   if (vec) {
@@ -424,20 +431,11 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K, int bo
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-int num_sms() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
-  return n;
-}
+int num_sms() { return device_sm_count(); }
 
 template <class Kern>
 cudaError_t set_smem(Kern k, size_t bytes) {
-  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  return ensure_smem_optin(reinterpret_cast<const void*>(k), (int)bytes);
 }
 
 template <int BN, int STAGES>
@@ -452,8 +450,7 @@ cudaError_t launch_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, i
   if ((e = set_smem(k, smem)) != cudaSuccess) return e;
   const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  k<<<grid, kThreads, smem, st>>>(ta, tb, y, M, N, K, scale, err);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, ta, tb, y, M, N, K, scale, err);
 }
 
 template <int BNT, int STAGES>
@@ -467,8 +464,8 @@ cudaError_t launch_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, float
   auto k = k_gemm_fp8_tc_skinny<BNT, STAGES>;
   if ((e = set_smem(k, smem)) != cudaSuccess) return e;
   dim3 grid((N + kBM - 1) / kBM, splits);
-  k<<<grid, kThreads, smem, st>>>(tw, tx, y, splits > 1 ? partial : nullptr, Mtok, N, K, kps, scale, err);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, dim3(kThreads), smem, st, tw, tx, y, splits > 1 ? partial : nullptr, Mtok, N, K, kps,
+                    scale, err);
 }
 
 }  // namespace
@@ -515,9 +512,9 @@ cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int 
     const size_t items = vec ? (size_t)Mtok * N / 4 : (size_t)Mtok * N;
     int blocks = (int)((items + 255) / 256);
     if (blocks > 4 * num_sms()) blocks = 4 * num_sms();
-    k_splitk_reduce<<<blocks, 256, 0, st>>>(partial, splits, Mtok, N, scale, y, vec);
+    e = launch_pdl(k_splitk_reduce, dim3(blocks), dim3(256), 0, st, (const float*)partial, splits, Mtok, N, scale,
+                   y, vec);
     *launches = 2;
-    e = cudaGetLastError();
   }
   return e;
 }

@@ -88,3 +88,10 @@ __device__ __forceinline__ int seq_of_token(const SeqInfo& si, int t) {
 }
 
 }  // namespace m2
+
+namespace m2 {
+// Programmatic dependent launch: wait for the previous kernel on the stream
+// (no-op when launched without the attribute) / let the next one start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+}  // namespace m2

