@@ -1,4 +1,4 @@
-// Paged decode, streaming version.  Same mathematics as k_decode_fused (conv
+// Paged decode of the mixer block (conv
 // window update + SiLU, dt, the single-step state update of each head read
 // from and written back to pool[slot] in place, y = S C + D x, gated group
 // RMSNorm and e4m3 quant), organised for HBM bandwidth:

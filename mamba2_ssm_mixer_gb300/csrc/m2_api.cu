@@ -306,7 +306,7 @@ struct PrefillWs {
   uint16_t* zx;
   uint16_t* u;
   float* dt;
-  float* cum;
+  float2* cum;
   float* states;
   uint16_t* y;
   uint8_t* q2;
@@ -322,7 +322,7 @@ static PrefillWs carve_prefill(void* base, int T, int chunks) {
   w.zx = c.take<uint16_t>((size_t)T * kZ);
   w.u = c.take<uint16_t>((size_t)T * kConv);
   w.dt = c.take<float>((size_t)T * kNH);
-  w.cum = c.take<float>((size_t)T * kNH);
+  w.cum = c.take<float2>((size_t)T * kNH);
   w.states = c.take<float>((size_t)chunks * kNH * kP * kN);
   w.y = c.take<uint16_t>((size_t)T * kI);
   w.q2 = c.take<uint8_t>((size_t)T * kI);

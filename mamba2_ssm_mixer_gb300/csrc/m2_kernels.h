@@ -36,31 +36,20 @@ cudaError_t launch_gated_norm_quant(const uint16_t* y, const uint16_t* zx, const
 cudaError_t launch_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps,
                                     uint16_t* normed, int T, int n, cudaStream_t st);
 
-// gemm_simt.cu: y[M,N] = bf16(scale * A[M,K] . B[N,K]^T), e4m3 operands
-cudaError_t launch_gemm_fp8_simt(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K,
-                                 float scale, cudaStream_t st);
-
 // ssd.cu
-cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, float* dt, float* cum,
+// cum: the in-chunk cumulative log-decay as (hi, lo) float pairs.
+cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, float* dt, float2* cum,
                               cudaStream_t st);
-cudaError_t launch_ssd_chunk_state(const uint16_t* u, const float* dt, const float* cum, const SeqInfo& si,
-                                   float* states, cudaStream_t st);
-cudaError_t launch_ssd_state_pass(float* states, const float* cum, const SeqInfo& si, float* ssm_state,
+cudaError_t launch_ssd_state_pass(float* states, const float2* cum, const SeqInfo& si, float* ssm_state,
                                   cudaStream_t st);
-cudaError_t launch_ssd_chunk_scan(const uint16_t* u, const float* dt, const float* cum, const float* states,
-                                  const BlockParams& bp, const SeqInfo& si, uint16_t* y, cudaStream_t st);
 
 // ssd_tc.cu (tensor-core chunk states and chunk scan)
-cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const float* dt, const float* cum, const SeqInfo& si,
+cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const float* dt, const float2* cum, const SeqInfo& si,
                                       float* states, int* err, cudaStream_t st);
-cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const float* dt, const float* cum, const float* states,
+cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const float* dt, const float2* cum, const float* states,
                                      const BlockParams& bp, const SeqInfo& si, uint16_t* y, int* err,
                                      cudaStream_t st);
 
-// decode.cu
-cudaError_t launch_decode_fused(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,
-                                int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
-                                const DecodeTaps& taps, cudaStream_t st);
 // decode_tma.cu (persistent, TMA-streamed state)
 cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,
                                  int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,

@@ -80,7 +80,7 @@ __device__ __forceinline__ bool wait_or_flag(uint64_t* bar, uint32_t parity, int
 // chunk states
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThr, 1)
-    k_ssd_state_tc(const uint16_t* __restrict__ u, const float* __restrict__ dt, const float* __restrict__ cum,
+    k_ssd_state_tc(const uint16_t* __restrict__ u, const float* __restrict__ dt, const float2* __restrict__ cum,
                    const SeqInfo si, float* __restrict__ states, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -126,9 +126,15 @@ __global__ void __launch_bounds__(kThr, 1)
 
   for (int hh = 0; hh < kHPG; ++hh) {
     const int h = g * kHPG + hh;
-    const float cl = cum[(size_t)(cp.t0 + cp.n - 1) * kNH + h];
-    for (int t = tid; t < kChunk; t += kThr)
-      wts[t] = t < cp.n ? expf(cl - cum[(size_t)(cp.t0 + t) * kNH + h]) * dt[(size_t)(cp.t0 + t) * kNH + h] : 0.f;
+    const float2 cl = cum[(size_t)(cp.t0 + cp.n - 1) * kNH + h];
+    for (int t = tid; t < kChunk; t += kThr) {
+      float w = 0.f;
+      if (t < cp.n) {
+        const float2 ct = cum[(size_t)(cp.t0 + t) * kNH + h];
+        w = expf((cl.x - ct.x) + (cl.y - ct.y)) * dt[(size_t)(cp.t0 + t) * kNH + h];
+      }
+      wts[t] = w;
+    }
     __syncthreads();
     // (w x)^T split into hi + lo: rows p, K = t.  32 (t) x 8 (p) blocks.
     for (int blk = tid; blk < 256; blk += kThr) {
@@ -208,7 +214,7 @@ __device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) 
 }
 
 __global__ void __launch_bounds__(kThr, 1)
-    k_ssd_scan_tc(const uint16_t* __restrict__ u, const float* __restrict__ dt, const float* __restrict__ cum,
+    k_ssd_scan_tc(const uint16_t* __restrict__ u, const float* __restrict__ dt, const float2* __restrict__ cum,
                   const float* __restrict__ states, const float* __restrict__ Dp, const SeqInfo si,
                   uint16_t* __restrict__ y, int* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -220,9 +226,9 @@ __global__ void __launch_bounds__(kThr, 1)
   uint8_t* sXT = sB + 256 * 128 * 2;     // [64 p][256 s]    32 KB
   uint8_t* sSh = sXT + 64 * 256 * 2;     // [64 p][128 n]    16 KB
   uint8_t* sSl = sSh + 64 * 128 * 2;     // [64 p][128 n]    16 KB
-  float* cums = reinterpret_cast<float*>(sSl + 64 * 128 * 2);   // [256]
-  float* dts = cums + kChunk;                                    // [256]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(dts + kChunk);    // [2]
+  float2* cums = reinterpret_cast<float2*>(sSl + 64 * 128 * 2);  // [256] (hi, lo)
+  float* dts = reinterpret_cast<float*>(cums + kChunk);           // [256]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dts + kChunk);     // [2]
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
 
   const int c = blockIdx.x, g = blockIdx.y, tb = blockIdx.z, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(kThr, 1)
   for (int hh = 0; hh < kHPG; ++hh) {
     const int h = g * kHPG + hh;
     for (int s = tid; s < KS; s += kThr) {
-      cums[s] = s < cp.n ? cum[(size_t)(cp.t0 + s) * kNH + h] : 0.f;
+      cums[s] = s < cp.n ? cum[(size_t)(cp.t0 + s) * kNH + h] : make_float2(0.f, 0.f);
       dts[s] = s < cp.n ? dt[(size_t)(cp.t0 + s) * kNH + h] : 0.f;
     }
     // x^T: rows p, K = s.  (KS/8) x 8 blocks.
@@ -316,7 +322,7 @@ __global__ void __launch_bounds__(kThr, 1)
       *reinterpret_cast<uint4*>(sSl + sw_chunk(p, k8, 64)) = *reinterpret_cast<const uint4*>(lo);
     }
     __syncthreads();
-    const float cum_t = tt < cp.n ? cums[tt] : 0.f;
+    const float2 cum_t = tt < cp.n ? cums[tt] : make_float2(0.f, 0.f);
     const int tlim = tt < cp.n ? tt : -1;
     for (int half = 0; half < KS / 128; ++half) {
       // P for sources [128 half, +128): warps 0-3 take 32-blocks 0, 1 and
@@ -334,7 +340,9 @@ __global__ void __launch_bounds__(kThr, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int s = s0 + j;
-          const float v = (s <= tlim) ? __uint_as_float(r[j]) * __expf(cum_t - cums[s]) * dts[s] : 0.f;
+          const float2 cs = cums[s];
+          const float v =
+              (s <= tlim) ? __uint_as_float(r[j]) * __expf((cum_t.x - cs.x) + (cum_t.y - cs.y)) * dts[s] : 0.f;
           split_bf16(v, hi[j], lo[j]);
         }
 #pragma unroll
@@ -378,7 +386,7 @@ __global__ void __launch_bounds__(kThr, 1)
     }
     // y = Y_diag + exp(cum_t) Y_off + D x; warps 0-3 write p < 32, warps 4-7 p >= 32
     {
-      const float et = expf(cum_t);
+      const float et = expf(cum_t.x + cum_t.y);
       const float Dh = Dp[h];
       uint32_t rd[32], ro[32];
       tmem_ld_32x32b_x32(lane_base + COL_YD + (uint32_t)(colhalf * 32), rd);
@@ -417,10 +425,10 @@ __global__ void __launch_bounds__(kThr, 1)
 // ---------------------------------------------------------------------------
 static size_t state_smem() { return 1024 + (128 * 256 + 2 * 64 * 256) * 2 + kChunk * 4 + 64; }
 static size_t scan_smem() {
-  return 1024 + (128 * 128 + 256 * 128 + 64 * 256 + 2 * 64 * 128) * 2 + 2 * kChunk * 4 + 64;
+  return 1024 + (128 * 128 + 256 * 128 + 64 * 256 + 2 * 64 * 128) * 2 + 3 * kChunk * 4 + 64;
 }
 
-cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const float* dt, const float* cum, const SeqInfo& si,
+cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const float* dt, const float2* cum, const SeqInfo& si,
                                       float* states, int* err, cudaStream_t st) {
   cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k_ssd_state_tc), (int)state_smem());
   if (e != cudaSuccess) return e;
@@ -428,7 +436,7 @@ cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const float* dt, const 
                     err);
 }
 
-cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const float* dt, const float* cum, const float* states,
+cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const float* dt, const float2* cum, const float* states,
                                      const BlockParams& bp, const SeqInfo& si, uint16_t* y, int* err,
                                      cudaStream_t st) {
   cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k_ssd_scan_tc), (int)scan_smem());
