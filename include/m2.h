@@ -243,6 +243,36 @@ m2_status fp8_linear(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_
                      int N, int K, void* workspace, size_t ws_bytes, void* stream);
 
 /*
+ * fp8_linear for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this entry point.
+ *
+ * Who needs it: code that embeds this library without owning a device
+ * allocator (a plain C host with no framework around it), serving loops that
+ * forbid allocation after start-up so their memory footprint stays fixed, and
+ * code that issues work while a CUDA stream is being captured, where a fresh
+ * workspace cannot be allocated on the spot.  fp8_linear needs a caller
+ * workspace for its split-K partial sums; this variant instead uses one
+ * library-owned scratch array in device memory (a file-scope __device__
+ * array of M2_NOALLOC_SCRATCH_BYTES = 32 MiB), so it calls no cudaMalloc,
+ * cudaFree or allocating library routine.  Every GPU on which this entry point
+ * has run holds that array until the process exits.
+ *
+ * Same arguments and result as fp8_linear without the workspace.  Only the
+ * few-row (decode) form is offered: 1 <= M <= 256, and the split-K partials
+ * (splits x M x N floats) must fit the scratch array; larger problems are
+ * refused with M2_ESHAPE and a message naming the limit.  The first call on
+ * each device looks the array up (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  All calls share
+ * the one array: calls that can overlap on the GPU (different streams, or
+ * different host threads) race on it and must be serialised by the caller.
+ * Every call overwrites the part of the array it reads, so no clearing is
+ * needed between calls.
+ */
+#define M2_NOALLOC_SCRATCH_BYTES (32u << 20)
+m2_status fp8_linear_noalloc(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_w, uint16_t* y, int M,
+                             int N, int K, void* stream);
+
+/*
  * The quantise-inside form (MatmulFp8CutlassD of PR #972): x bf16 [M, K] is
  * quantised with s_a (as fp8_quant) into the workspace, then as fp8_linear.
  * Workspace: M*K bytes (rounded up to 256) plus fp8_linear's.

@@ -32,7 +32,7 @@ STATUS_NAMES = {0: "M2_OK", 1: "M2_EINVAL", 2: "M2_ESHAPE", 3: "M2_ECUDA", 4: "M
 EXPORTED = ["m2_last_error", "m2_create", "m2_destroy", "m2_get_stats", "m2_set_taps", "m2_check",
             "m2_prefill_workspace_size", "m2_prefill", "m2_decode_workspace_size", "m2_decode",
             "fp8_quant", "fp8_linear_workspace_size", "fp8_linear", "fp8_linear_bf16",
-            "m2_rmsnorm_residual", "m2_profile_enable", "m2_profile_read"]
+            "m2_rmsnorm_residual", "m2_profile_enable", "m2_profile_read", "fp8_linear_noalloc"]
 
 STAGES = ["quant_in", "in_proj", "conv", "conv_state", "ssd_cumsum", "ssd_chunk_state", "ssd_state_pass",
           "ssd_chunk_scan", "norm_quant", "out_proj", "decode_fused", "dec_quant_in", "dec_in_proj",
@@ -90,6 +90,7 @@ _sigs = {
     "m2_rmsnorm_residual": ([_vp, _vp, _vp, _f, _vp, _i, _i, _vp], _i),
     "m2_profile_enable": ([_vp, _i], _i),
     "m2_profile_read": ([_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)], _i),
+    "fp8_linear_noalloc": ([_vp, _f, _vp, _f, _vp, _i, _i, _i, _vp], _i),
 }
 for _name, (_args, _ret) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -284,6 +285,18 @@ def fp8_linear(a_q: torch.Tensor, s_a: float, w_q: torch.Tensor, s_w: float, y: 
         workspace = torch.empty(max(fp8_linear_workspace_size(M, N, K), 1), dtype=torch.uint8, device=a_q.device)
     _check(_lib.fp8_linear(_ptr(a_q), s_a, _ptr(w_q), s_w, _ptr(y), M, N, K, _ptr(workspace), workspace.numel(),
                            _stream(stream)))
+    return y
+
+
+def fp8_linear_noalloc(a_q: torch.Tensor, s_a: float, w_q: torch.Tensor, s_w: float, y: torch.Tensor,
+                       stream=None) -> torch.Tensor:
+    """fp8_linear without a workspace (library-owned scratch; M <= 256)."""
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    _need(a_q, "a_q", torch.uint8, (M, K))
+    _need(w_q, "w_q", torch.uint8, (N, K))
+    _need(y, "y", torch.bfloat16, (M, N))
+    _check(_lib.fp8_linear_noalloc(_ptr(a_q), s_a, _ptr(w_q), s_w, _ptr(y), M, N, K, _stream(stream)))
     return y
 
 

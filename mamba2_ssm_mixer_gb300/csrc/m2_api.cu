@@ -4,6 +4,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -544,4 +546,54 @@ m2_status m2_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* 
   return M2_OK;
 }
 
+// ---------------------------------------------------------------- fp8_linear without allocation
+
 }  // extern "C"
+
+namespace {
+// Library-owned scratch for fp8_linear_noalloc: the split-K partial sums.
+// Host code must not use this name as an address; it looks the device address
+// up once per device (noalloc_scratch below).
+__device__ __align__(256) float g_noalloc_scratch[M2_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+m2_status noalloc_scratch(float** out) {
+  static std::mutex mu;
+  static std::map<int, float*> by_device;
+  int dev = 0;
+  M2_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = by_device.find(dev);
+  if (it != by_device.end()) {
+    *out = it->second;
+    return M2_OK;
+  }
+  float* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_noalloc_scratch);
+  if (e != cudaSuccess || !p)
+    return fail(M2_ECUDA, "fp8_linear_noalloc: cudaGetSymbolAddress of the scratch array failed: %s",
+                cudaGetErrorString(e));
+  by_device[dev] = p;
+  *out = p;
+  return M2_OK;
+}
+}  // namespace
+
+extern "C" m2_status fp8_linear_noalloc(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_w, uint16_t* y,
+                                        int M, int N, int K, void* stream) {
+  g_err.clear();
+  m2_status s = check_linear(a_q, w_q, y, M, N, K, s_a, s_w, "fp8_linear_noalloc");
+  if (s) return s;
+  if (M < 1 || M > kSkinnyMaxRows)
+    return fail(M2_ESHAPE, "fp8_linear_noalloc: M = %d; this entry point takes 1 <= M <= %d", M, kSkinnyMaxRows);
+  const size_t need = gemm_tc_skinny_workspace(M, N, K);
+  if (need > (size_t)M2_NOALLOC_SCRATCH_BYTES)
+    return fail(M2_ESHAPE, "fp8_linear_noalloc: %d x %d x %d needs %zu bytes of scratch, above the %u-byte array", M,
+                N, K, need, (unsigned)M2_NOALLOC_SCRATCH_BYTES);
+  float* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch))) return s;
+  int nl = 0;
+  M2_CUDA(gemm_tc_skinny(a_q, w_q, y, M, N, K, s_a * s_w, scratch, (size_t)M2_NOALLOC_SCRATCH_BYTES, nullptr,
+                         static_cast<cudaStream_t>(stream), &nl));
+  return M2_OK;
+}
+
