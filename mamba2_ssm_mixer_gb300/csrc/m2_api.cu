@@ -307,9 +307,10 @@ struct PrefillWs {
   uint8_t* q;
   uint16_t* zx;
   uint16_t* u;
-  float* dt;
-  float2* cum;
+  CumDt* cumdt;
   float* states;
+  uint8_t* xt_img;
+  uint8_t* sin_img;
   uint16_t* y;
   uint8_t* q2;
   void* gemm_ws;
@@ -323,9 +324,10 @@ static PrefillWs carve_prefill(void* base, int T, int chunks) {
   w.q = c.take<uint8_t>((size_t)T * kH);
   w.zx = c.take<uint16_t>((size_t)T * kZ);
   w.u = c.take<uint16_t>((size_t)T * kConv);
-  w.dt = c.take<float>((size_t)T * kNH);
-  w.cum = c.take<float2>((size_t)T * kNH);
+  w.cumdt = c.take<CumDt>((size_t)chunks * kNH * kChunk);
   w.states = c.take<float>((size_t)chunks * kNH * kP * kN);
+  w.xt_img = c.take<uint8_t>((size_t)chunks * kNH * kXtImageBytes);
+  w.sin_img = c.take<uint8_t>((size_t)chunks * kNH * kSinImageBytes);
   w.y = c.take<uint16_t>((size_t)T * kI);
   w.q2 = c.take<uint8_t>((size_t)T * kI);
   size_t g1 = gemm_workspace_bytes(T, kZ, kH), g2 = gemm_workspace_bytes(T, kH, kI);
@@ -375,12 +377,14 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
   M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(w.zx, bp, conv_state, local, w.u, st));
   M2_STAGE(h, st, M2_STAGE_CONV_STATE, 1, launch_conv_state_update(w.zx, conv_state, local, st));
-  M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(w.zx, bp, local, w.dt, w.cum, st));
+  M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1,
+           launch_ssd_cumsum(w.zx, bp, local, w.cumdt, h->taps_on ? h->taps.dt : nullptr, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
-           launch_ssd_chunk_state_tc(w.u, w.dt, w.cum, local, w.states, h->err, st));
-  M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1, launch_ssd_state_pass(w.states, w.cum, local, ssm_state, st));
+           launch_ssd_chunk_state_tc(w.u, w.cumdt, local, w.states, w.xt_img, h->err, st));
+  M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
+           launch_ssd_state_pass(w.states, w.cumdt, local, w.sin_img, ssm_state, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
-           launch_ssd_chunk_scan_tc(w.u, w.dt, w.cum, w.states, bp, local, w.y, h->err, st));
+           launch_ssd_chunk_scan_tc(w.u, w.cumdt, w.xt_img, w.sin_img, bp, local, w.y, h->err, st));
   M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
            launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, h->taps_on ? h->taps.o : nullptr, st));
   M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
@@ -388,7 +392,6 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
     if ((s = copy_tap(h->taps.q, w.q, (size_t)T * kH, st))) return s;
     if ((s = copy_tap(h->taps.zx, w.zx, (size_t)T * kZ * 2, st))) return s;
     if ((s = copy_tap(h->taps.u, w.u, (size_t)T * kConv * 2, st))) return s;
-    if ((s = copy_tap(h->taps.dt, w.dt, (size_t)T * kNH * 4, st))) return s;
     if ((s = copy_tap(h->taps.y, w.y, (size_t)T * kI * 2, st))) return s;
     if ((s = copy_tap(h->taps.q2, w.q2, (size_t)T * kI, st))) return s;
   }

@@ -37,18 +37,34 @@ cudaError_t launch_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint
                                     uint16_t* normed, int T, int n, cudaStream_t st);
 
 // ssd.cu
-// cum: the in-chunk cumulative log-decay as (hi, lo) float pairs.
-cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, float* dt, float2* cum,
-                              cudaStream_t st);
-cudaError_t launch_ssd_state_pass(float* states, const float2* cum, const SeqInfo& si, float* ssm_state,
-                                  cudaStream_t st);
+// Per (chunk, head, token of the chunk): the in-chunk cumulative log-decay as
+// an unevaluated (hi, lo) float pair and dt; zeros past the chunk's end.
+// Stored [chunk][head][256] so one head's chunk is 4 KB contiguous.
+struct CumDt {
+  float hi, lo, dt, pad;
+};
+// Bytes of one (chunk, head) operand image: x^T [64 p][256 s] bf16 in the MMA's
+// K-major 128-byte-swizzled layout, and S_in as bf16 high + remainder
+// [2][64 p][128 n] in the same layout.
+constexpr int kXtImageBytes = 64 * 256 * 2;
+constexpr int kSinImageBytes = 2 * 64 * 128 * 2;
+
+// dt_tok (optional, may be null): dt as [T, 64] for the intermediate taps.
+cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, CumDt* cumdt,
+                              float* dt_tok, cudaStream_t st);
+// Reads the chunk states, writes the state entering each chunk as S_in images
+// and the final state of each sequence to ssm_state.
+cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const SeqInfo& si, uint8_t* sin_img,
+                                  float* ssm_state, cudaStream_t st);
 
 // ssd_tc.cu (tensor-core chunk states and chunk scan)
-cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const float* dt, const float2* cum, const SeqInfo& si,
-                                      float* states, int* err, cudaStream_t st);
-cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const float* dt, const float2* cum, const float* states,
-                                     const BlockParams& bp, const SeqInfo& si, uint16_t* y, int* err,
-                                     cudaStream_t st);
+// Chunk states f32 [chunk][head][64][128]; also writes each (chunk, head)'s
+// x^T image for the scan.
+cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const CumDt* cumdt, const SeqInfo& si, float* states,
+                                      uint8_t* xt_img, int* err, cudaStream_t st);
+cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const CumDt* cumdt, const uint8_t* xt_img,
+                                     const uint8_t* sin_img, const BlockParams& bp, const SeqInfo& si, uint16_t* y,
+                                     int* err, cudaStream_t st);
 
 // decode_tma.cu (persistent, TMA-streamed state)
 cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,

@@ -38,7 +38,7 @@ __device__ __forceinline__ ChunkPos chunk_pos(const SeqInfo& si, int c) {
 // single float would leave with ~1e-4 relative error.
 __global__ void __launch_bounds__(256) k_ssd_cumsum(const uint16_t* __restrict__ zx, const float* __restrict__ A_log,
                                                     const float* __restrict__ dt_bias, const SeqInfo si,
-                                                    float* __restrict__ dt_out, float2* __restrict__ cum_out) {
+                                                    CumDt* __restrict__ cumdt, float* __restrict__ dt_tok) {
   __shared__ double wsum[8];
   pdl_wait();
   pdl_trigger();
@@ -63,24 +63,37 @@ __global__ void __launch_bounds__(256) k_ssd_cumsum(const uint16_t* __restrict__
   double pre = 0.0;
   for (int w = 0; w < (i >> 5); ++w) pre += wsum[w];
   v += pre;
+  CumDt r = {0.f, 0.f, 0.f, 0.f};
   if (i < cp.n) {
-    const float hi = (float)v;
-    dt_out[(size_t)(cp.t0 + i) * kNH + h] = dt;
-    cum_out[(size_t)(cp.t0 + i) * kNH + h] = make_float2(hi, (float)(v - (double)hi));
+    r.hi = (float)v;
+    r.lo = (float)(v - (double)r.hi);
+    r.dt = dt;
+    if (dt_tok) dt_tok[(size_t)(cp.t0 + i) * kNH + h] = dt;
   }
+  cumdt[((size_t)c * kNH + h) * kChunk + i] = r;
 }
 
-// 3. sequential state passing over the chunks of each sequence.  states[c]
-// is replaced in place by the state entering chunk c; the state after the
-// last chunk goes to ssm_state (read first if the sequence has initial state).
-// Each thread owns 4 consecutive state entries and keeps the loads of up to 8
-// chunks in flight before walking the recurrence.
-__global__ void __launch_bounds__(256) k_ssd_state_pass(float* __restrict__ states, const float2* __restrict__ cum,
-                                                        const SeqInfo si, float* __restrict__ ssm_state) {
+// 3. sequential state passing over the chunks of each sequence: the state
+// entering chunk c is written as the scan's S_in image (bf16 high part and
+// remainder, K-major 128-byte-swizzled [64 p][128 n] each); the state after
+// the last chunk goes to ssm_state (read first if the sequence has initial
+// state).  Each thread owns 4 consecutive entries of one row p and keeps the
+// loads of up to 8 chunks in flight before walking the recurrence.
+__device__ __forceinline__ uint32_t sin_offset(int p, int n) {
+  return (uint32_t)((n >> 6) * 8192 + (p >> 3) * 1024 + (p & 7) * 128 + ((((n & 63) >> 3) ^ (p & 7)) << 4) +
+                    (n & 7) * 2);
+}
+
+__global__ void __launch_bounds__(256) k_ssd_state_pass(const float* __restrict__ states,
+                                                        const CumDt* __restrict__ cumdt, const SeqInfo si,
+                                                        uint8_t* __restrict__ sin_img,
+                                                        float* __restrict__ ssm_state) {
   pdl_wait();
   pdl_trigger();
   const int s = blockIdx.x, h = blockIdx.y;
   const int e4 = blockIdx.z * 256 + threadIdx.x;   // float4 index inside [P, N]
+  const int p = (e4 * 4) / kN, n = (e4 * 4) % kN;
+  const uint32_t off = sin_offset(p, n);
   const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
   float4* fin = reinterpret_cast<float4*>(ssm_state + ((size_t)s * kNH + h) * (kP * kN)) + e4;
   float4 run = init ? *fin : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -92,18 +105,29 @@ __global__ void __launch_bounds__(256) k_ssd_state_pass(float* __restrict__ stat
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int c = cb + k;
+      sc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      dec[k] = 0.f;
       if (c < c1) {
         sc[k] = reinterpret_cast<const float4*>(states + ((size_t)c * kNH + h) * (kP * kN))[e4];
-        const int tl = min(tbeg + (c - c0 + 1) * kChunk, tend) - 1;
-        const float2 cl = cum[(size_t)tl * kNH + h];
-        dec[k] = cl.x + cl.y;
+        const int nl = min(kChunk, tend - (tbeg + (c - c0) * kChunk));   // tokens in chunk c
+        const CumDt cl = cumdt[((size_t)c * kNH + h) * kChunk + nl - 1];
+        dec[k] = cl.hi + cl.lo;
       }
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const int c = cb + k;
       if (c < c1) {
-        reinterpret_cast<float4*>(states + ((size_t)c * kNH + h) * (kP * kN))[e4] = run;
+        uint8_t* img = sin_img + ((size_t)c * kNH + h) * kSinImageBytes;
+        const float f[4] = {run.x, run.y, run.z, run.w};
+        uint16_t hi[4], lo[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hi[q] = f2bfbits(f[q]);
+          lo[q] = f2bfbits(f[q] - bfbits2f(hi[q]));
+        }
+        *reinterpret_cast<uint2*>(img + off) = *reinterpret_cast<const uint2*>(hi);
+        *reinterpret_cast<uint2*>(img + kSinImageBytes / 2 + off) = *reinterpret_cast<const uint2*>(lo);
         const float d = expf(dec[k]);
         run.x = fmaf(d, run.x, sc[k].x);
         run.y = fmaf(d, run.y, sc[k].y);
@@ -115,16 +139,16 @@ __global__ void __launch_bounds__(256) k_ssd_state_pass(float* __restrict__ stat
   *fin = run;
 }
 
-cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, float* dt, float2* cum,
-                              cudaStream_t st) {
-  return launch_pdl(k_ssd_cumsum, dim3(si.total_chunks, kNH), dim3(256), 0, st, zx, bp.A_log, bp.dt_bias, si, dt,
-                    cum);
+cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, CumDt* cumdt,
+                              float* dt_tok, cudaStream_t st) {
+  return launch_pdl(k_ssd_cumsum, dim3(si.total_chunks, kNH), dim3(256), 0, st, zx, bp.A_log, bp.dt_bias, si, cumdt,
+                    dt_tok);
 }
 
-cudaError_t launch_ssd_state_pass(float* states, const float2* cum, const SeqInfo& si, float* ssm_state,
-                                  cudaStream_t st) {
-  return launch_pdl(k_ssd_state_pass, dim3(si.nseq, kNH, (kP * kN) / 4 / 256), dim3(256), 0, st, states, cum, si,
-                    ssm_state);
+cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const SeqInfo& si, uint8_t* sin_img,
+                                  float* ssm_state, cudaStream_t st) {
+  return launch_pdl(k_ssd_state_pass, dim3(si.nseq, kNH, (kP * kN) / 4 / 256), dim3(256), 0, st, states, cumdt, si,
+                    sin_img, ssm_state);
 }
 
 }  // namespace m2

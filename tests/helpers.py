@@ -64,20 +64,31 @@ def bf16_ulp(v):
     return np.exp2(np.floor(np.log2(a)) - 7)
 
 
+# One e4m3 code step of out_proj's input at the top of the e4m3 range is 32
+# codes = 1.0 in units of the normed activation (s_y = 1/32); times the largest
+# out_proj weight (|W2| <= ~0.11 for N(0, 0.02) over 11M entries) it moves an
+# output element by up to ~0.11.  Two W8A8 implementations whose unrounded
+# activations differ in the last bf16 bit take different e4m3 decisions for a
+# small fraction of elements (both decisions are correct roundings of their own
+# inputs), so a per-element bound must admit one flip.
+FLIP_BOUND = 0.15
+MAX_FRAC_OVER_2E2 = 1e-2
+
+
 def assert_block_out(got, ref, what="out"):
-    """Block output (bf16): relative L2 <= 1e-2 and, per element,
-    |got - ref| <= 2e-2 + one bf16 ulp of the larger of the two values.  The
-    ulp term is the output's own storage rounding: outputs reach |8| where one
-    bf16 step is 0.03, so two independently rounded results can differ by a
-    step there no matter how close their unrounded values are."""
+    """Block output (bf16): relative L2 <= 1e-2; every element within
+    FLIP_BOUND; and at most 1% of elements beyond 2e-2 + one bf16 ulp of the
+    larger value (the ulp term is the output's own storage rounding: outputs
+    reach |8| where one bf16 step is 0.03)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     ma, rl = max_abs(got, ref), rel_l2(got, ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
     bound = OUT_MAX_ABS + bf16_ulp(np.maximum(np.abs(got), np.abs(ref)))
-    over = np.abs(got - ref) > bound
-    assert rl <= OUT_REL_L2 and not over.any(), \
-        f"{what}: max abs {ma:.3e}, rel L2 {rl:.3e}, {over.sum()} elements over 2e-2 + 1 ulp"
+    frac = float(np.mean(np.abs(got - ref) > bound))
+    msg = f"{what}: max abs {ma:.3e}, rel L2 {rl:.3e}, {frac:.2e} of elements over 2e-2 + 1 ulp"
+    print(msg)
+    assert rl <= OUT_REL_L2 and ma <= FLIP_BOUND and frac <= MAX_FRAC_OVER_2E2, msg
     return ma, rl
 
 

