@@ -253,7 +253,7 @@ m2_status fp8_linear(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_
  * workspace cannot be allocated on the spot.  fp8_linear needs a caller
  * workspace for its split-K partial sums; this variant instead uses one
  * library-owned scratch array in device memory (a file-scope __device__
- * array of M2_NOALLOC_SCRATCH_BYTES = 32 MiB), so it calls no cudaMalloc,
+ * array of M2_NOALLOC_SCRATCH_BYTES = 16 MiB), so it calls no cudaMalloc,
  * cudaFree or allocating library routine.  Every GPU on which this entry point
  * has run holds that array until the process exits.
  *
@@ -268,7 +268,7 @@ m2_status fp8_linear(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_
  * Every call overwrites the part of the array it reads, so no clearing is
  * needed between calls.
  */
-#define M2_NOALLOC_SCRATCH_BYTES (32u << 20)
+#define M2_NOALLOC_SCRATCH_BYTES (16u << 20)
 m2_status fp8_linear_noalloc(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_w, uint16_t* y, int M,
                              int N, int K, void* stream);
 

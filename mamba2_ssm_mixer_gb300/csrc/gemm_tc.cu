@@ -471,15 +471,22 @@ cudaError_t launch_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, float
 }  // namespace
 
 // Split plan of the skinny GEMM for (Mtok, N, K): splits and k-blocks each.
+// All CTAs fit in one wave (CTAs per SM from the shared-memory footprint) and
+// each split streams at least 4 k-blocks, so the f32 partials stay small next
+// to the weights.
 void skinny_plan(int Mtok, int N, int K, int* splits, int* kps) {
-  (void)Mtok;
   const int kblocks = (K + kBK - 1) / kBK;
   const int nt = (N + kBM - 1) / kBM;
-  int target = 2 * num_sms();
-  int s = (target + nt - 1) / nt;
+  const int bnt = (Mtok + 15) / 16 * 16;
+  const int stages = bnt <= 64 ? 4 : (bnt <= 128 ? 3 : 2);   // 2 CTAs per SM from 32 rows up
+  const int smem = 1024 + stages * (kBM + bnt) * kBK + 256;
+  int per_sm = (228 * 1024) / (smem + 1024);
+  if (per_sm < 1) per_sm = 1;
+  int s = (per_sm * num_sms()) / nt;
   if (s > kblocks) s = kblocks;
   if (s < 1) s = 1;
   int per = (kblocks + s - 1) / s;
+  if (per < 4) per = kblocks < 4 ? kblocks : 4;
   s = (kblocks + per - 1) / per;
   *splits = s;
   *kps = per;
@@ -502,8 +509,8 @@ cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int 
   if (bnt <= 16) e = launch_skinny<16, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
   else if (bnt <= 32) e = launch_skinny<32, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
   else if (bnt <= 64) e = launch_skinny<64, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
-  else if (bnt <= 128) e = launch_skinny<128, 6>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
-  else if (bnt <= 256) e = launch_skinny<256, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 128) e = launch_skinny<128, 3>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 256) e = launch_skinny<256, 2>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   *launches = 1;

@@ -2,13 +2,19 @@
 512-slot pool per layer, then varlen prefill {4096, 1024, 512, 37}, against the
 oracle's stack (h <- h + block(rmsnorm(h) * w), bf16 residual stream).
 
-Stack tolerance: the residual stream is bf16 with |h| growing through the
-layers, so one bf16 rounding step of h is 2^-8 |h|.  Output: relative L2
-<= 1e-2 and |err| <= FLIP_BOUND + 2^-7 |ref| per element.  SSM states: layer
-0 sees identical inputs on both sides and keeps the block tolerance (relative
-L2 <= 1e-3); a deeper layer's input already carries the stack's accumulated
-difference, which the e4m3 input quantisation turns into whole-code flips, so
-its bound grows with depth.  Every layer's figure is printed.
+Two checks per direction:
+  * per layer, at the block tolerances: the GPU block l is run on the oracle's
+    own input to layer l (oracle -> GPU, never the other way), with that
+    layer's weights, pools and slot routing, and its output and states are
+    compared with the oracle's;
+  * end to end, the composition: the whole stack runs on the GPU from the
+    first input.  The e4m3 quantisation of each layer's input and of out_proj's
+    input turns last-bit differences into whole-code flips (FLIP_BOUND), and 23
+    layers compound them (measured in decode: layer-0 states agree to 3.5e-6,
+    layer-22 states to 2.5e-2, final output rel L2 4.9e-2; in prefill the
+    final states integrate every token's input, layer-1 states 1.05e-2), so the
+    end-to-end check is a composition check: relative L2 <= 1e-1 on the output
+    and on every layer's states (a routing or residual error is O(1)).
 """
 import concurrent.futures as cf
 import multiprocessing as mp
@@ -20,30 +26,18 @@ import torch
 
 import oracle
 import synth
-from helpers import FLIP_BOUND, bf16_dev, device_weights, rel_l2, to_np
+from helpers import assert_block_out, assert_state, bf16_dev, device_weights, rel_l2, to_np
 
 pytestmark = pytest.mark.gpu
 
 m2 = pytest.importorskip("mamba2_ssm_mixer_gb300")
 
 CFG, LAYERS = 4, 23
+EPS = 1e-5
 
 
-def _stack_ok(got, ref):
-    got, ref = np.asarray(got, np.float64), np.asarray(ref, np.float64)
-    assert np.all(np.isfinite(got))
-    rl = rel_l2(got, ref)
-    bad = np.abs(got - ref) > FLIP_BOUND + 2.0 ** -7 * np.abs(ref)
-    print(f"stack output: rel L2 {rl:.3e}, max abs {np.abs(got - ref).max():.3e}")
-    assert rl <= 1e-2 and not bad.any(), f"stack: rel L2 {rl:.3e}, {bad.sum()} elements over the bound"
-
-
-def _state_bound(l):
-    """Layer 0 sees identical inputs on both sides: the block tolerance.  A
-    deeper layer's input carries the stack's accumulated e4m3 decision flips
-    (see FLIP_BOUND); measured growth is ~2e-3 per layer, bounded here at
-    1e-3 + 3e-3 l."""
-    return 1e-3 + 3e-3 * l
+def _e2e_state_bound(l):
+    return 1e-1
 
 
 @pytest.fixture(scope="module")
@@ -58,7 +52,7 @@ def stack():
         nw = synth.make_stack_norm_w(CFG, l)
         norm_ws_np.append(nw)
         norm_ws.append(bf16_dev(nw))
-    return weights, m2.Mamba2Stack(blocks, norm_ws, 1e-5), norm_ws_np
+    return weights, m2.Mamba2Stack(blocks, norm_ws, EPS), norm_ws_np
 
 
 def test_config4_stack_decode_b128_512_slots(stack):
@@ -70,29 +64,42 @@ def test_config4_stack_decode_b128_512_slots(stack):
     ssm_pools = [synth.device_normal((n_slots, 64, 64, 128), CFG, l, synth.T_SSM_STATE, 0.1, torch.float32, dev)
                  for l in range(LAYERS)]
     slots = synth.make_slot_idx(CFG, n_slots, Bt)
-    untouched = np.setdiff1d(np.arange(n_slots), slots)[::37]
-    # the oracle reads only the selected rows: copy them (and a sample of the
-    # untouched rows) to the host before the call
-    sel_conv = [to_np(p[torch.from_numpy(slots).long().to(dev)]) for p in conv_pools]
-    sel_ssm = [p[torch.from_numpy(slots).long().to(dev)].cpu().numpy() for p in ssm_pools]
-    keep_ssm = [p[torch.from_numpy(untouched).long().to(dev)].clone() for p in ssm_pools]
+    sl = torch.from_numpy(slots).long().to(dev)
+    untouched = torch.from_numpy(np.setdiff1d(np.arange(n_slots), slots)[::37]).long().to(dev)
+    # the oracle reads only the selected rows: keep them (and a sample of the
+    # untouched rows) before the GPU advances the pools
+    sel_conv = [p[sl].clone() for p in conv_pools]
+    sel_ssm = [p[sl].clone() for p in ssm_pools]
+    keep_ssm = [p[untouched].clone() for p in ssm_pools]
     h = synth.make_hidden(CFG, Bt)
     out = stk.decode(bf16_dev(h), conv_pools, ssm_pools, torch.from_numpy(slots).to(dev))
     torch.cuda.synchronize()
     for b in stk.blocks:
         b.check()
-    # oracle, layer by layer
-    hh = h.astype(np.float64)
+    e2e_rows = [p[sl].cpu().numpy() for p in ssm_pools]
     ident = np.arange(Bt)
+    ident_dev = torch.arange(Bt, dtype=torch.int32, device=dev)
+    hh = h.astype(np.float64)
     for l in range(LAYERS):
-        r = oracle.block_decode(weights[l], oracle.rmsnorm(hh, norm_ws_np[l], 1e-5), sel_conv[l], sel_ssm[l], ident)
+        assert torch.equal(ssm_pools[l][untouched], keep_ssm[l])            # untouched slots byte-identical
+        conv_rows = to_np(sel_conv[l])
+        ssm_rows = sel_ssm[l].cpu().numpy()
+        x = oracle.rmsnorm(hh, norm_ws_np[l], EPS)
+        r = oracle.block_decode(weights[l], x, conv_rows, ssm_rows, ident)
+        # per layer, on the oracle's input to this layer
+        c_pool, s_pool = sel_conv[l].clone(), sel_ssm[l].clone()
+        got = stk.blocks[l].decode(bf16_dev(x), c_pool, s_pool, ident_dev)
+        torch.cuda.synchronize()
+        assert_block_out(to_np(got), r["out"], what=f"decode layer {l} out")
+        assert_state(s_pool.cpu().numpy(), r["ssm_rows"], what=f"decode layer {l} ssm rows")
+        # end to end, on the GPU stack's own input
+        e = rel_l2(e2e_rows[l], r["ssm_rows"])
+        print(f"decode layer {l}: end-to-end ssm rows rel L2 {e:.3e}")
+        assert e <= _e2e_state_bound(l), f"layer {l} end-to-end ssm rows: rel L2 {e:.3e}"
         hh = oracle.bf16_round(hh + r["out"])
-        got_rows = ssm_pools[l][torch.from_numpy(slots).long().to(dev)].cpu().numpy()
-        e = rel_l2(got_rows, r["ssm_rows"])
-        print(f"decode layer {l}: ssm rows rel L2 {e:.3e}")
-        assert e <= _state_bound(l), f"layer {l} ssm rows: rel L2 {e:.3e}"
-        assert torch.equal(ssm_pools[l][torch.from_numpy(untouched).long().to(dev)], keep_ssm[l])
-    _stack_ok(to_np(out), hh)
+    rl = rel_l2(to_np(out), hh)
+    print(f"decode stack output: end-to-end rel L2 {rl:.3e}")
+    assert np.all(np.isfinite(to_np(out))) and rl <= 1e-1
 
 
 def test_config4_stack_varlen_prefill(stack):
@@ -106,12 +113,24 @@ def test_config4_stack_varlen_prefill(stack):
     torch.cuda.synchronize()
     for b in stk.blocks:
         b.check()
+    ws = torch.empty(stk.blocks[0].prefill_workspace_size(lens), dtype=torch.uint8, device=dev)
+    hh = h.astype(np.float64)
     # the oracle's recurrence runs group by group on a spawn pool (groups are
     # independent; each group's recurrence is still token by token)
     with cf.ProcessPoolExecutor(max_workers=min(8, os.cpu_count() or 1), mp_context=mp.get_context("spawn")) as ex:
-        ref_h, _, ref_ssm = oracle.stack_prefill(weights, norm_ws_np, h, lens, 1e-5, map_fn=ex.map)
-    for l in range(LAYERS):
-        e = rel_l2(to_np(ssm[l]), ref_ssm[l])
-        print(f"prefill layer {l}: final ssm state rel L2 {e:.3e}")
-        assert e <= _state_bound(l), f"layer {l} final ssm state: rel L2 {e:.3e}"
-    _stack_ok(to_np(out), ref_h)
+        for l in range(LAYERS):
+            x = oracle.rmsnorm(hh, norm_ws_np[l], EPS)
+            r = oracle.block_prefill(weights[l], x, lens, map_fn=ex.map)
+            c1 = torch.zeros((4, 6144, 3), dtype=torch.bfloat16, device=dev)
+            s1 = torch.zeros((4, 64, 64, 128), dtype=torch.float32, device=dev)
+            got = stk.blocks[l].prefill(bf16_dev(x), lens, c1, s1, workspace=ws)
+            torch.cuda.synchronize()
+            assert_block_out(to_np(got), r["out"], what=f"prefill layer {l} out")
+            assert_state(to_np(s1), r["ssm_state"], what=f"prefill layer {l} final ssm state")
+            e = rel_l2(to_np(ssm[l]), r["ssm_state"])
+            print(f"prefill layer {l}: end-to-end final ssm state rel L2 {e:.3e}")
+            assert e <= _e2e_state_bound(l), f"layer {l} end-to-end final state: rel L2 {e:.3e}"
+            hh = oracle.bf16_round(hh + r["out"])
+    rl = rel_l2(to_np(out), hh)
+    print(f"prefill stack output: end-to-end rel L2 {rl:.3e}")
+    assert np.all(np.isfinite(to_np(out))) and rl <= 1e-1
