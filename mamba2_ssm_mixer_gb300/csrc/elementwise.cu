@@ -67,89 +67,108 @@ cudaError_t launch_quant_e4m3(const uint16_t* x, size_t n, float scale, uint8_t*
 // read in place from the in_proj row (the split is addressing).  Taps before a
 // sequence's first token come from conv_state (has_initial) or are zero.
 //   u[t, c] = bf16(silu(b[c] + sum_j w[c, j] * x[t - 3 + j, c]))
-// One thread per channel pair and 16 consecutive tokens, the 3 previous
-// inputs kept in registers (a sliding window reset at sequence starts).
+// One CTA per tile of 64 tokens x 256 channels: the tile's rows plus the 3
+// rows before it are staged in shared memory with 16-byte asynchronous copies
+// (all of them in flight at once), then each thread runs one channel pair
+// over 32 consecutive tokens with the 3 previous inputs in registers (a
+// sliding window reset at sequence starts).
 // ---------------------------------------------------------------------------
-constexpr int kConvTokens = 16;
+constexpr int kCvT = 64;                 // tokens per tile
+constexpr int kCvC = 256;                // channels per tile
+constexpr int kCvRows = kCvT + kW - 1;   // staged rows: 3 before the tile + the tile
 
-__device__ __forceinline__ float4 ld_bf4(const uint16_t* p) {
-  const uint2 v = *reinterpret_cast<const uint2*>(p);
-  return make_float4(bfbits2f((uint16_t)(v.x & 0xFFFFu)), bfbits2f((uint16_t)(v.x >> 16)),
-                     bfbits2f((uint16_t)(v.y & 0xFFFFu)), bfbits2f((uint16_t)(v.y >> 16)));
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   (uint32_t)__cvta_generic_to_shared(dst_smem)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-// One thread per 4 channels and 16 consecutive tokens: the 16 inputs are
-// loaded up front (independent loads in flight), then the window slides.
-__global__ void __launch_bounds__(128) k_conv_silu_prefill(const uint16_t* __restrict__ zx,
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
+  return make_float2(bfbits2f((uint16_t)(v & 0xFFFFu)), bfbits2f((uint16_t)(v >> 16)));
+}
+
+__global__ void __launch_bounds__(256) k_conv_silu_prefill(const uint16_t* __restrict__ zx,
                                                            const uint16_t* __restrict__ conv_w,
                                                            const uint16_t* __restrict__ conv_b,
                                                            const uint16_t* __restrict__ conv_state,
                                                            const SeqInfo si, uint16_t* __restrict__ u) {
+  __shared__ __align__(16) uint16_t tile[kCvRows][kCvC];   // 33.5 KB
   pdl_wait();
   pdl_trigger();
-  const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-  const int t_begin = blockIdx.y * kConvTokens;
-  if (c >= kConv || t_begin >= si.total_tokens) return;
-  const int nt = min(kConvTokens, si.total_tokens - t_begin);
-  float w[4][kW], bias[4];
+  const int c0 = blockIdx.x * kCvC, t0 = blockIdx.y * kCvT, T = si.total_tokens;
+  // rows t0 - 3 .. t0 + 63 (rows outside [0, T) are never read: zero them)
+  for (int i = threadIdx.x; i < kCvRows * (kCvC / 8); i += blockDim.x) {
+    const int r = i / (kCvC / 8), q = i % (kCvC / 8);
+    const int t = t0 - (kW - 1) + r;
+    if (t >= 0 && t < T)
+      cp_async16(&tile[r][q * 8], zx + (size_t)t * kZ + kOffXBC + c0 + q * 8);
+    else
+      *reinterpret_cast<uint4*>(&tile[r][q * 8]) = make_uint4(0, 0, 0, 0);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
+  const int pr = threadIdx.x & (kCvC / 2 - 1), half = threadIdx.x / (kCvC / 2);
+  const int c = c0 + 2 * pr;
+  const int t_begin = t0 + half * (kCvT / 2);
+  if (t_begin >= T) return;
+  const int t_end = min(t_begin + kCvT / 2, T);
+  float w[2][kW], bias[2];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
+  for (int e = 0; e < 2; ++e) {
     bias[e] = conv_b ? bfbits2f(conv_b[c + e]) : 0.f;
 #pragma unroll
     for (int j = 0; j < kW; ++j) w[e][j] = bfbits2f(conv_w[(c + e) * kW + j]);
   }
-  float4 xs[kConvTokens];
-#pragma unroll
-  for (int i = 0; i < kConvTokens; ++i)
-    xs[i] = i < nt ? ld_bf4(zx + (size_t)(t_begin + i) * kZ + kOffXBC + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  // staged input of token t (t0 - 3 <= t < t0 + 64)
+  auto row = [&](int t) { return bf2_to_f2(*reinterpret_cast<const uint32_t*>(&tile[t - t0 + kW - 1][2 * pr])); };
   int s = seq_of_token(si, t_begin);
   int seq_start = si.cu_seqlens[s], seq_end = si.cu_seqlens[s + 1];
-  // win[k] = input at time t - 3 + k (k = 0, 1, 2) for the next token t
-  float4 win[kW - 1];
+  // window[k] = input at time t - 3 + k (k = 0, 1, 2) for the next token t
+  float2 win[kW - 1];
   auto load_window = [&](int t) {
     const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
 #pragma unroll
     for (int k = 0; k < kW - 1; ++k) {
       const int tt = t - (kW - 1) + k;
       if (tt >= seq_start) {
-        win[k] = ld_bf4(zx + (size_t)tt * kZ + kOffXBC + c);
+        win[k] = row(tt);
       } else if (init) {
         const int tap = (kW - 1) + (tt - seq_start);   // 0..2
         const uint16_t* st = conv_state + ((size_t)s * kConv + c) * (kW - 1);
-        win[k] = make_float4(bfbits2f(st[tap]), bfbits2f(st[3 + tap]), bfbits2f(st[6 + tap]), bfbits2f(st[9 + tap]));
+        win[k] = make_float2(bfbits2f(st[tap]), bfbits2f(st[(kW - 1) + tap]));
       } else {
-        win[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        win[k] = make_float2(0.f, 0.f);
       }
     }
   };
   load_window(t_begin);
-#pragma unroll
-  for (int i = 0; i < kConvTokens; ++i) {
-    if (i < nt) {
-      const int t = t_begin + i;
-      if (t == seq_end) {   // first token of the next sequence
-        ++s;
-        seq_start = seq_end;
-        seq_end = si.cu_seqlens[s + 1];
-        load_window(t);
-      }
-      const float4 x = xs[i];
-      const float in[4][kW] = {{win[0].x, win[1].x, win[2].x, x.x}, {win[0].y, win[1].y, win[2].y, x.y},
-                               {win[0].z, win[1].z, win[2].z, x.z}, {win[0].w, win[1].w, win[2].w, x.w}};
-      uint16_t o[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        float acc = bias[e];
-#pragma unroll
-        for (int j = 0; j < kW; ++j) acc = fmaf(w[e][j], in[e][j], acc);
-        o[e] = f2bfbits(silu_f(acc));
-      }
-      *reinterpret_cast<uint2*>(u + (size_t)t * kConv + c) =
-          make_uint2((uint32_t)o[0] | ((uint32_t)o[1] << 16), (uint32_t)o[2] | ((uint32_t)o[3] << 16));
-      win[0] = win[1];
-      win[1] = win[2];
-      win[2] = x;
+  for (int t = t_begin; t < t_end; ++t) {
+    if (t == seq_end) {   // first token of the next sequence
+      ++s;
+      seq_start = seq_end;
+      seq_end = si.cu_seqlens[s + 1];
+      load_window(t);
     }
+    const float2 x = row(t);
+    float a0 = bias[0], a1 = bias[1];
+    a0 = fmaf(w[0][0], win[0].x, a0);
+    a1 = fmaf(w[1][0], win[0].y, a1);
+    a0 = fmaf(w[0][1], win[1].x, a0);
+    a1 = fmaf(w[1][1], win[1].y, a1);
+    a0 = fmaf(w[0][2], win[2].x, a0);
+    a1 = fmaf(w[1][2], win[2].y, a1);
+    a0 = fmaf(w[0][3], x.x, a0);
+    a1 = fmaf(w[1][3], x.y, a1);
+    *reinterpret_cast<uint32_t*>(u + (size_t)t * kConv + c) =
+        (uint32_t)f2bfbits(silu_f(a0)) | ((uint32_t)f2bfbits(silu_f(a1)) << 16);
+    win[0] = win[1];
+    win[1] = win[2];
+    win[2] = x;
   }
 }
 
@@ -182,8 +201,9 @@ __global__ void __launch_bounds__(256) k_conv_state_update(const uint16_t* __res
 
 cudaError_t launch_conv_silu_prefill(const uint16_t* zx, const BlockParams& bp, const uint16_t* conv_state,
                                      const SeqInfo& si, uint16_t* u, cudaStream_t st) {
-  dim3 grid((kConv / 4 + 127) / 128, (si.total_tokens + kConvTokens - 1) / kConvTokens);
-  return launch_pdl(k_conv_silu_prefill, grid, dim3(128), 0, st, zx, bp.conv_w, bp.conv_b, conv_state, si, u);
+  static_assert(kConv % kCvC == 0, "conv tiles cover the channels exactly");
+  dim3 grid(kConv / kCvC, (si.total_tokens + kCvT - 1) / kCvT);
+  return launch_pdl(k_conv_silu_prefill, grid, dim3(kCvC), 0, st, zx, bp.conv_w, bp.conv_b, conv_state, si, u);
 }
 
 cudaError_t launch_conv_state_update(const uint16_t* zx, uint16_t* conv_state, const SeqInfo& si,

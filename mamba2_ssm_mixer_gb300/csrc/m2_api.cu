@@ -309,7 +309,6 @@ struct PrefillWs {
   uint16_t* u;
   CumDt* cumdt;
   float* states;
-  uint8_t* xt_img;
   uint8_t* sin_img;
   uint16_t* y;
   uint8_t* q2;
@@ -326,7 +325,6 @@ static PrefillWs carve_prefill(void* base, int T, int chunks) {
   w.u = c.take<uint16_t>((size_t)T * kConv);
   w.cumdt = c.take<CumDt>((size_t)chunks * kNH * kChunk);
   w.states = c.take<float>((size_t)chunks * kNH * kP * kN);
-  w.xt_img = c.take<uint8_t>((size_t)chunks * kNH * kXtImageBytes);
   w.sin_img = c.take<uint8_t>((size_t)chunks * kNH * kSinImageBytes);
   w.y = c.take<uint16_t>((size_t)T * kI);
   w.q2 = c.take<uint8_t>((size_t)T * kI);
@@ -380,11 +378,11 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
   M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1,
            launch_ssd_cumsum(w.zx, bp, local, w.cumdt, h->taps_on ? h->taps.dt : nullptr, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
-           launch_ssd_chunk_state_tc(w.u, w.cumdt, local, w.states, w.xt_img, h->err, st));
+           launch_ssd_chunk_state_tc(w.u, w.cumdt, local, w.states, h->err, st));
   M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
            launch_ssd_state_pass(w.states, w.cumdt, local, w.sin_img, ssm_state, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
-           launch_ssd_chunk_scan_tc(w.u, w.cumdt, w.xt_img, w.sin_img, bp, local, w.y, h->err, st));
+           launch_ssd_chunk_scan_tc(w.u, w.cumdt, w.sin_img, bp, local, w.y, h->err, st));
   M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
            launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, h->taps_on ? h->taps.o : nullptr, st));
   M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));

@@ -37,16 +37,16 @@ cudaError_t launch_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint
                                     uint16_t* normed, int T, int n, cudaStream_t st);
 
 // ssd.cu
-// Per (chunk, head, token of the chunk): the in-chunk cumulative log-decay as
-// an unevaluated (hi, lo) float pair and dt; zeros past the chunk's end.
-// Stored [chunk][head][256] so one head's chunk is 4 KB contiguous.
+// Per (chunk, head, token s of the chunk): the in-chunk cumulative log-decay
+// cum_s as an unevaluated (hi, lo) float pair, dt_s, and the source factor
+// colf_s = dt_s exp(cum_e - cum_s) with e the last token of s's 32-token block
+// (<= dt_s: cum never increases); zeros past the chunk's end.  Stored
+// [chunk][head][256] so one head's chunk is 4 KB contiguous.
 struct CumDt {
-  float hi, lo, dt, pad;
+  float hi, lo, dt, colf;
 };
-// Bytes of one (chunk, head) operand image: x^T [64 p][256 s] bf16 in the MMA's
-// K-major 128-byte-swizzled layout, and S_in as bf16 high + remainder
-// [2][64 p][128 n] in the same layout.
-constexpr int kXtImageBytes = 64 * 256 * 2;
+// Bytes of one (chunk, head) S_in operand image: bf16 high part and remainder
+// [2][64 p][128 n] in the MMA's K-major 128-byte-swizzled layout.
 constexpr int kSinImageBytes = 2 * 64 * 128 * 2;
 
 // dt_tok (optional, may be null): dt as [T, 64] for the intermediate taps.
@@ -58,13 +58,12 @@ cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const
                                   float* ssm_state, cudaStream_t st);
 
 // ssd_tc.cu (tensor-core chunk states and chunk scan)
-// Chunk states f32 [chunk][head][64][128]; also writes each (chunk, head)'s
-// x^T image for the scan.
+// Chunk states f32 [chunk][head][64][128].
 cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const CumDt* cumdt, const SeqInfo& si, float* states,
-                                      uint8_t* xt_img, int* err, cudaStream_t st);
-cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const CumDt* cumdt, const uint8_t* xt_img,
-                                     const uint8_t* sin_img, const BlockParams& bp, const SeqInfo& si, uint16_t* y,
-                                     int* err, cudaStream_t st);
+                                      int* err, cudaStream_t st);
+cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const CumDt* cumdt, const uint8_t* sin_img,
+                                     const BlockParams& bp, const SeqInfo& si, uint16_t* y, int* err,
+                                     cudaStream_t st);
 
 // decode_tma.cu (persistent, TMA-streamed state)
 cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,

@@ -32,42 +32,62 @@ __device__ __forceinline__ ChunkPos chunk_pos(const SeqInfo& si, int c) {
 
 // 1. dt and the in-chunk cumulative log-decay.  One CTA (256 threads) per
 // (chunk, head); thread i owns token i of the chunk.  The cumulative sum is
-// formed in double and stored as an unevaluated pair of floats (hi, lo):
-// within a chunk it reaches |cum| ~ 400 for fast-decaying heads, and the
+// carried as an unevaluated pair of floats (hi, lo) with error-free additions
+// (Knuth's two-sum, folded as in double-float arithmetic), ~48 significant
+// bits: within a chunk it reaches |cum| ~ 400 for fast-decaying heads, and the
 // decay factors are exponentials of differences of two such sums, which a
-// single float would leave with ~1e-4 relative error.
+// single float would leave with ~1e-4 relative error.  (Float pairs rather
+// than double: this part's FP64 rate is a small fraction of its FP32 rate.)
+namespace {
+struct FF {
+  float hi, lo;
+};
+__device__ __forceinline__ FF ff_add(FF a, FF b) {
+  const float s = a.hi + b.hi;
+  const float bb = s - a.hi;
+  const float e = (a.hi - (s - bb)) + (b.hi - bb);   // s + e == a.hi + b.hi exactly
+  const float l = e + (a.lo + b.lo);
+  const float h = s + l;
+  return {h, l - (h - s)};
+}
+}  // namespace
+
 __global__ void __launch_bounds__(256) k_ssd_cumsum(const uint16_t* __restrict__ zx, const float* __restrict__ A_log,
                                                     const float* __restrict__ dt_bias, const SeqInfo si,
                                                     CumDt* __restrict__ cumdt, float* __restrict__ dt_tok) {
-  __shared__ double wsum[8];
+  __shared__ FF wsum[8];
+  __shared__ FF cums[kChunk];
   pdl_wait();
   pdl_trigger();
   const int c = blockIdx.x, h = blockIdx.y, i = threadIdx.x;
   const ChunkPos cp = chunk_pos(si, c);
   const float A = -expf(A_log[h]);
   float dt = 0.f;
-  double a = 0.0;
+  FF v = {0.f, 0.f};
   if (i < cp.n) {
     dt = softplus_f(bfbits2f(zx[(size_t)(cp.t0 + i) * kZ + kOffDt + h]) + dt_bias[h]);
-    a = (double)(dt * A);
+    v.hi = dt * A;
   }
-  // inclusive block scan in double
-  double v = a;
+  // inclusive block scan
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double n = __shfl_up_sync(0xffffffffu, v, o);
-    if ((i & 31) >= o) v += n;
+    const FF n = {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+    if ((i & 31) >= o) v = ff_add(v, n);
   }
   if ((i & 31) == 31) wsum[i >> 5] = v;
   __syncthreads();
-  double pre = 0.0;
-  for (int w = 0; w < (i >> 5); ++w) pre += wsum[w];
-  v += pre;
+  FF pre = {0.f, 0.f};
+  for (int w = 0; w < (i >> 5); ++w) pre = ff_add(pre, wsum[w]);
+  v = ff_add(v, pre);
+  cums[i] = v;
+  __syncthreads();
   CumDt r = {0.f, 0.f, 0.f, 0.f};
   if (i < cp.n) {
-    r.hi = (float)v;
-    r.lo = (float)(v - (double)r.hi);
+    r.hi = v.hi;
+    r.lo = v.lo;
     r.dt = dt;
+    const FF ce = cums[min(i | 31, cp.n - 1)];            // last token of this 32-token block
+    r.colf = dt * expf((ce.hi - v.hi) + (ce.lo - v.lo));  // exponent <= 0
     if (dt_tok) dt_tok[(size_t)(cp.t0 + i) * kNH + h] = dt;
   }
   cumdt[((size_t)c * kNH + h) * kChunk + i] = r;

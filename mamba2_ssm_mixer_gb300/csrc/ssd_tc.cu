@@ -2,25 +2,28 @@
 // prefill SSD scan (Mamba2ChunkScan of vllm.cpp PR #1288, "What it does"; SSD
 // block decomposition of Dao & Gu 2024):
 //
-// k_ssd_state_tc  one CTA per (chunk, group), 8 warps: for each of the group's
-//   8 heads  S_c[n, p] = sum_t B[t, n] (w_t x[t, p]),  w_t = exp(cum_last - cum_t) dt_t,
-//   a 128 x 64 x 256 MMA.  w x is split into a bf16 high part and a bf16
-//   remainder (two MMAs) so the chunk state keeps ~16 bits.  Staging of head
-//   h + 1 overlaps the MMA of head h (double-buffered operands and TMEM).  It
-//   also writes each head's x^T tile exactly as the scan's MMA reads it from
-//   shared memory, so the scan fetches it with one bulk copy.
-// k_ssd_scan_tc   one CTA per (chunk, group, 128-row half of the chunk),
-//   warp-specialised: warp 0 loads (TMA for the C and B tiles, bulk copies of
-//   the per-head x^T image, S_in image and cum/dt record, one head ahead);
-//   warp 1 issues the MMAs; warps 2-9 build P and run the epilogue.
+// k_ssd_state_tc  one CTA per (chunk, group): a loader warp brings the B tile
+//   and, one head ahead, each head's x tile in by TMA; both stay in the layout
+//   TMA writes ([tokens][64 columns], 128-byte swizzle) and feed the MMA as
+//   MN-major operands, so nothing is transposed.  For each of the group's 8
+//   heads, S_c[n, p] = sum_t B[t, n] (w_t x[t, p]) with
+//   w_t = exp(cum_last - cum_t) dt_t is a 128 x 64 x 256 MMA; worker thread t
+//   scales its token row by w_t and splits it into a bf16 high part and a bf16
+//   remainder (two MMAs) so the chunk state keeps ~16 bits; head h's epilogue
+//   overlaps head h+1's staging.
+// k_ssd_scan_tc   one CTA per (128-row half of the chunk, chunk, group),
+//   warp-specialised: warp 0 loads (TMA for the C, B and per-head x tiles,
+//   bulk copies of the S_in image and cum/dt record, one head ahead); warp 1
+//   issues the MMAs; warps 2-9 build P and run the epilogue.
 //     G = C B^T                      once per CTA (128 x 256 x 128)
 //     P[t, s] = G[t, s] exp(cum_t - cum_s) dt_s   (s <= t, else 0)
 //     Y_diag = P x,  Y_off = C S_in^T,  y = Y_diag + exp(cum_t) Y_off + D x
 //   P and S_in are split into bf16 high part + remainder (a single bf16
 //   rounding of P gives y a ~1e-3 relative error, enough to flip e4m3 codes of
 //   the out_proj input downstream).  P is produced in 32-source blocks into a
-//   double buffer that the MMA warp consumes; the Y accumulators are
-//   double-buffered in TMEM so head h's epilogue overlaps head h+1's MMAs.
+//   double buffer that the MMA warp consumes; x is the MMA's N-major operand
+//   as TMA wrote it; the Y accumulators are double-buffered in TMEM so head
+//   h's epilogue overlaps head h+1's MMAs.
 // Every wait is bounded; a wait that runs out raises the device error word and
 // a CTA-wide abort flag that makes the remaining waits return at once.
 #include <cudaTypedefs.h>
@@ -49,17 +52,6 @@ __device__ __forceinline__ uint32_t bf2(float a, float b) {
 __device__ __forceinline__ uint16_t h16(const uint4& v, int j) {
   const uint32_t w = (j < 2) ? v.x : (j < 4) ? v.y : (j < 6) ? v.z : v.w;
   return (uint16_t)((j & 1) ? (w >> 16) : (w & 0xFFFFu));
-}
-
-// 8 x 8 bf16 transpose: in[i] holds row i (8 values); out[j] holds column j.
-__device__ __forceinline__ void transpose8(const uint4 (&in)[8], uint4 (&out)[8]) {
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    uint32_t w[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = (uint32_t)h16(in[2 * q], j) | ((uint32_t)h16(in[2 * q + 1], j) << 16);
-    out[j] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
 }
 
 struct ChunkPos {
@@ -94,134 +86,166 @@ __device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) 
 // ---------------------------------------------------------------------------
 // chunk states
 // ---------------------------------------------------------------------------
-constexpr int kStThr = 256;
-constexpr int kWBuf = 2 * 64 * 256 * 2;   // one operand buffer: hi + lo [64 p][256 t]
+constexpr int kStWork = 256;             // 8 worker warps; worker thread t owns token row t
+constexpr int kStThr = kStWork + 32;     // + a loader warp
+constexpr int kStSmB = 0;                // B [2 slices of 64 n][256 t][64] as TMA writes it   64 KB
+constexpr int kStSmX = 64 * 1024;        // x [2 buffers][256 t][64 p] as TMA writes it        64 KB
+constexpr int kStSmW = 128 * 1024;       // w x, bf16 high then remainder, [256 t][64 p] each 64 KB
+constexpr int kStSmBar = 192 * 1024;
+constexpr int kStSmem = kStSmBar + 128 + 1024;
+
+struct StateBars {
+  uint64_t b_full, x_full[2], x_empty[2], mma[2], drain;
+  uint32_t tslot;
+  int abort;
+};
+
+// 16-byte chunk c (0..7) of row r in a 128-byte-swizzled tile with 128-byte
+// rows (what TMA writes with CU_TENSOR_MAP_SWIZZLE_128B)
+__device__ __forceinline__ uint32_t sw_row_chunk(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
 
 __global__ void __launch_bounds__(kStThr, 1)
-    k_ssd_state_tc(const uint16_t* __restrict__ u, const CumDt* __restrict__ cumdt, const SeqInfo si,
-                   float* __restrict__ states, uint8_t* __restrict__ xt_img, int* err) {
+    k_ssd_state_tc(const __grid_constant__ CUtensorMap tm_u, const CumDt* __restrict__ cumdt, const SeqInfo si,
+                   float* __restrict__ states, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sBT = smem;                       // [128 n][256 t]   64 KB
-  uint8_t* sW = sBT + 128 * 256 * 2;         // [2 buffers] x (hi, lo)   2 x 64 KB
-  float* wts = reinterpret_cast<float*>(sW + 2 * kWBuf);    // [2][256]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(wts + 2 * kChunk);   // [2]
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
-  int* abortp = reinterpret_cast<int*>(tslot + 1);
-  volatile int* abort = abortp;
+  StateBars* sb = reinterpret_cast<StateBars*>(smem + kStSmBar);
+  volatile int* abort = &sb->abort;
+  uint8_t* sB = smem + kStSmB;
+  uint8_t* sX = smem + kStSmX;
+  uint8_t* sWh = smem + kStSmW;
+  uint8_t* sWl = sWh + 32 * 1024;
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, side = warp >> 2;
   const ChunkPos cp = chunk_of(si, c);
-  constexpr uint32_t IDESC = idesc_f32acc(128, 64, 1u);   // bf16 x bf16 -> f32, M = 128 (n), N = 64 (p)
+  // bf16 x bf16 -> f32, M = 128 (n), N = 64 (p), both operands MN-major
+  constexpr uint32_t IDESC = idesc_f32acc_mn(128, 64, 1u, true, true);
 
   if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    *abortp = 0;
+    mbar_init(&sb->b_full, 1);
+    mbar_init(&sb->drain, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&sb->x_full[k], 1);
+      mbar_init(&sb->x_empty[k], kStWork / 32);
+      mbar_init(&sb->mma[k], 1);
+    }
+    sb->abort = 0;
     fence_mbar_init();
+    tma_prefetch(&tm_u);
   }
   if (warp == 0) {
-    tmem_alloc(tslot, 128);
+    tmem_alloc(&sb->tslot, 128);
     tc_fence_before();
-  }
-  pdl_wait();
-  pdl_trigger();
-  // B^T: rows n, K = t.  8 x 8 blocks: 32 (t) x 16 (n) = 512 blocks.
-  for (int blk = tid; blk < 512; blk += kStThr) {
-    const int tb = blk >> 4, nb = blk & 15;
-    uint4 in[8], out[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = tb * 8 + i;
-      in[i] = t < cp.n ? *reinterpret_cast<const uint4*>(u + (size_t)(cp.t0 + t) * kConv + kOffB + g * kN + nb * 8)
-                       : make_uint4(0, 0, 0, 0);
-    }
-    transpose8(in, out);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) *reinterpret_cast<uint4*>(sBT + sw_chunk(nb * 8 + j, tb, 128)) = out[j];
   }
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tslot;
+  const uint32_t tmem = sb->tslot;
+  pdl_wait();
+  pdl_trigger();
 
-  // read the accumulator of head hd and write its chunk state
-  auto epilogue = [&](int hd) {
-    const int k = hd & 1;
-    const bool ok = wait_ab(&bar[k], (hd >> 1) & 1, abort, err);
-    tc_fence_after();
-    // D[n = 32 quarter + lane][p] -> states[c][h][p][n]; warps 0-3 take p < 32,
-    // warps 4-7 p >= 32
-    float* out = states + ((size_t)c * kNH + g * kHPG + hd) * (kP * kN) + quarter * 32 + lane;
-    uint32_t r[32];
-    tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(k * 64 + side * 32), r);
-    tmem_ld_wait();
-    if (ok) {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) out[(size_t)(side * 32 + j) * kN] = __uint_as_float(r[j]);
-    }
-    tc_fence_before();
-  };
-
-  for (int hh = 0; hh < kHPG; ++hh) {
-    const int h = g * kHPG + hh, k = hh & 1;
-    uint8_t* sWh = sW + k * kWBuf;
-    uint8_t* sWl = sWh + kWBuf / 2;
-    float* w = wts + k * kChunk;
-    const CumDt* cd = cumdt + ((size_t)c * kNH + h) * kChunk;
-    const CumDt cl = cd[cp.n - 1];
-    for (int t = tid; t < kChunk; t += kStThr) {
-      const CumDt ct = cd[t];
-      w[t] = t < cp.n ? expf((cl.hi - ct.hi) + (cl.lo - ct.lo)) * ct.dt : 0.f;
-    }
-    __syncthreads();
-    // x^T (rows p, K = t): written to the scan's image as is, and scaled by w
-    // into the hi / lo operands here.  32 (t) x 8 (p) blocks of 8 x 8.
-    uint8_t* img = xt_img + ((size_t)c * kNH + h) * kXtImageBytes;
-    for (int blk = tid; blk < 256; blk += kStThr) {
-      const int tb = blk >> 3, pb = blk & 7;
-      uint4 in[8], out[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int t = tb * 8 + i;
-        in[i] = t < cp.n ? *reinterpret_cast<const uint4*>(u + (size_t)(cp.t0 + t) * kConv + h * kP + pb * 8)
-                         : make_uint4(0, 0, 0, 0);
+  if (warp == kStWork / 32) {
+    // ------------------------------------------------ loader
+    if (lane == 0) {
+      // B: two 64-column slices of 256 rows (rows past the chunk are other
+      // tokens or zeros; their products vanish because w = 0 there)
+      mbar_expect_tx(&sb->b_full, 256 * 128 * 2);
+      for (int a = 0; a < 2; ++a)
+        tma_load_2d(sB + a * 256 * 128, &tm_u, &sb->b_full, kOffB + g * kN + a * 64, cp.t0);
+      bool issued[2] = {false, false};
+      uint32_t par[2] = {0, 0};
+      for (int hh = 0; hh < kHPG; ++hh) {
+        const int k = hh & 1;
+        if (!wait_ab(&sb->x_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
+        mbar_expect_tx(&sb->x_full[k], 256 * 64 * 2);
+        tma_load_2d(sX + k * 32 * 1024, &tm_u, &sb->x_full[k], (g * kHPG + hh) * kP, cp.t0);
+        issued[k] = true;
+        par[k] = (hh >> 1) & 1;
       }
-      transpose8(in, out);
-      float wv[8];
+      if (*abort) {   // let copies in flight land before the CTA can exit
+        mbar_wait(&sb->b_full, 0, nullptr, 100000000ull);
+        for (int k = 0; k < 2; ++k)
+          if (issued[k]) mbar_wait(&sb->x_full[k], par[k], nullptr, 100000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------ workers (8 warps)
+    const int quarter = warp & 3, side = warp >> 2;
+    const int t = tid;
+    const CumDt* cd0 = cumdt + ((size_t)c * kNH + g * kHPG) * kChunk;
+    CumDt ct = cd0[t], cl = cd0[cp.n - 1];   // this head's; the next head's are fetched one head ahead
+    bool ok = wait_ab(&sb->b_full, 0, abort, err);
+
+    auto epilogue = [&](int hd) {
+      const int k = hd & 1;
+      const bool okm = wait_ab(&sb->mma[k], (hd >> 1) & 1, abort, err);
+      tc_fence_after();
+      // D[n = 32 quarter + lane][p] -> states[c][h][p][n]; warps 0-3 take p < 32,
+      // warps 4-7 p >= 32
+      float* out = states + ((size_t)c * kNH + g * kHPG + hd) * (kP * kN) + quarter * 32 + lane;
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(k * 64 + side * 32), r);
+      tmem_ld_wait();
+      if (ok && okm) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) wv[i] = w[tb * 8 + i];
+        for (int j = 0; j < 32; ++j) out[(size_t)(side * 32 + j) * kN] = __uint_as_float(r[j]);
+      }
+      tc_fence_before();
+    };
+
+    for (int hh = 0; hh < kHPG; ++hh) {
+      const int k = hh & 1;
+      // w_t = exp(cum_last - cum_t) dt_t; zero past the chunk's end
+      const float w = t < cp.n ? expf((cl.hi - ct.hi) + (cl.lo - ct.lo)) * ct.dt : 0.f;
+      if (hh + 1 < kHPG) {
+        ct = cd0[(hh + 1) * kChunk + t];
+        cl = cd0[(hh + 1) * kChunk + cp.n - 1];
+      }
+      ok = wait_ab(&sb->x_full[k], (hh >> 1) & 1, abort, err) && ok;
+      const uint8_t* xs = sX + k * 32 * 1024;
+      uint4 xv[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t off = sw_chunk(pb * 8 + j, tb, 64);
-        *reinterpret_cast<uint4*>(img + off) = out[j];
+      for (int q = 0; q < 8; ++q) xv[q] = *reinterpret_cast<const uint4*>(xs + sw_row_chunk(t, q));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb->x_empty[k]);   // this warp's reads of the x tile are done
+      // the single (w x) buffer is free once head hh-1's MMA has finished
+      if (hh > 0) epilogue(hh - 1);
+      // row t of (w x), bf16 high part and remainder, in the x tile's own layout
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
         uint16_t hi[8], lo[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) split_bf16(wv[i] * bfbits2f(h16(out[j], i)), hi[i], lo[i]);
+        for (int e = 0; e < 8; ++e) split_bf16(w * bfbits2f(h16(xv[q], e)), hi[e], lo[e]);
+        const uint32_t off = sw_row_chunk(t, q);
         *reinterpret_cast<uint4*>(sWh + off) = *reinterpret_cast<const uint4*>(hi);
         *reinterpret_cast<uint4*>(sWl + off) = *reinterpret_cast<const uint4*>(lo);
       }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(sBT), h0 = smem_u32(sWh), l0 = smem_u32(sWl);
-      const uint32_t d = tmem + (uint32_t)(k * 64);
+      fence_proxy_async_smem();
+      asm volatile("bar.sync 1, %0;" ::"n"(kStWork) : "memory");
+      if (tid == 0) {
+        // S[n, p] += sum_t B[t, n] (w x)[t, p]: 16 K-steps of 16 tokens
+        // (2048 bytes of both tiles); B's two 64-column slices are 32 KB apart
+        tc_fence_after();
+        const uint32_t b0 = smem_u32(sB), h0 = smem_u32(sWh), l0 = smem_u32(sWl);
+        const uint32_t d = tmem + (uint32_t)(k * 64);
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint64_t ad = desc_kmajor_sw128(a0 + a * 128 * 128) + 2 * j;
-          mma_f16(d, ad, desc_kmajor_sw128(h0 + a * 64 * 128) + 2 * j, IDESC, (a | j) != 0);
-          mma_f16(d, ad, desc_kmajor_sw128(l0 + a * 64 * 128) + 2 * j, IDESC, 1u);
+        for (int ks = 0; ks < 16; ++ks) {
+          const uint64_t ad = desc_mnmajor_sw128(b0 + ks * 2048, 256 * 128);
+          mma_f16(d, ad, desc_mnmajor_sw128(h0 + ks * 2048, 1024), IDESC, ks != 0);
+          mma_f16(d, ad, desc_mnmajor_sw128(l0 + ks * 2048, 1024), IDESC, 1u);
         }
-      mma_commit(&bar[k]);
+        mma_commit(&sb->mma[k]);
+      }
+      __syncwarp();
     }
-    __syncwarp();
-    if (hh > 0) epilogue(hh - 1);   // overlaps the MMA just issued
+    epilogue(kHPG - 1);
+    if (tid == 0 && *abort) {   // no MMA may still be running when TMEM is freed
+      mma_commit(&sb->drain);
+      mbar_wait(&sb->drain, 0, nullptr, 100000000ull);
+    }
   }
-  epilogue(kHPG - 1);
+  __syncwarp();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
@@ -238,7 +262,7 @@ constexpr int kScP = 256;     // P / epilogue threads
 // shared-memory map (bytes from the 1024-aligned base)
 constexpr int kSmC = 0;                // C   [128 t][128 n]                 32 KB
 constexpr int kSmB = 32 * 1024;        // B   [KS s][128 n] 64 KB; after G: operand buffer 1
-constexpr int kSmOp0 = 96 * 1024;      // operand buffer 0: x^T 32 KB + S_in hi/lo 32 KB
+constexpr int kSmOp0 = 96 * 1024;      // operand buffer 0: x [256 s][64 p] 32 KB + S_in hi/lo 32 KB
 constexpr int kSmP = 160 * 1024;       // P   hi atom [128][64] 16 KB + lo atom 16 KB
 constexpr int kSmCD = 192 * 1024;      // CumDt [2][256]                     8 KB
 constexpr int kSmBar = 200 * 1024;     // barriers
@@ -254,8 +278,7 @@ struct ScanBars {
 };
 
 __global__ void __launch_bounds__(kScThr, 1)
-    k_ssd_scan_tc(const __grid_constant__ CUtensorMap tm_u, const uint16_t* __restrict__ u,
-                  const CumDt* __restrict__ cumdt, const uint8_t* __restrict__ xt_img,
+    k_ssd_scan_tc(const __grid_constant__ CUtensorMap tm_u, const CumDt* __restrict__ cumdt,
                   const uint8_t* __restrict__ sin_img, const float* __restrict__ Dp, const SeqInfo si,
                   uint16_t* __restrict__ y, int* err) {
   extern __shared__ uint8_t smem_raw[];
@@ -263,13 +286,16 @@ __global__ void __launch_bounds__(kScThr, 1)
   ScanBars* sb = reinterpret_cast<ScanBars*>(smem + kSmBar);
   volatile int* abort = &sb->abort;
 
-  const int c = blockIdx.x, g = blockIdx.y, tb = blockIdx.z, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // the two halves of a (chunk, group) are neighbours in launch order, so the
+  // second one's reads of B, x, S_in and cum/dt hit L2
+  const int tb = blockIdx.x, c = blockIdx.y, g = blockIdx.z, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const ChunkPos cp = chunk_of(si, c);
   if (tb * 128 >= cp.n) return;
   const int KS = (tb + 1) * 128;       // sources s < KS (causal)
   const int NBLK = KS / 32;            // 32-source P blocks per head
   constexpr uint32_t TMEM_COLS = 512;  // G [0, 256); Y_diag[k] at 256 + 128 k, Y_off[k] at 320 + 128 k
-  constexpr uint32_t IDESC_Y = idesc_f32acc(128, 64, 1u);
+  constexpr uint32_t IDESC_Y = idesc_f32acc(128, 64, 1u);               // C S_in^T: both K-major
+  constexpr uint32_t IDESC_PX = idesc_f32acc_mn(128, 64, 1u, false, true);  // P x: x as TMA writes it
 
   if (tid == 0) {
     mbar_init(&sb->cb, 1);
@@ -310,7 +336,7 @@ __global__ void __launch_bounds__(kScThr, 1)
           tma_load_2d(smem + kSmB + a * KS * 128 + rb * 128 * 128, &tm_u, &sb->cb, kOffB + g * kN + a * 64,
                       cp.t0 + rb * 128);
       }
-      const uint32_t xt_bytes = (uint32_t)(KS / 64) * (64 * 128);
+      const uint32_t x_bytes = (uint32_t)KS * 128;   // x [KS s][64 p]
       bool issued[2] = {false, false};
       uint32_t issued_par[2] = {0, 0};
       for (int hh = 0; hh < kHPG; ++hh) {
@@ -318,8 +344,9 @@ __global__ void __launch_bounds__(kScThr, 1)
         if (hh == 1 && !wait_ab(&sb->g, 0, abort, err)) break;   // buffer 1 is the B tile's memory
         if (!wait_ab(&sb->op_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
         uint8_t* ob = smem + (k == 0 ? kSmOp0 : kSmB);
-        mbar_expect_tx(&sb->op_full[k], xt_bytes + (uint32_t)kSinImageBytes + (uint32_t)(kChunk * sizeof(CumDt)));
-        bulk_g2s(ob, xt_img + (ch0 + hh) * kXtImageBytes, xt_bytes, &sb->op_full[k]);
+        mbar_expect_tx(&sb->op_full[k], x_bytes + (uint32_t)kSinImageBytes + (uint32_t)(kChunk * sizeof(CumDt)));
+        for (int rb = 0; rb < KS / 128; ++rb)
+          tma_load_2d(ob + rb * 128 * 128, &tm_u, &sb->op_full[k], (g * kHPG + hh) * kP, cp.t0 + rb * 128);
         bulk_g2s(ob + 32 * 1024, sin_img + (ch0 + hh) * kSinImageBytes, kSinImageBytes, &sb->op_full[k]);
         bulk_g2s(smem + kSmCD + k * 4096, cumdt + (ch0 + hh) * kChunk, kChunk * sizeof(CumDt), &sb->op_full[k]);
         issued[k] = true;
@@ -373,14 +400,14 @@ __global__ void __launch_bounds__(kScThr, 1)
             break;
           }
           tc_fence_after();
-          // block j: sources [32 j, 32 j + 32) = half (j & 1) of x^T atom j / 2;
-          // P block b = half b of the P atoms
+          // block j: sources [32 j, 32 j + 32) = x rows 32 j.. (4096 bytes per
+          // block, 2048 per 16-source K-step); P block b = half b of the P atoms
 #pragma unroll
           for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t xd = desc_kmajor_sw128(x0 + (j >> 1) * 64 * 128) + (uint64_t)((j & 1) * 4 + kk * 2);
+            const uint64_t xd = desc_mnmajor_sw128(x0 + j * 4096 + kk * 2048, 1024);
             const uint64_t pofs = (uint64_t)(b * 4 + kk * 2);
-            mma_f16(yd, desc_kmajor_sw128(ph0) + pofs, xd, IDESC_Y, (j | kk) != 0);
-            mma_f16(yd, desc_kmajor_sw128(pl0) + pofs, xd, IDESC_Y, 1u);
+            mma_f16(yd, desc_kmajor_sw128(ph0) + pofs, xd, IDESC_PX, (j | kk) != 0);
+            mma_f16(yd, desc_kmajor_sw128(pl0) + pofs, xd, IDESC_PX, 1u);
           }
           mma_commit(&sb->p_empty[b]);
         }
@@ -420,16 +447,32 @@ __global__ void __launch_bounds__(kScThr, 1)
         uint32_t r[16];
         tmem_ld_32x32b_x16(lane_base + (uint32_t)s0, r);
         tmem_ld_wait();
+        // The warp's 32 rows are the 32-token block [tb*128 + 32 quarter, +32);
+        // relative to source block j it is below the diagonal, on it, or above
+        // it (all zero).  Below: exp(cum_t - cum_s) = exp(cum_t - cum_e)
+        // exp(cum_e - cum_s), both factors <= 1 with e the block's last source
+        // (the second, times dt_s, is colf_s).  On it: one exp per element.
+        const int rblk = tb * 4 + quarter;   // this warp's 32-token block
         uint16_t hi[16], lo[16];
+        if (j < rblk) {
+          const CumDt ce = cd[min(j * 32 + 31, cp.n - 1)];
+          const float rf = tt < cp.n ? __expf((ct.hi - ce.hi) + (ct.lo - ce.lo)) : 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int s = s0 + e;
-          float v = 0.f;
-          if (s <= tlim) {
-            const CumDt cs = cd[s];
-            v = __uint_as_float(r[e]) * __expf((ct.hi - cs.hi) + (ct.lo - cs.lo)) * cs.dt;
+          for (int e = 0; e < 16; ++e) split_bf16(__uint_as_float(r[e]) * rf * cd[s0 + e].colf, hi[e], lo[e]);
+        } else if (j == rblk) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int s = s0 + e;
+            float v = 0.f;
+            if (s <= tlim) {
+              const CumDt cs = cd[s];
+              v = __uint_as_float(r[e]) * __expf((ct.hi - cs.hi) + (ct.lo - cs.lo)) * cs.dt;
+            }
+            split_bf16(v, hi[e], lo[e]);
           }
-          split_bf16(v, hi[e], lo[e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0;
         }
         // 16 sources = two 16-byte chunks: chunk index inside the 64-source
         // atom row is b * 4 + side * 2 (+1)
@@ -455,11 +498,12 @@ __global__ void __launch_bounds__(kScThr, 1)
         tmem_ld_32x32b_x32(lane_base + 320 + 128 * k + (uint32_t)(side * 32), ro);
         tmem_ld_wait();
         if (ok && tt < cp.n) {
-          const uint16_t* xr = u + (size_t)(cp.t0 + tt) * kConv + h * kP + side * 32;
+          // x[tt, p] from the operand buffer's x tile (row tt, 16-byte chunk p / 8)
+          const uint8_t* xrow = smem + (k == 0 ? kSmOp0 : kSmB);
           uint16_t* yr = y + (size_t)(cp.t0 + tt) * kI + h * kP + side * 32;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xr + q * 8);
+            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + sw_row_chunk(tt, side * 4 + q));
             uint32_t o[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -493,16 +537,6 @@ __global__ void __launch_bounds__(kScThr, 1)
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-static size_t state_smem() { return 1024 + 128 * 256 * 2 + 2 * kWBuf + 2 * kChunk * 4 + 64; }
-
-cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const CumDt* cumdt, const SeqInfo& si, float* states,
-                                      uint8_t* xt_img, int* err, cudaStream_t st) {
-  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k_ssd_state_tc), (int)state_smem());
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k_ssd_state_tc, dim3(si.total_chunks, kG), dim3(kStThr), state_smem(), st, u, cumdt, si, states,
-                    xt_img, err);
-}
-
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn_ssd() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -516,26 +550,43 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn_ssd() {
   return fn;
 }
 
-cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const CumDt* cumdt, const uint8_t* xt_img,
-                                     const uint8_t* sin_img, const BlockParams& bp, const SeqInfo& si, uint16_t* y,
-                                     int* err, cudaStream_t st) {
-  // u [T, 6144] bf16 as a 2-D tensor: 64-column (128-byte) x 128-row boxes,
-  // 128-byte swizzle, rows past T read as zeros
+// u [T, 6144] bf16 as a 2-D tensor: 64-column (128-byte) boxes of box_rows rows,
+// 128-byte swizzle, rows past T read as zeros
+static cudaError_t make_u_map(CUtensorMap* tm, const uint16_t* u, int total_tokens, int box_rows) {
   auto fn = encode_fn_ssd();
   if (!fn) return cudaErrorNotSupported;
-  CUtensorMap tm;
-  cuuint64_t dims[2] = {(cuuint64_t)kConv, (cuuint64_t)si.total_tokens};
+  cuuint64_t dims[2] = {(cuuint64_t)kConv, (cuuint64_t)total_tokens};
   cuuint64_t strides[1] = {(cuuint64_t)kConv * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  if (fn(&tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(u), dims, strides, box, estr,
+  if (fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(u), dims, strides, box, estr,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
-  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k_ssd_scan_tc), kScanSmem);
+  return cudaSuccess;
+}
+
+cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const CumDt* cumdt, const SeqInfo& si, float* states,
+                                      int* err, cudaStream_t st) {
+  CUtensorMap tm;
+  cudaError_t e = make_u_map(&tm, u, si.total_tokens, 256);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_ssd_scan_tc, dim3(si.total_chunks, kG, 2), dim3(kScThr), (size_t)kScanSmem, st, tm, u, cumdt,
-                    xt_img, sin_img, bp.D, si, y, err);
+  e = ensure_smem_optin(reinterpret_cast<const void*>(k_ssd_state_tc), kStSmem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_ssd_state_tc, dim3(si.total_chunks, kG), dim3(kStThr), (size_t)kStSmem, st, tm, cumdt, si,
+                    states, err);
+}
+
+cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const CumDt* cumdt, const uint8_t* sin_img,
+                                     const BlockParams& bp, const SeqInfo& si, uint16_t* y, int* err,
+                                     cudaStream_t st) {
+  CUtensorMap tm;
+  cudaError_t e = make_u_map(&tm, u, si.total_tokens, 128);
+  if (e != cudaSuccess) return e;
+  e = ensure_smem_optin(reinterpret_cast<const void*>(k_ssd_scan_tc), kScanSmem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_ssd_scan_tc, dim3(2, si.total_chunks, kG), dim3(kScThr), (size_t)kScanSmem, st, tm, cumdt,
+                    sin_img, bp.D, si, y, err);
 }
 
 }  // namespace m2

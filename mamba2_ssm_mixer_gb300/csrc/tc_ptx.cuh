@@ -135,6 +135,28 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// Instruction descriptor as above with either operand MN-major: bit 15 marks
+// A as M-major, bit 16 marks B as N-major.
+__host__ __device__ constexpr uint32_t idesc_f32acc_mn(int M, int N, uint32_t ab_format, bool a_mn, bool b_mn) {
+  return idesc_f32acc(M, N, ab_format) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16);
+}
+
+// Shared-memory matrix descriptor for an MN-major operand tile stored as TMA
+// writes a [K rows][64 MN] bf16 box with the 128-byte swizzle: each K row is
+// 128 bytes of 64 consecutive M (or N) elements, 8-row groups along K 1024
+// bytes apart (stride byte offset), and further 64-element slices along M/N
+// `mn_stride` bytes apart (leading byte offset).  The tile base must be
+// 1024-byte aligned; stepping K by 16 rows adds 2048 bytes to the start.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);          // start address
+  d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64-element MN slice
+  d |= (uint64_t)(1024 >> 4) << 32;                  // stride byte offset: next 8-row group along K
+  d |= (uint64_t)1 << 46;                            // descriptor version (sm_100 family)
+  d |= (uint64_t)2 << 61;                            // 128-byte swizzle
+  return d;
+}
+
 // 32 lanes x 32 consecutive f32 columns of TMEM into 32 registers per thread.
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
