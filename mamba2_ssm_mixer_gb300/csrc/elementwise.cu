@@ -13,7 +13,7 @@ namespace m2 {
 // 8 bf16 in (16 B), 8 codes out (8 B) per thread; grid-stride.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_quant_e4m3_vec(const uint4* __restrict__ x, size_t nvec, float scale,
-                                                        uint2* __restrict__ q) {
+                                                        float inv, uint2* __restrict__ q) {
   pdl_wait();
   pdl_trigger();
   size_t stride = (size_t)gridDim.x * blockDim.x;
@@ -23,9 +23,8 @@ __global__ void __launch_bounds__(256) k_quant_e4m3_vec(const uint4* __restrict_
     uint32_t o[2] = {0u, 0u};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      uint32_t lo = quant_e4m3(bfbits2f((uint16_t)(w[j] & 0xFFFFu)), scale);
-      uint32_t hi = quant_e4m3(bfbits2f((uint16_t)(w[j] >> 16)), scale);
-      o[j >> 1] |= (lo | (hi << 8)) << ((j & 1) * 16);
+      const uint32_t two = quant2_e4m3(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u), scale, inv);
+      o[j >> 1] |= two << ((j & 1) * 16);
     }
     q[i] = make_uint2(o[0], o[1]);
   }
@@ -48,7 +47,8 @@ cudaError_t launch_quant_e4m3(const uint16_t* x, size_t n, float scale, uint8_t*
     size_t blocks = (nvec + 255) / 256;
     if (blocks > 152 * 16) blocks = 152 * 16;
     cudaError_t e = launch_pdl(k_quant_e4m3_vec, dim3((unsigned)blocks), dim3(256), 0, st,
-                               reinterpret_cast<const uint4*>(x), nvec, scale, reinterpret_cast<uint2*>(q));
+                               reinterpret_cast<const uint4*>(x), nvec, scale, exact_inverse(scale),
+                               reinterpret_cast<uint2*>(q));
     if (e != cudaSuccess) return e;
   }
   size_t rest = n - nvec * 8;
@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(256) k_conv_silu_prefill(const uint16_t* __res
     a0 = fmaf(w[0][3], x.x, a0);
     a1 = fmaf(w[1][3], x.y, a1);
     *reinterpret_cast<uint32_t*>(u + (size_t)t * kConv + c) =
-        (uint32_t)f2bfbits(silu_f(a0)) | ((uint32_t)f2bfbits(silu_f(a1)) << 16);
+        (uint32_t)f2bfbits(silu_fast(a0)) | ((uint32_t)f2bfbits(silu_fast(a1)) << 16);
     win[0] = win[1];
     win[1] = win[2];
     win[2] = x;
@@ -223,7 +223,7 @@ cudaError_t launch_conv_state_update(const uint16_t* zx, uint16_t* conv_state, c
 __global__ void __launch_bounds__(256) k_gated_norm_quant(const uint16_t* __restrict__ y,
                                                           const uint16_t* __restrict__ zx,
                                                           const uint16_t* __restrict__ norm_w, float eps,
-                                                          float s_y, uint8_t* __restrict__ q2,
+                                                          float s_y, float inv_y, uint8_t* __restrict__ q2,
                                                           uint16_t* __restrict__ o_tap) {
   pdl_wait();
   pdl_trigger();
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(256) k_gated_norm_quant(const uint16_t* __rest
   float ss = 0.f;
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    gv[e] = bfbits2f(yb[e]) * silu_f(bfbits2f(zb[e]));
+    gv[e] = bfbits2f(yb[e]) * silu_fast(bfbits2f(zb[e]));
     ss = fmaf(gv[e], gv[e], ss);
   }
 #pragma unroll
@@ -249,10 +249,10 @@ __global__ void __launch_bounds__(256) k_gated_norm_quant(const uint16_t* __rest
   uint32_t qq[4] = {0u, 0u, 0u, 0u};
   uint16_t ob[16];
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    ob[e] = f2bfbits(gv[e] * r * bfbits2f(wb[e]));
-    qq[e >> 2] |= (uint32_t)quant_e4m3(bfbits2f(ob[e]), s_y) << (8 * (e & 3));
-  }
+  for (int e = 0; e < 16; ++e) ob[e] = f2bfbits(gv[e] * r * bfbits2f(wb[e]));
+#pragma unroll
+  for (int e = 0; e < 16; e += 2)
+    qq[e >> 2] |= (uint32_t)quant2_e4m3(bfbits2f(ob[e]), bfbits2f(ob[e + 1]), s_y, inv_y) << (8 * (e & 3));
   *reinterpret_cast<uint4*>(q2 + (size_t)t * kI + c) = make_uint4(qq[0], qq[1], qq[2], qq[3]);
   if (o_tap) {
     uint4* op = reinterpret_cast<uint4*>(o_tap + (size_t)t * kI + c);
@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(256) k_gated_norm_quant(const uint16_t* __rest
 cudaError_t launch_gated_norm_quant(const uint16_t* y, const uint16_t* zx, const BlockParams& bp, int T,
                                     uint8_t* q2, uint16_t* o_tap, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(k_gated_norm_quant, dim3(T), dim3(256), 0, st, y, zx, bp.norm_w, bp.eps, bp.s_y, q2, o_tap);
+  return launch_pdl(k_gated_norm_quant, dim3(T), dim3(256), 0, st, y, zx, bp.norm_w, bp.eps, bp.s_y,
+                    exact_inverse(bp.s_y), q2, o_tap);
 }
 
 // ---------------------------------------------------------------------------

@@ -47,10 +47,6 @@ __device__ __forceinline__ void raise_abort(Ctl* ctl, int* err) {
   if (err) atomicOr(err, kErrTimeout);
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  return (uint32_t)f2bfbits(a) | ((uint32_t)f2bfbits(b) << 16);
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------------------

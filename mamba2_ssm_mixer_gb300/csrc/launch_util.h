@@ -3,11 +3,21 @@
 #pragma once
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 #include <set>
 #include <utility>
 
 namespace m2 {
+
+// 1 / s when that is exact (s > 0 a power of two with a normal inverse), else
+// 0: kernels then multiply instead of divide and get the identical quotient.
+inline float exact_inverse(float s) {
+  int e = 0;
+  if (!(s > 0.f) || std::frexp(s, &e) != 0.5f) return 0.f;
+  const float inv = 1.0f / s;
+  return (std::isnormal(inv) && inv * s == 1.0f) ? inv : 0.f;
+}
 
 // cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (device, kernel).
 inline cudaError_t ensure_smem_optin(const void* func, int bytes) {

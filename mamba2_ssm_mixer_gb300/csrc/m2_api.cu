@@ -323,7 +323,7 @@ static PrefillWs carve_prefill(void* base, int T, int chunks) {
   w.q = c.take<uint8_t>((size_t)T * kH);
   w.zx = c.take<uint16_t>((size_t)T * kZ);
   w.u = c.take<uint16_t>((size_t)T * kConv);
-  w.cumdt = c.take<CumDt>((size_t)chunks * kNH * kChunk);
+  w.cumdt = c.take<CumDt>((size_t)chunks * kNH);
   w.states = c.take<float>((size_t)chunks * kNH * kP * kN);
   w.sin_img = c.take<uint8_t>((size_t)chunks * kNH * kSinImageBytes);
   w.y = c.take<uint16_t>((size_t)T * kI);

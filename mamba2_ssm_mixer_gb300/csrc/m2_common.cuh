@@ -39,6 +39,12 @@ __device__ __forceinline__ uint16_t f2bfbits(float v) {
   __nv_bfloat16 h = __float2bfloat16_rn(v);
   return *reinterpret_cast<uint16_t*>(&h);
 }
+// Two floats to one bf16x2 word (round to nearest even), a in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(b), "f"(a));
+  return d;
+}
 // Round to bf16 and back (storage rounding between ops).
 __device__ __forceinline__ float round_bf16(float v) { return bfbits2f(f2bfbits(v)); }
 
@@ -49,7 +55,23 @@ __device__ __forceinline__ uint8_t quant_e4m3(float v, float scale) {
   return (uint8_t)__nv_cvt_float_to_fp8(t, __NV_SATFINITE, __NV_E4M3);
 }
 
+// Two e4m3 codes (a in the low byte) of fp32(a / scale), fp32(b / scale).
+// When inv is nonzero it is exactly 1 / scale (scale a power of two), and
+// v * inv is the same correctly rounded quotient as the division.
+__device__ __forceinline__ uint16_t quant2_e4m3(float a, float b, float scale, float inv) {
+  float2 t;
+  if (inv != 0.f) {
+    t = make_float2(a * inv, b * inv);
+  } else {
+    t = make_float2(__fdiv_rn(a, scale), __fdiv_rn(b, scale));
+  }
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(t, __NV_SATFINITE, __NV_E4M3);
+}
+
 __device__ __forceinline__ float silu_f(float v) { return v / (1.0f + expf(-v)); }
+// SiLU with the fast exponential and division (a few float ulps; used where
+// the result is rounded to bf16 next).
+__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
 __device__ __forceinline__ float softplus_f(float v) { return v > 20.0f ? v : log1pf(expf(v)); }
 
 // Two e4m3 codes (low byte first) to two floats.

@@ -37,14 +37,16 @@ cudaError_t launch_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint
                                     uint16_t* normed, int T, int n, cudaStream_t st);
 
 // ssd.cu
-// Per (chunk, head, token s of the chunk): the in-chunk cumulative log-decay
-// cum_s as an unevaluated (hi, lo) float pair, dt_s, and the source factor
-// colf_s = dt_s exp(cum_e - cum_s) with e the last token of s's 32-token block
-// (<= dt_s: cum never increases); zeros past the chunk's end.  Stored
-// [chunk][head][256] so one head's chunk is 4 KB contiguous.
+// Per (chunk, head), for each token s of the chunk: the in-chunk cumulative
+// log-decay cum_s as an unevaluated (hi, lo) float pair, dt_s, and the source
+// factor colf_s = dt_s exp(cum_e - cum_s) with e the last token of s's
+// 32-token block (<= dt_s: cum never increases); zeros past the chunk's end.
+// One 4 KB record per (chunk, head), arrays of 256 (vector loads of 4
+// consecutive tokens), stored [chunk][head].
 struct CumDt {
-  float hi, lo, dt, colf;
+  float hi[kChunk], lo[kChunk], dt[kChunk], colf[kChunk];
 };
+static_assert(sizeof(CumDt) == 4096, "one cum/dt record is 4 KB (one bulk copy)");
 // Bytes of one (chunk, head) S_in operand image: bf16 high part and remainder
 // [2][64 p][128 n] in the MMA's K-major 128-byte-swizzled layout.
 constexpr int kSinImageBytes = 2 * 64 * 128 * 2;

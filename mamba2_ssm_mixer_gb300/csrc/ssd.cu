@@ -81,16 +81,19 @@ __global__ void __launch_bounds__(256) k_ssd_cumsum(const uint16_t* __restrict__
   v = ff_add(v, pre);
   cums[i] = v;
   __syncthreads();
-  CumDt r = {0.f, 0.f, 0.f, 0.f};
+  CumDt& r = cumdt[(size_t)c * kNH + h];
+  float colf = 0.f;
   if (i < cp.n) {
-    r.hi = v.hi;
-    r.lo = v.lo;
-    r.dt = dt;
     const FF ce = cums[min(i | 31, cp.n - 1)];            // last token of this 32-token block
-    r.colf = dt * expf((ce.hi - v.hi) + (ce.lo - v.lo));  // exponent <= 0
+    colf = dt * expf((ce.hi - v.hi) + (ce.lo - v.lo));   // exponent <= 0
     if (dt_tok) dt_tok[(size_t)(cp.t0 + i) * kNH + h] = dt;
+  } else {
+    v = {0.f, 0.f};
   }
-  cumdt[((size_t)c * kNH + h) * kChunk + i] = r;
+  r.hi[i] = v.hi;
+  r.lo[i] = v.lo;
+  r.dt[i] = dt;
+  r.colf[i] = colf;
 }
 
 // 3. sequential state passing over the chunks of each sequence: the state
@@ -130,8 +133,8 @@ __global__ void __launch_bounds__(256) k_ssd_state_pass(const float* __restrict_
       if (c < c1) {
         sc[k] = reinterpret_cast<const float4*>(states + ((size_t)c * kNH + h) * (kP * kN))[e4];
         const int nl = min(kChunk, tend - (tbeg + (c - c0) * kChunk));   // tokens in chunk c
-        const CumDt cl = cumdt[((size_t)c * kNH + h) * kChunk + nl - 1];
-        dec[k] = cl.hi + cl.lo;
+        const CumDt& cl = cumdt[(size_t)c * kNH + h];
+        dec[k] = cl.hi[nl - 1] + cl.lo[nl - 1];
       }
     }
 #pragma unroll

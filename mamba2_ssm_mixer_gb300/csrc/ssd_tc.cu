@@ -13,17 +13,18 @@
 //   overlaps head h+1's staging.
 // k_ssd_scan_tc   one CTA per (128-row half of the chunk, chunk, group),
 //   warp-specialised: warp 0 loads (TMA for the C, B and per-head x tiles,
-//   bulk copies of the S_in image and cum/dt record, one head ahead); warp 1
+//   bulk copies of the cum/dt record and S_in image, one head ahead); warp 1
 //   issues the MMAs; warps 2-9 build P and run the epilogue.
 //     G = C B^T                      once per CTA (128 x 256 x 128)
-//     P[t, s] = G[t, s] exp(cum_t - cum_s) dt_s   (s <= t, else 0)
-//     Y_diag = P x,  Y_off = C S_in^T,  y = Y_diag + exp(cum_t) Y_off + D x
-//   P and S_in are split into bf16 high part + remainder (a single bf16
-//   rounding of P gives y a ~1e-3 relative error, enough to flip e4m3 codes of
-//   the out_proj input downstream).  P is produced in 32-source blocks into a
-//   double buffer that the MMA warp consumes; x is the MMA's N-major operand
-//   as TMA wrote it; the Y accumulators are double-buffered in TMEM so head
-//   h's epilogue overlaps head h+1's MMAs.
+//     P[t, s] = G[t, s] exp(cum_t - cum_s) dt_s  (s < t),  G[t, t] dt_t + D  (s = t),  0  (s > t)
+//     Y_diag = P x,  Y_off = C S_in^T,  y = Y_diag + exp(cum_t) Y_off
+//   (D x rides on P's diagonal).  P and S_in are split into bf16 high part +
+//   remainder (a single bf16 rounding of P gives y a ~1e-3 relative error,
+//   enough to flip e4m3 codes of the out_proj input downstream).  P is
+//   produced in 32-source blocks into a 4-slot ring that the MMA warp
+//   consumes; x is the MMA's N-major operand as TMA wrote it; the Y
+//   accumulators are double-buffered in TMEM and each head's epilogue runs
+//   after the next head's P blocks, when its MMAs have long finished.
 // Every wait is bounded; a wait that runs out raises the device error word and
 // a CTA-wide abort flag that makes the remaining waits return at once.
 #include <cudaTypedefs.h>
@@ -46,9 +47,7 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int k8, int rows) {
   return (uint32_t)(a * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t bf2(float a, float b) {
-  return (uint32_t)f2bfbits(a) | ((uint32_t)f2bfbits(b) << 16);
-}
+__device__ __forceinline__ uint32_t bf2(float a, float b) { return pack_bf16x2(a, b); }
 __device__ __forceinline__ uint16_t h16(const uint4& v, int j) {
   const uint32_t w = (j < 2) ? v.x : (j < 4) ? v.y : (j < 6) ? v.z : v.w;
   return (uint16_t)((j & 1) ? (w >> 16) : (w & 0xFFFFu));
@@ -68,7 +67,7 @@ __device__ __forceinline__ ChunkPos chunk_of(const SeqInfo& si, int c) {
 // Bounded wait; a wait that runs out flags the device error word and the CTA's
 // abort flag, after which every wait returns false at once.
 __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile int* abort, int* err) {
-  if (mbar_wait(bar, parity, abort)) return true;
+  if (mbar_wait_sleep(bar, parity, abort)) return true;
   if (!*abort) {
     *abort = 1;
     if (err) atomicOr(err, kErrTimeout);
@@ -173,8 +172,10 @@ __global__ void __launch_bounds__(kStThr, 1)
     // ------------------------------------------------ workers (8 warps)
     const int quarter = warp & 3, side = warp >> 2;
     const int t = tid;
-    const CumDt* cd0 = cumdt + ((size_t)c * kNH + g * kHPG) * kChunk;
-    CumDt ct = cd0[t], cl = cd0[cp.n - 1];   // this head's; the next head's are fetched one head ahead
+    const CumDt* cd0 = cumdt + (size_t)c * kNH + g * kHPG;
+    // this head's cum_t, cum_last and dt_t; the next head's are fetched one head ahead
+    float ct_hi = cd0->hi[t], ct_lo = cd0->lo[t], ct_dt = cd0->dt[t];
+    float cl_hi = cd0->hi[cp.n - 1], cl_lo = cd0->lo[cp.n - 1];
     bool ok = wait_ab(&sb->b_full, 0, abort, err);
 
     auto epilogue = [&](int hd) {
@@ -197,10 +198,14 @@ __global__ void __launch_bounds__(kStThr, 1)
     for (int hh = 0; hh < kHPG; ++hh) {
       const int k = hh & 1;
       // w_t = exp(cum_last - cum_t) dt_t; zero past the chunk's end
-      const float w = t < cp.n ? expf((cl.hi - ct.hi) + (cl.lo - ct.lo)) * ct.dt : 0.f;
+      const float w = t < cp.n ? expf((cl_hi - ct_hi) + (cl_lo - ct_lo)) * ct_dt : 0.f;
       if (hh + 1 < kHPG) {
-        ct = cd0[(hh + 1) * kChunk + t];
-        cl = cd0[(hh + 1) * kChunk + cp.n - 1];
+        const CumDt* nx = cd0 + hh + 1;
+        ct_hi = nx->hi[t];
+        ct_lo = nx->lo[t];
+        ct_dt = nx->dt[t];
+        cl_hi = nx->hi[cp.n - 1];
+        cl_lo = nx->lo[cp.n - 1];
       }
       ok = wait_ab(&sb->x_full[k], (hh >> 1) & 1, abort, err) && ok;
       const uint8_t* xs = sX + k * 32 * 1024;
@@ -257,25 +262,35 @@ __global__ void __launch_bounds__(kStThr, 1)
 // chunk scan
 // ---------------------------------------------------------------------------
 constexpr int kScThr = 320;   // warp 0 loads, warp 1 MMA, warps 2-9 P + epilogue
-constexpr int kScP = 256;     // P / epilogue threads
+constexpr int kScPW = 8;      // P / epilogue warps
+constexpr int kScRing = 4;    // P ring slots (32 sources each)
 
 // shared-memory map (bytes from the 1024-aligned base)
-constexpr int kSmC = 0;                // C   [128 t][128 n]                 32 KB
-constexpr int kSmB = 32 * 1024;        // B   [KS s][128 n] 64 KB; after G: operand buffer 1
-constexpr int kSmOp0 = 96 * 1024;      // operand buffer 0: x [256 s][64 p] 32 KB + S_in hi/lo 32 KB
-constexpr int kSmP = 160 * 1024;       // P   hi atom [128][64] 16 KB + lo atom 16 KB
-constexpr int kSmCD = 192 * 1024;      // CumDt [2][256]                     8 KB
-constexpr int kSmBar = 200 * 1024;     // barriers
+constexpr int kSmC = 0;                 // C [128 t][128 n] K-major, two 64-column atoms   32 KB
+constexpr int kSmX0 = 32 * 1024;        // x buffer 0 [256 s][64 p] as TMA writes it       32 KB
+constexpr int kSmB = 64 * 1024;         // B [KS s][128 n] (G only); then x buffer 1 + S_in 64 KB
+constexpr int kSmX1 = kSmB;             //   x buffer 1                                    32 KB
+constexpr int kSmSin = kSmB + 32 * 1024;  // S_in hi, lo [64 p][128 n] K-major each         32 KB
+constexpr int kSmP = 128 * 1024;        // P ring: hi atoms [2][128][64], lo atoms [2][128][64] 64 KB
+constexpr int kSmCD = 192 * 1024;       // cum/dt records [2]                               8 KB
+constexpr int kSmBar = 200 * 1024;      // barriers
 constexpr int kScanSmem = kSmBar + 256 + 1024;
 
 struct ScanBars {
-  uint64_t cb, g, drain;
+  uint64_t cb, g, drain, sin_full, sin_empty;
   uint64_t op_full[2], op_empty[2];
-  uint64_t p_full[2], p_empty[2];
+  uint64_t p_full[kScRing], p_empty[kScRing];
   uint64_t y_full[2], y_empty[2];
   uint32_t tslot;
   int abort;
 };
+
+// Two floats -> bf16x2 high parts and bf16x2 remainders (v - high), low half
+// first.
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
+}
 
 __global__ void __launch_bounds__(kScThr, 1)
     k_ssd_scan_tc(const __grid_constant__ CUtensorMap tm_u, const CumDt* __restrict__ cumdt,
@@ -294,20 +309,24 @@ __global__ void __launch_bounds__(kScThr, 1)
   const int KS = (tb + 1) * 128;       // sources s < KS (causal)
   const int NBLK = KS / 32;            // 32-source P blocks per head
   constexpr uint32_t TMEM_COLS = 512;  // G [0, 256); Y_diag[k] at 256 + 128 k, Y_off[k] at 320 + 128 k
-  constexpr uint32_t IDESC_Y = idesc_f32acc(128, 64, 1u);               // C S_in^T: both K-major
+  constexpr uint32_t IDESC_Y = idesc_f32acc(128, 64, 1u);                   // C S_in^T: both K-major
   constexpr uint32_t IDESC_PX = idesc_f32acc_mn(128, 64, 1u, false, true);  // P x: x as TMA writes it
 
   if (tid == 0) {
     mbar_init(&sb->cb, 1);
     mbar_init(&sb->g, 1);
     mbar_init(&sb->drain, 1);
+    mbar_init(&sb->sin_full, 1);
+    mbar_init(&sb->sin_empty, 1);
     for (int k = 0; k < 2; ++k) {
       mbar_init(&sb->op_full[k], 1);
-      mbar_init(&sb->op_empty[k], 2);   // MMA commit + the P side
-      mbar_init(&sb->p_full[k], 8);     // one lane per P warp
-      mbar_init(&sb->p_empty[k], 1);
+      mbar_init(&sb->op_empty[k], 1 + kScPW);   // MMA commit + each P warp
       mbar_init(&sb->y_full[k], 1);
-      mbar_init(&sb->y_empty[k], 8);
+      mbar_init(&sb->y_empty[k], kScPW);
+    }
+    for (int k = 0; k < kScRing; ++k) {
+      mbar_init(&sb->p_full[k], kScPW / 2);   // the 4 warps of one side
+      mbar_init(&sb->p_empty[k], 1);
     }
     sb->abort = 0;
     fence_mbar_init();
@@ -336,26 +355,40 @@ __global__ void __launch_bounds__(kScThr, 1)
           tma_load_2d(smem + kSmB + a * KS * 128 + rb * 128 * 128, &tm_u, &sb->cb, kOffB + g * kN + a * 64,
                       cp.t0 + rb * 128);
       }
-      const uint32_t x_bytes = (uint32_t)KS * 128;   // x [KS s][64 p]
-      bool issued[2] = {false, false};
-      uint32_t issued_par[2] = {0, 0};
+      int op_issued[2] = {-1, -1}, sin_issued = -1;   // last head whose copies were issued
+      bool g_done = false;
       for (int hh = 0; hh < kHPG; ++hh) {
         const int k = hh & 1;
-        if (hh == 1 && !wait_ab(&sb->g, 0, abort, err)) break;   // buffer 1 is the B tile's memory
+        // x tile and cum/dt record of head hh (buffer 1 is the B tile's memory)
         if (!wait_ab(&sb->op_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
-        uint8_t* ob = smem + (k == 0 ? kSmOp0 : kSmB);
-        mbar_expect_tx(&sb->op_full[k], x_bytes + (uint32_t)kSinImageBytes + (uint32_t)(kChunk * sizeof(CumDt)));
+        if (k == 1 && !g_done) {
+          if (!wait_ab(&sb->g, 0, abort, err)) break;
+          g_done = true;
+        }
+        mbar_expect_tx(&sb->op_full[k], (uint32_t)(KS * 128 + sizeof(CumDt)));
+        uint8_t* xb = smem + (k == 0 ? kSmX0 : kSmX1);
         for (int rb = 0; rb < KS / 128; ++rb)
-          tma_load_2d(ob + rb * 128 * 128, &tm_u, &sb->op_full[k], (g * kHPG + hh) * kP, cp.t0 + rb * 128);
-        bulk_g2s(ob + 32 * 1024, sin_img + (ch0 + hh) * kSinImageBytes, kSinImageBytes, &sb->op_full[k]);
-        bulk_g2s(smem + kSmCD + k * 4096, cumdt + (ch0 + hh) * kChunk, kChunk * sizeof(CumDt), &sb->op_full[k]);
-        issued[k] = true;
-        issued_par[k] = (hh >> 1) & 1;
+          tma_load_2d(xb + rb * 128 * 128, &tm_u, &sb->op_full[k], (g * kHPG + hh) * kP, cp.t0 + rb * 128);
+        bulk_g2s(smem + kSmCD + k * sizeof(CumDt), cumdt + ch0 + hh, (uint32_t)sizeof(CumDt), &sb->op_full[k]);
+        op_issued[k] = hh;
+        // S_in of head hh: one buffer, free once head hh-1's C S_in^T MMAs are done
+        if (hh == 0) {
+          if (!g_done) {
+            if (!wait_ab(&sb->g, 0, abort, err)) break;
+            g_done = true;
+          }
+        } else if (!wait_ab(&sb->sin_empty, (hh - 1) & 1, abort, err)) {
+          break;
+        }
+        mbar_expect_tx(&sb->sin_full, (uint32_t)kSinImageBytes);
+        bulk_g2s(smem + kSmSin, sin_img + (ch0 + hh) * kSinImageBytes, kSinImageBytes, &sb->sin_full);
+        sin_issued = hh;
       }
       if (*abort) {   // let copies in flight land before the CTA can exit
         mbar_wait(&sb->cb, 0, nullptr, 100000000ull);
         for (int k = 0; k < 2; ++k)
-          if (issued[k]) mbar_wait(&sb->op_full[k], issued_par[k], nullptr, 100000000ull);
+          if (op_issued[k] >= 0) mbar_wait(&sb->op_full[k], (op_issued[k] >> 1) & 1, nullptr, 100000000ull);
+        if (sin_issued >= 0) mbar_wait(&sb->sin_full, sin_issued & 1, nullptr, 100000000ull);
       }
     }
   } else if (warp == 1) {
@@ -373,16 +406,42 @@ __global__ void __launch_bounds__(kScThr, 1)
                     desc_kmajor_sw128(b0 + a * KS * 128) + 2 * j, idesc_g, (a | j) != 0);
         mma_commit(&sb->g);
       }
-      int pb = 0;   // P blocks consumed so far (buffer pb & 1, use pb >> 1)
+      const uint32_t ph0 = smem_u32(smem + kSmP), pl0 = ph0 + 32 * 1024;
+      const uint32_t c0 = smem_u32(smem + kSmC), sh0 = smem_u32(smem + kSmSin), sl0 = sh0 + 16 * 1024;
+      int pb = 0;   // P blocks consumed so far (slot pb % 4, use pb / 4)
       for (int hh = 0; hh < kHPG && !*abort; ++hh) {
         const int k = hh & 1;
         if (!wait_ab(&sb->op_full[k], (hh >> 1) & 1, abort, err)) break;
         if (!wait_ab(&sb->y_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
         tc_fence_after();
         const uint32_t yd = tmem + 256 + 128 * k, yo = yd + 64;
-        uint8_t* ob = smem + (k == 0 ? kSmOp0 : kSmB);
-        const uint32_t x0 = smem_u32(ob), sh0 = smem_u32(ob + 32 * 1024), sl0 = sh0 + 16 * 1024;
-        const uint32_t c0 = smem_u32(smem + kSmC);
+        const uint32_t x0 = smem_u32(smem + (k == 0 ? kSmX0 : kSmX1));
+        bool ok = true;
+        for (int j = 0; j < NBLK; ++j, ++pb) {
+          const int b = pb & (kScRing - 1);
+          if (!wait_ab(&sb->p_full[b], (pb >> 2) & 1, abort, err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // block j: sources [32 j, 32 j + 32) = x rows 32 j.. (4096 bytes per
+          // block, 2048 per 16-source K-step); slot b = half (b & 1) of the
+          // P atoms b / 2
+          const uint32_t pa = (uint32_t)(b >> 1) * 16 * 1024;
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t xd = desc_mnmajor_sw128(x0 + j * 4096 + kk * 2048, 1024);
+            const uint64_t pofs = (uint64_t)((b & 1) * 4 + kk * 2);
+            mma_f16(yd, desc_kmajor_sw128(ph0 + pa) + pofs, xd, IDESC_PX, (j | kk) != 0);
+            mma_f16(yd, desc_kmajor_sw128(pl0 + pa) + pofs, xd, IDESC_PX, 1u);
+          }
+          mma_commit(&sb->p_empty[b]);
+        }
+        if (!ok) break;
+        mma_commit(&sb->op_empty[k]);   // x(hh) is no longer read once these finish
+        // Y_off = C S_in^T (S_in as bf16 high part + remainder)
+        if (!wait_ab(&sb->sin_full, hh & 1, abort, err)) break;
+        tc_fence_after();
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -391,28 +450,7 @@ __global__ void __launch_bounds__(kScThr, 1)
             mma_f16(yo, cd, desc_kmajor_sw128(sh0 + a * 64 * 128) + 2 * j, IDESC_Y, (a | j) != 0);
             mma_f16(yo, cd, desc_kmajor_sw128(sl0 + a * 64 * 128) + 2 * j, IDESC_Y, 1u);
           }
-        const uint32_t ph0 = smem_u32(smem + kSmP), pl0 = ph0 + 16 * 1024;
-        bool ok = true;
-        for (int j = 0; j < NBLK; ++j, ++pb) {
-          const int b = pb & 1;
-          if (!wait_ab(&sb->p_full[b], (pb >> 1) & 1, abort, err)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          // block j: sources [32 j, 32 j + 32) = x rows 32 j.. (4096 bytes per
-          // block, 2048 per 16-source K-step); P block b = half b of the P atoms
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t xd = desc_mnmajor_sw128(x0 + j * 4096 + kk * 2048, 1024);
-            const uint64_t pofs = (uint64_t)(b * 4 + kk * 2);
-            mma_f16(yd, desc_kmajor_sw128(ph0) + pofs, xd, IDESC_PX, (j | kk) != 0);
-            mma_f16(yd, desc_kmajor_sw128(pl0) + pofs, xd, IDESC_PX, 1u);
-          }
-          mma_commit(&sb->p_empty[b]);
-        }
-        if (!ok) break;
-        mma_commit(&sb->op_empty[k]);
+        mma_commit(&sb->sin_empty);
         mma_commit(&sb->y_full[k]);
       }
       if (*abort) {
@@ -424,107 +462,124 @@ __global__ void __launch_bounds__(kScThr, 1)
     // ------------------------------------------------ P and epilogue (warps 2..9)
     const int pw = warp - 2;                 // 0..7
     const int quarter = warp & 3;            // TMEM lane quarter this warp may access
-    const int side = pw >> 2;                // P: 16-source half of each block; epilogue: 32-column half of p
+    const int side = pw >> 2;                // P: blocks j = side (mod 2); epilogue: 32-column half of p
     const int row = quarter * 32 + lane;     // row of the tile = TMEM lane
     const int tt = tb * 128 + row;           // chunk-local token of that row
     const int tlim = tt < cp.n ? tt : -1;
+    const int rblk = tb * 4 + quarter;       // this warp's 32-token block
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* sPh = smem + kSmP;
-    uint8_t* sPl = sPh + 16 * 1024;
+    uint8_t* sPl = sPh + 32 * 1024;
     bool ok = wait_ab(&sb->g, 0, abort, err);
     tc_fence_after();
+    float prev_cum = 0.f;   // cum_t of the previous head (its epilogue runs one head late)
+
+    // y = Y_diag + exp(cum_t) Y_off for head hd (D x is folded into P's diagonal)
+    auto epilogue = [&](int hd, float cum_t) {
+      const int k = hd & 1;
+      ok = wait_ab(&sb->y_full[k], (hd >> 1) & 1, abort, err) && ok;
+      tc_fence_after();
+      const float et = expf(cum_t);
+      uint32_t rd[32], ro[32];
+      tmem_ld_32x32b_x32(lane_base + 256 + 128 * k + (uint32_t)(side * 32), rd);
+      tmem_ld_32x32b_x32(lane_base + 320 + 128 * k + (uint32_t)(side * 32), ro);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb->y_empty[k]);
+      if (ok && tt < cp.n) {
+        uint16_t* yr = y + (size_t)(cp.t0 + tt) * kI + (g * kHPG + hd) * kP + side * 32;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int jj = q * 8 + 2 * e;
+            o[e] = bf2(__uint_as_float(rd[jj]) + et * __uint_as_float(ro[jj]),
+                       __uint_as_float(rd[jj + 1]) + et * __uint_as_float(ro[jj + 1]));
+          }
+          *reinterpret_cast<uint4*>(yr + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    };
+
     int pb = 0;
     for (int hh = 0; hh < kHPG; ++hh) {
       const int h = g * kHPG + hh, k = hh & 1;
       ok = wait_ab(&sb->op_full[k], (hh >> 1) & 1, abort, err) && ok;
-      const CumDt* cd = reinterpret_cast<const CumDt*>(smem + kSmCD + k * 4096);
-      const CumDt ct = tt < cp.n ? cd[tt] : CumDt{0.f, 0.f, 0.f, 0.f};
-      for (int j = 0; j < NBLK; ++j, ++pb) {
-        const int b = pb & 1;
-        ok = wait_ab(&sb->p_empty[b], ((pb >> 1) & 1) ^ 1u, abort, err) && ok;
+      const CumDt* cd = reinterpret_cast<const CumDt*>(smem + kSmCD + k * sizeof(CumDt));
+      const float ct_hi = tt < cp.n ? cd->hi[tt] : 0.f, ct_lo = tt < cp.n ? cd->lo[tt] : 0.f;
+      const float Dh = Dp[h];
+      // the two sides take alternate 32-source blocks, so each side owns ring
+      // slots of one parity (NBLK is even) and 32 sources per warp and block
+      for (int j = side; j < NBLK; j += 2) {
+        const int pj = pb + j, b = pj & (kScRing - 1);
+        ok = wait_ab(&sb->p_empty[b], ((pj >> 2) & 1) ^ 1u, abort, err) && ok;
         tc_fence_after();
-        const int s0 = j * 32 + side * 16;
-        uint32_t r[16];
-        tmem_ld_32x32b_x16(lane_base + (uint32_t)s0, r);
+        const int s0 = j * 32;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(lane_base + (uint32_t)s0, r);
         tmem_ld_wait();
-        // The warp's 32 rows are the 32-token block [tb*128 + 32 quarter, +32);
-        // relative to source block j it is below the diagonal, on it, or above
-        // it (all zero).  Below: exp(cum_t - cum_s) = exp(cum_t - cum_e)
-        // exp(cum_e - cum_s), both factors <= 1 with e the block's last source
-        // (the second, times dt_s, is colf_s).  On it: one exp per element.
-        const int rblk = tb * 4 + quarter;   // this warp's 32-token block
-        uint16_t hi[16], lo[16];
+        // The warp's 32 rows are the 32-token block rblk; relative to source
+        // block j it is below the diagonal, on it, or above it (all zero).
+        // Below: exp(cum_t - cum_s) = exp(cum_t - cum_e) exp(cum_e - cum_s),
+        // both factors <= 1 with e the block's last source (the second, times
+        // dt_s, is colf_s).  On it: one exp per element, and D on s = t.
+        float v[32];
         if (j < rblk) {
-          const CumDt ce = cd[min(j * 32 + 31, cp.n - 1)];
-          const float rf = tt < cp.n ? __expf((ct.hi - ce.hi) + (ct.lo - ce.lo)) : 0.f;
+          const int e = min(j * 32 + 31, cp.n - 1);
+          const float rf = tt < cp.n ? __expf((ct_hi - cd->hi[e]) + (ct_lo - cd->lo[e])) : 0.f;
+          const float4* cf = reinterpret_cast<const float4*>(cd->colf + s0);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) split_bf16(__uint_as_float(r[e]) * rf * cd[s0 + e].colf, hi[e], lo[e]);
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = cf[q];
+            v[4 * q + 0] = __uint_as_float(r[4 * q + 0]) * (rf * f.x);
+            v[4 * q + 1] = __uint_as_float(r[4 * q + 1]) * (rf * f.y);
+            v[4 * q + 2] = __uint_as_float(r[4 * q + 2]) * (rf * f.z);
+            v[4 * q + 3] = __uint_as_float(r[4 * q + 3]) * (rf * f.w);
+          }
         } else if (j == rblk) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
+          for (int e = 0; e < 32; ++e) {
             const int s = s0 + e;
-            float v = 0.f;
+            float val = 0.f;
             if (s <= tlim) {
-              const CumDt cs = cd[s];
-              v = __uint_as_float(r[e]) * __expf((ct.hi - cs.hi) + (ct.lo - cs.lo)) * cs.dt;
+              val = __uint_as_float(r[e]) * __expf((ct_hi - cd->hi[s]) + (ct_lo - cd->lo[s])) * cd->dt[s];
+              if (s == tt) val += Dh;
             }
-            split_bf16(v, hi[e], lo[e]);
+            v[e] = val;
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0;
+          for (int e = 0; e < 32; ++e) v[e] = 0.f;
         }
-        // 16 sources = two 16-byte chunks: chunk index inside the 64-source
-        // atom row is b * 4 + side * 2 (+1)
+        // 32 sources = the four 16-byte chunks (b & 1) * 4 + q of this row in
+        // the P atoms b / 2
+        const uint32_t pa = (uint32_t)(b >> 1) * 16 * 1024;
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const uint32_t off = sw_chunk(row, b * 4 + side * 2 + q, 128);
-          *reinterpret_cast<uint4*>(sPh + off) = *reinterpret_cast<const uint4*>(hi + 8 * q);
-          *reinterpret_cast<uint4*>(sPl + off) = *reinterpret_cast<const uint4*>(lo + 8 * q);
+        for (int q = 0; q < 4; ++q) {
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2(v[8 * q + 2 * e], v[8 * q + 2 * e + 1], hi[e], lo[e]);
+          const uint32_t off = pa + sw_chunk(row, (b & 1) * 4 + q, 128);
+          *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sb->p_full[b]);
       }
-      // epilogue of head hh: y = Y_diag + exp(cum_t) Y_off + D x
-      ok = wait_ab(&sb->y_full[k], (hh >> 1) & 1, abort, err) && ok;
-      tc_fence_after();
-      {
-        const float et = expf(ct.hi + ct.lo);
-        const float Dh = Dp[h];
-        uint32_t rd[32], ro[32];
-        tmem_ld_32x32b_x32(lane_base + 256 + 128 * k + (uint32_t)(side * 32), rd);
-        tmem_ld_32x32b_x32(lane_base + 320 + 128 * k + (uint32_t)(side * 32), ro);
-        tmem_ld_wait();
-        if (ok && tt < cp.n) {
-          // x[tt, p] from the operand buffer's x tile (row tt, 16-byte chunk p / 8)
-          const uint8_t* xrow = smem + (k == 0 ? kSmOp0 : kSmB);
-          uint16_t* yr = y + (size_t)(cp.t0 + tt) * kI + h * kP + side * 32;
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 xv = *reinterpret_cast<const uint4*>(xrow + sw_row_chunk(tt, side * 4 + q));
-            uint32_t o[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int jj = q * 8 + 2 * e;
-              const float a =
-                  __uint_as_float(rd[jj]) + et * __uint_as_float(ro[jj]) + Dh * bfbits2f(h16(xv, 2 * e));
-              const float bb = __uint_as_float(rd[jj + 1]) + et * __uint_as_float(ro[jj + 1]) +
-                               Dh * bfbits2f(h16(xv, 2 * e + 1));
-              o[e] = bf2(a, bb);
-            }
-            *reinterpret_cast<uint4*>(yr + q * 8) = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-        }
-      }
-      tc_fence_before();
+      pb += NBLK;
+      // this warp no longer reads head hh's cum/dt record
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sb->y_empty[k]);
-      // this side no longer reads the operand buffer's cum/dt record
-      asm volatile("bar.sync 1, %0;" ::"n"(kScP) : "memory");
-      if (pw == 0 && lane == 0) mbar_arrive(&sb->op_empty[k]);
+      if (lane == 0) mbar_arrive(&sb->op_empty[k]);
+      // head hh-1's accumulators are complete by now (its MMAs ran during this
+      // head's P blocks)
+      if (hh > 0) epilogue(hh - 1, prev_cum);
+      prev_cum = ct_hi + ct_lo;
     }
+    epilogue(kHPG - 1, prev_cum);
   }
   __syncwarp();
   __syncthreads();
