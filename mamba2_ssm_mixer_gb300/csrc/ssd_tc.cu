@@ -48,10 +48,6 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int k8, int rows) {
 }
 
 __device__ __forceinline__ uint32_t bf2(float a, float b) { return pack_bf16x2(a, b); }
-__device__ __forceinline__ uint16_t h16(const uint4& v, int j) {
-  const uint32_t w = (j < 2) ? v.x : (j < 4) ? v.y : (j < 6) ? v.z : v.w;
-  return (uint16_t)((j & 1) ? (w >> 16) : (w & 0xFFFFu));
-}
 
 struct ChunkPos {
   int t0, n;
@@ -75,10 +71,13 @@ __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile
   return false;
 }
 
-__device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) {
-  hi = f2bfbits(v);
-  lo = f2bfbits(v - bfbits2f(hi));
+// Two floats -> bf16x2 high parts and bf16x2 remainders (v - high), low half
+// first.
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
 }
+
 
 }  // namespace
 
@@ -87,14 +86,14 @@ __device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) 
 // ---------------------------------------------------------------------------
 constexpr int kStWork = 256;             // 8 worker warps; worker thread t owns token row t
 constexpr int kStThr = kStWork + 32;     // + a loader warp
-constexpr int kStSmB = 0;                // B [2 slices of 64 n][256 t][64] as TMA writes it   64 KB
-constexpr int kStSmX = 64 * 1024;        // x [2 buffers][256 t][64 p] as TMA writes it        64 KB
-constexpr int kStSmW = 128 * 1024;       // w x, bf16 high then remainder, [256 t][64 p] each 64 KB
-constexpr int kStSmBar = 192 * 1024;
+constexpr int kStSmB = 0;                // B [2 slices of 64 n][256 t][64] as TMA writes it    64 KB
+constexpr int kStSmX = 64 * 1024;        // x [256 t][64 p] as TMA writes it                    32 KB
+constexpr int kStSmW = 96 * 1024;        // w x [2 buffers] x (bf16 high, remainder) [256 t][64 p] 128 KB
+constexpr int kStSmBar = 224 * 1024;
 constexpr int kStSmem = kStSmBar + 128 + 1024;
 
 struct StateBars {
-  uint64_t b_full, x_full[2], x_empty[2], mma[2], drain;
+  uint64_t b_full, x_full, x_empty, mma[2], drain;
   uint32_t tslot;
   int abort;
 };
@@ -114,8 +113,6 @@ __global__ void __launch_bounds__(kStThr, 1)
   volatile int* abort = &sb->abort;
   uint8_t* sB = smem + kStSmB;
   uint8_t* sX = smem + kStSmX;
-  uint8_t* sWh = smem + kStSmW;
-  uint8_t* sWl = sWh + 32 * 1024;
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const ChunkPos cp = chunk_of(si, c);
@@ -124,12 +121,11 @@ __global__ void __launch_bounds__(kStThr, 1)
 
   if (tid == 0) {
     mbar_init(&sb->b_full, 1);
+    mbar_init(&sb->x_full, 1);
+    mbar_init(&sb->x_empty, kStWork / 32);
+    mbar_init(&sb->mma[0], 1);
+    mbar_init(&sb->mma[1], 1);
     mbar_init(&sb->drain, 1);
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(&sb->x_full[k], 1);
-      mbar_init(&sb->x_empty[k], kStWork / 32);
-      mbar_init(&sb->mma[k], 1);
-    }
     sb->abort = 0;
     fence_mbar_init();
     tma_prefetch(&tm_u);
@@ -152,20 +148,17 @@ __global__ void __launch_bounds__(kStThr, 1)
       mbar_expect_tx(&sb->b_full, 256 * 128 * 2);
       for (int a = 0; a < 2; ++a)
         tma_load_2d(sB + a * 256 * 128, &tm_u, &sb->b_full, kOffB + g * kN + a * 64, cp.t0);
-      bool issued[2] = {false, false};
-      uint32_t par[2] = {0, 0};
+      int issued = -1;
       for (int hh = 0; hh < kHPG; ++hh) {
-        const int k = hh & 1;
-        if (!wait_ab(&sb->x_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
-        mbar_expect_tx(&sb->x_full[k], 256 * 64 * 2);
-        tma_load_2d(sX + k * 32 * 1024, &tm_u, &sb->x_full[k], (g * kHPG + hh) * kP, cp.t0);
-        issued[k] = true;
-        par[k] = (hh >> 1) & 1;
+        // the x tile is free once every worker has read head hh-1's rows
+        if (!wait_ab(&sb->x_empty, (hh & 1) ^ 1u, abort, err)) break;
+        mbar_expect_tx(&sb->x_full, 256 * 64 * 2);
+        tma_load_2d(sX, &tm_u, &sb->x_full, (g * kHPG + hh) * kP, cp.t0);
+        issued = hh;
       }
       if (*abort) {   // let copies in flight land before the CTA can exit
         mbar_wait(&sb->b_full, 0, nullptr, 100000000ull);
-        for (int k = 0; k < 2; ++k)
-          if (issued[k]) mbar_wait(&sb->x_full[k], par[k], nullptr, 100000000ull);
+        if (issued >= 0) mbar_wait(&sb->x_full, issued & 1, nullptr, 100000000ull);
       }
     }
   } else {
@@ -188,15 +181,17 @@ __global__ void __launch_bounds__(kStThr, 1)
       uint32_t r[32];
       tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(k * 64 + side * 32), r);
       tmem_ld_wait();
+      tc_fence_before();
       if (ok && okm) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) out[(size_t)(side * 32 + j) * kN] = __uint_as_float(r[j]);
       }
-      tc_fence_before();
     };
 
     for (int hh = 0; hh < kHPG; ++hh) {
       const int k = hh & 1;
+      uint8_t* sWh = smem + kStSmW + k * 64 * 1024;
+      uint8_t* sWl = sWh + 32 * 1024;
       // w_t = exp(cum_last - cum_t) dt_t; zero past the chunk's end
       const float w = t < cp.n ? expf((cl_hi - ct_hi) + (cl_lo - ct_lo)) * ct_dt : 0.f;
       if (hh + 1 < kHPG) {
@@ -207,24 +202,25 @@ __global__ void __launch_bounds__(kStThr, 1)
         cl_hi = nx->hi[cp.n - 1];
         cl_lo = nx->lo[cp.n - 1];
       }
-      ok = wait_ab(&sb->x_full[k], (hh >> 1) & 1, abort, err) && ok;
-      const uint8_t* xs = sX + k * 32 * 1024;
+      ok = wait_ab(&sb->x_full, hh & 1, abort, err) && ok;
       uint4 xv[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) xv[q] = *reinterpret_cast<const uint4*>(xs + sw_row_chunk(t, q));
+      for (int q = 0; q < 8; ++q) xv[q] = *reinterpret_cast<const uint4*>(sX + sw_row_chunk(t, q));
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sb->x_empty[k]);   // this warp's reads of the x tile are done
-      // the single (w x) buffer is free once head hh-1's MMA has finished
-      if (hh > 0) epilogue(hh - 1);
-      // row t of (w x), bf16 high part and remainder, in the x tile's own layout
+      if (lane == 0) mbar_arrive(&sb->x_empty);   // this warp's reads of the x tile are done
+      // row t of (w x), bf16 high part and remainder, in the x tile's own
+      // layout; buffer k was last read by head hh-2's MMA, which this thread
+      // saw finish in that head's epilogue
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        uint16_t hi[8], lo[8];
+        uint32_t hi[4], lo[4];
+        const uint32_t wd[4] = {xv[q].x, xv[q].y, xv[q].z, xv[q].w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) split_bf16(w * bfbits2f(h16(xv[q], e)), hi[e], lo[e]);
+        for (int e = 0; e < 4; ++e)
+          split2(w * __uint_as_float(wd[e] << 16), w * __uint_as_float(wd[e] & 0xFFFF0000u), hi[e], lo[e]);
         const uint32_t off = sw_row_chunk(t, q);
-        *reinterpret_cast<uint4*>(sWh + off) = *reinterpret_cast<const uint4*>(hi);
-        *reinterpret_cast<uint4*>(sWl + off) = *reinterpret_cast<const uint4*>(lo);
+        *reinterpret_cast<uint4*>(sWh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       fence_proxy_async_smem();
       asm volatile("bar.sync 1, %0;" ::"n"(kStWork) : "memory");
@@ -243,6 +239,8 @@ __global__ void __launch_bounds__(kStThr, 1)
         mma_commit(&sb->mma[k]);
       }
       __syncwarp();
+      // head hh-1's accumulator: its MMA ran while this head was staged
+      if (hh > 0) epilogue(hh - 1);
     }
     epilogue(kHPG - 1);
     if (tid == 0 && *abort) {   // no MMA may still be running when TMEM is freed
@@ -284,13 +282,6 @@ struct ScanBars {
   uint32_t tslot;
   int abort;
 };
-
-// Two floats -> bf16x2 high parts and bf16x2 remainders (v - high), low half
-// first.
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16x2(a, b);
-  lo = pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
-}
 
 __global__ void __launch_bounds__(kScThr, 1)
     k_ssd_scan_tc(const __grid_constant__ CUtensorMap tm_u, const CumDt* __restrict__ cumdt,
