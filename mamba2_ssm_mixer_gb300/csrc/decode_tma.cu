@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
                     const int32_t* __restrict__ slot_idx, int Bt, uint8_t* __restrict__ q2, int* __restrict__ err,
                     DecodeTaps taps) {
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  Smem& sm = *reinterpret_cast<Smem*>(smem_align<128>(smem_raw));
   volatile int* abort = &sm.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = Bt * kG;

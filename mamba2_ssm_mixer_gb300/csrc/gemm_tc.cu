@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t IDESC = idesc_f32acc(kBM, BN, 0u);
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align<1024>(smem_raw);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
   volatile int* abort = &ctl->abort;
 
@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t IDESC = idesc_f32acc(kBM, BNT, 0u);
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align<1024>(smem_raw);
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
   volatile int* abort = &ctl->abort;
 

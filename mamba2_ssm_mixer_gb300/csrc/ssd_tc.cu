@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kStThr, 1)
     k_ssd_state_tc(const __grid_constant__ CUtensorMap tm_u, const CumDt* __restrict__ cumdt, const SeqInfo si,
                    float* __restrict__ states, int* err) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align<1024>(smem_raw);
   StateBars* sb = reinterpret_cast<StateBars*>(smem + kStSmBar);
   volatile int* abort = &sb->abort;
   uint8_t* sB = smem + kStSmB;
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kScThr, 1)
                   const uint8_t* __restrict__ sin_img, const float* __restrict__ Dp, const SeqInfo si,
                   uint16_t* __restrict__ y, int* err) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_align<1024>(smem_raw);
   ScanBars* sb = reinterpret_cast<ScanBars*>(smem + kSmBar);
   volatile int* abort = &sb->abort;
 
@@ -397,8 +397,15 @@ __global__ void __launch_bounds__(kScThr, 1)
                     desc_kmajor_sw128(b0 + a * KS * 128) + 2 * j, idesc_g, (a | j) != 0);
         mma_commit(&sb->g);
       }
-      const uint32_t ph0 = smem_u32(smem + kSmP), pl0 = ph0 + 32 * 1024;
-      const uint32_t c0 = smem_u32(smem + kSmC), sh0 = smem_u32(smem + kSmSin), sl0 = sh0 + 16 * 1024;
+      // descriptors: the start-address field counts 16-byte units, so moving
+      // within a tile adds (bytes >> 4)
+      const uint64_t ph_d = desc_kmajor_sw128(smem_u32(smem + kSmP));
+      const uint64_t pl_d = desc_kmajor_sw128(smem_u32(smem + kSmP + 32 * 1024));
+      const uint64_t c_d = desc_kmajor_sw128(smem_u32(smem + kSmC));
+      const uint64_t sh_d = desc_kmajor_sw128(smem_u32(smem + kSmSin));
+      const uint64_t sl_d = desc_kmajor_sw128(smem_u32(smem + kSmSin + 16 * 1024));
+      const uint64_t x_d[2] = {desc_mnmajor_sw128(smem_u32(smem + kSmX0), 1024),
+                               desc_mnmajor_sw128(smem_u32(smem + kSmX1), 1024)};
       int pb = 0;   // P blocks consumed so far (slot pb % 4, use pb / 4)
       for (int hh = 0; hh < kHPG && !*abort; ++hh) {
         const int k = hh & 1;
@@ -406,7 +413,7 @@ __global__ void __launch_bounds__(kScThr, 1)
         if (!wait_ab(&sb->y_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
         tc_fence_after();
         const uint32_t yd = tmem + 256 + 128 * k, yo = yd + 64;
-        const uint32_t x0 = smem_u32(smem + (k == 0 ? kSmX0 : kSmX1));
+        const uint64_t xk = k == 0 ? x_d[0] : x_d[1];
         bool ok = true;
         for (int j = 0; j < NBLK; ++j, ++pb) {
           const int b = pb & (kScRing - 1);
@@ -417,15 +424,13 @@ __global__ void __launch_bounds__(kScThr, 1)
           tc_fence_after();
           // block j: sources [32 j, 32 j + 32) = x rows 32 j.. (4096 bytes per
           // block, 2048 per 16-source K-step); slot b = half (b & 1) of the
-          // P atoms b / 2
-          const uint32_t pa = (uint32_t)(b >> 1) * 16 * 1024;
-#pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t xd = desc_mnmajor_sw128(x0 + j * 4096 + kk * 2048, 1024);
-            const uint64_t pofs = (uint64_t)((b & 1) * 4 + kk * 2);
-            mma_f16(yd, desc_kmajor_sw128(ph0 + pa) + pofs, xd, IDESC_PX, (j | kk) != 0);
-            mma_f16(yd, desc_kmajor_sw128(pl0 + pa) + pofs, xd, IDESC_PX, 1u);
-          }
+          // P atoms b / 2 (16 KB apart), 32 bytes per K-step
+          const uint64_t xd = xk + (uint64_t)(j * 256);
+          const uint64_t po = (uint64_t)((b >> 1) * 1024 + (b & 1) * 4);
+          mma_f16(yd, ph_d + po, xd, IDESC_PX, j != 0);
+          mma_f16(yd, pl_d + po, xd, IDESC_PX, 1u);
+          mma_f16(yd, ph_d + po + 2, xd + 128, IDESC_PX, 1u);
+          mma_f16(yd, pl_d + po + 2, xd + 128, IDESC_PX, 1u);
           mma_commit(&sb->p_empty[b]);
         }
         if (!ok) break;
@@ -433,13 +438,15 @@ __global__ void __launch_bounds__(kScThr, 1)
         // Y_off = C S_in^T (S_in as bf16 high part + remainder)
         if (!wait_ab(&sb->sin_full, hh & 1, abort, err)) break;
         tc_fence_after();
+        // two 64-column atoms of C (16 KB apart) and of S_in (8 KB apart)
 #pragma unroll
         for (int a = 0; a < 2; ++a)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            const uint64_t cd = desc_kmajor_sw128(c0 + a * 128 * 128) + 2 * j;
-            mma_f16(yo, cd, desc_kmajor_sw128(sh0 + a * 64 * 128) + 2 * j, IDESC_Y, (a | j) != 0);
-            mma_f16(yo, cd, desc_kmajor_sw128(sl0 + a * 64 * 128) + 2 * j, IDESC_Y, 1u);
+            const uint64_t cd = c_d + (uint64_t)(a * 1024 + 2 * j);
+            const uint64_t so = (uint64_t)(a * 512 + 2 * j);
+            mma_f16(yo, cd, sh_d + so, IDESC_Y, (a | j) != 0);
+            mma_f16(yo, cd, sl_d + so, IDESC_Y, 1u);
           }
         mma_commit(&sb->sin_empty);
         mma_commit(&sb->y_full[k]);
@@ -530,15 +537,22 @@ __global__ void __launch_bounds__(kScThr, 1)
             v[4 * q + 3] = __uint_as_float(r[4 * q + 3]) * (rf * f.w);
           }
         } else if (j == rblk) {
+          // s > t (or a row past the chunk) selects 0; the exponential there
+          // may overflow and is discarded by the select
+          const float4* h4 = reinterpret_cast<const float4*>(cd->hi + s0);
+          const float4* l4 = reinterpret_cast<const float4*>(cd->lo + s0);
+          const float4* d4 = reinterpret_cast<const float4*>(cd->dt + s0);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const int s = s0 + e;
-            float val = 0.f;
-            if (s <= tlim) {
-              val = __uint_as_float(r[e]) * __expf((ct_hi - cd->hi[s]) + (ct_lo - cd->lo[s])) * cd->dt[s];
-              if (s == tt) val += Dh;
+          for (int q = 0; q < 8; ++q) {
+            const float4 hq = h4[q], lq = l4[q], dq = d4[q];
+            const float hs[4] = {hq.x, hq.y, hq.z, hq.w}, ls[4] = {lq.x, lq.y, lq.z, lq.w};
+            const float ds[4] = {dq.x, dq.y, dq.z, dq.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int s = s0 + 4 * q + e;
+              const float val = __uint_as_float(r[4 * q + e]) * __expf((ct_hi - hs[e]) + (ct_lo - ls[e])) * ds[e];
+              v[4 * q + e] = s <= tlim ? val + (s == tt ? Dh : 0.f) : 0.f;
             }
-            v[e] = val;
           }
         } else {
 #pragma unroll

@@ -13,6 +13,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// `raw` (a __shared__ array) rounded up to kAlign bytes by pointer arithmetic
+// on the array itself, so the compiler keeps the result in the shared address
+// space (LDS / STS rather than generic loads and stores).
+template <uint32_t kAlign>
+__device__ __forceinline__ uint8_t* smem_align(uint8_t* raw) {
+  const uint32_t a = smem_u32(raw);
+  return raw + ((kAlign - (a & (kAlign - 1))) & (kAlign - 1));
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
