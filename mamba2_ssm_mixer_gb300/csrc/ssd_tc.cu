@@ -71,13 +71,31 @@ __device__ __forceinline__ bool wait_ab(uint64_t* bar, uint32_t parity, volatile
   return false;
 }
 
-// Two floats -> bf16x2 high parts and bf16x2 remainders (v - high), low half
-// first.
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16x2(a, b);
-  lo = pack_bf16x2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
+// Packed pairs of floats (the sm_100 family's f32x2 arithmetic): element 0
+// in the low word.
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
 }
-
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// Two packed floats v -> bf16x2 high parts hi (v truncated to its top 16
+// bits) and bf16x2 remainders lo = bf16(v - hi); v - hi is exact, so
+// |v - (hi + lo)| <= 2^-9 |v - hi| < 2^-16 |v|.  Element 0 in the low half.
+__device__ __forceinline__ void split2t(uint64_t v, uint32_t& hi, uint32_t& lo) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(v), "l"(v & 0xFFFF0000FFFF0000ull));
+  uint32_t v0, v1;
+  asm("mov.b64 {%0, %1}, %2;" : "=r"(v0), "=r"(v1) : "l"(v));
+  asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(hi) : "r"(v0), "r"(v1));
+  float r0, r1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
+  lo = pack_bf16x2(r0, r1);
+}
 
 }  // namespace
 
@@ -211,13 +229,14 @@ __global__ void __launch_bounds__(kStThr, 1)
       // row t of (w x), bf16 high part and remainder, in the x tile's own
       // layout; buffer k was last read by head hh-2's MMA, which this thread
       // saw finish in that head's epilogue
+      const uint64_t w2 = pk2(w, w);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         uint32_t hi[4], lo[4];
         const uint32_t wd[4] = {xv[q].x, xv[q].y, xv[q].z, xv[q].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          split2(w * __uint_as_float(wd[e] << 16), w * __uint_as_float(wd[e] & 0xFFFF0000u), hi[e], lo[e]);
+          split2t(mul2(w2, pk2(__uint_as_float(wd[e] << 16), __uint_as_float(wd[e] & 0xFFFF0000u))), hi[e], lo[e]);
         const uint32_t off = sw_row_chunk(t, q);
         *reinterpret_cast<uint4*>(sWh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -524,17 +543,19 @@ __global__ void __launch_bounds__(kScThr, 1)
         // both factors <= 1 with e the block's last source (the second, times
         // dt_s, is colf_s).  On it: one exp per element, and D on s = t.
         float v[32];
+        uint32_t hi[16], lo[16];   // bf16 pairs: sources 2i, 2i+1
         if (j < rblk) {
           const int e = min(j * 32 + 31, cp.n - 1);
           const float rf = tt < cp.n ? __expf((ct_hi - cd->hi[e]) + (ct_lo - cd->lo[e])) : 0.f;
+          const uint64_t rf2 = pk2(rf, rf);
           const float4* cf = reinterpret_cast<const float4*>(cd->colf + s0);
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const float4 f = cf[q];
-            v[4 * q + 0] = __uint_as_float(r[4 * q + 0]) * (rf * f.x);
-            v[4 * q + 1] = __uint_as_float(r[4 * q + 1]) * (rf * f.y);
-            v[4 * q + 2] = __uint_as_float(r[4 * q + 2]) * (rf * f.z);
-            v[4 * q + 3] = __uint_as_float(r[4 * q + 3]) * (rf * f.w);
+            const uint64_t g01 = pk2(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]));
+            const uint64_t g23 = pk2(__uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+            split2t(mul2(g01, mul2(rf2, pk2(f.x, f.y))), hi[2 * q], lo[2 * q]);
+            split2t(mul2(g23, mul2(rf2, pk2(f.z, f.w))), hi[2 * q + 1], lo[2 * q + 1]);
           }
         } else if (j == rblk) {
           // s > t (or a row past the chunk) selects 0; the exponential there
@@ -554,21 +575,20 @@ __global__ void __launch_bounds__(kScThr, 1)
               v[4 * q + e] = s <= tlim ? val + (s == tt ? Dh : 0.f) : 0.f;
             }
           }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) split2t(pk2(v[2 * e], v[2 * e + 1]), hi[e], lo[e]);
         } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = 0.f;
+          for (int e = 0; e < 16; ++e) hi[e] = lo[e] = 0u;
         }
         // 32 sources = the four 16-byte chunks (b & 1) * 4 + q of this row in
         // the P atoms b / 2
         const uint32_t pa = (uint32_t)(b >> 1) * 16 * 1024;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split2(v[8 * q + 2 * e], v[8 * q + 2 * e + 1], hi[e], lo[e]);
           const uint32_t off = pa + sw_chunk(row, (b & 1) * 4 + q, 128);
-          *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(sPh + off) = make_uint4(hi[4 * q], hi[4 * q + 1], hi[4 * q + 2], hi[4 * q + 3]);
+          *reinterpret_cast<uint4*>(sPl + off) = make_uint4(lo[4 * q], lo[4 * q + 1], lo[4 * q + 2], lo[4 * q + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
