@@ -203,6 +203,24 @@ def run_reference(args, rank, world):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------- replicas
+def max_over_ranks(x, dist=None, device=None):
+    """The largest value of x over all ranks (the slowest replica sets the
+    step time); x itself when there is one rank."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, ms_max, world):
+    """Whole-job tokens/s: every replica processes tokens_per_rank tokens per
+    step; the job's step lasts as long as its slowest replica."""
+    return tokens_per_rank * world / (ms_max * 1e-3)
+
+
 # ---------------------------------------------------------------- ours (GPU)
 
 def build_workload(dev):
@@ -334,10 +352,7 @@ def run_ours(args, rank, world, local_rank):
     blk.check()
     ms = ms_graph if ms_graph is not None else ms_eager
     launches = int(round(launches_per_step * args.steps))
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
 
     # ---- end to end: host buffers, copies inside the timed interval
     hd_pin = torch.from_numpy(h_dec_np).to(torch.bfloat16).pin_memory()
@@ -356,10 +371,7 @@ def run_ours(args, rank, world, local_rank):
         e2e_ev[i][1].record()
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
     h2d = hd_pin.numel() * 2 + hp_pin.numel() * 2
     d2h = od_pin.numel() * 2 + op_pin.numel() * 2
 
@@ -402,7 +414,7 @@ def run_ours(args, rank, world, local_rank):
     cb = None
     if world == 1 and not args.no_cpu_baseline:
         cb, _ = oracle_sample()
-    value = TOKENS_PER_STEP * world / (ms * 1e-3)
+    value = job_throughput(TOKENS_PER_STEP, ms, world)
     line = dict(metric=METRIC, value=value, unit="tokens/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
                 ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="fp8",
                 data="synthetic",
@@ -419,7 +431,7 @@ def run_ours(args, rank, world, local_rank):
                                                               "dec_out_proj")) / args.steps,
                             graph_error=None if graph is not None else graph_error),
                 clocks=clocks,
-                e2e=dict(value=TOKENS_PER_STEP * world / (e2e_ms * 1e-3), unit="tokens/s",
+                e2e=dict(value=job_throughput(TOKENS_PER_STEP, e2e_ms, world), unit="tokens/s",
                          h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h),
                 gpu_launches=launches, roofline=roof, cpu_baseline=cb,
                 stages={k: {kk: (round(vv, 5) if isinstance(vv, float) else vv) for kk, vv in v.items()}
