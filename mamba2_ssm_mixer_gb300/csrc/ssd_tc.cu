@@ -294,7 +294,7 @@ constexpr int kSmBar = 200 * 1024;      // barriers
 constexpr int kScanSmem = kSmBar + 256 + 1024;
 
 struct ScanBars {
-  uint64_t cb, g, drain, sin_full, sin_empty;
+  uint64_t cb, g, drain, drain_ld, sin_full, sin_empty;
   uint64_t op_full[2], op_empty[2];
   uint64_t p_full[kScRing], p_empty[kScRing];
   uint64_t y_full[2], y_empty[2];
@@ -326,12 +326,13 @@ __global__ void __launch_bounds__(kScThr, 1)
     mbar_init(&sb->cb, 1);
     mbar_init(&sb->g, 1);
     mbar_init(&sb->drain, 1);
+    mbar_init(&sb->drain_ld, 1);
     mbar_init(&sb->sin_full, 1);
     mbar_init(&sb->sin_empty, 1);
     for (int k = 0; k < 2; ++k) {
       mbar_init(&sb->op_full[k], 1);
       mbar_init(&sb->op_empty[k], 1 + kScPW);   // MMA commit + each P warp
-      mbar_init(&sb->y_full[k], 1);
+      mbar_init(&sb->y_full[k], 2);           // P x (MMA warp) and C S_in^T (load warp)
       mbar_init(&sb->y_empty[k], kScPW);
     }
     for (int k = 0; k < kScRing; ++k) {
@@ -393,6 +394,35 @@ __global__ void __launch_bounds__(kScThr, 1)
         mbar_expect_tx(&sb->sin_full, (uint32_t)kSinImageBytes);
         bulk_g2s(smem + kSmSin, sin_img + (ch0 + hh) * kSinImageBytes, kSinImageBytes, &sb->sin_full);
         sin_issued = hh;
+        // Y_off = C S_in^T of head hh (S_in as bf16 high part + remainder),
+        // issued from this warp so the MMA warp only issues P x; Y_off[k] is
+        // free once head hh-2's epilogue has read it
+        if (!wait_ab(&sb->cb, 0, abort, err)) break;
+        if (!wait_ab(&sb->sin_full, hh & 1, abort, err)) break;
+        if (!wait_ab(&sb->y_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
+        tc_fence_after();
+        {
+          const uint64_t c_d = desc_kmajor_sw128(smem_u32(smem + kSmC));
+          const uint64_t sh_d = desc_kmajor_sw128(smem_u32(smem + kSmSin));
+          const uint64_t sl_d = desc_kmajor_sw128(smem_u32(smem + kSmSin + 16 * 1024));
+          const uint32_t yo = tmem + 320 + 128 * k;
+          // two 64-column atoms of C (16 KB apart) and of S_in (8 KB apart)
+#pragma unroll
+          for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t cd = c_d + (uint64_t)(a * 1024 + 2 * j);
+              const uint64_t so = (uint64_t)(a * 512 + 2 * j);
+              mma_f16(yo, cd, sh_d + so, IDESC_Y, (a | j) != 0);
+              mma_f16(yo, cd, sl_d + so, IDESC_Y, 1u);
+            }
+        }
+        mma_commit(&sb->sin_empty);
+        mma_commit(&sb->y_full[k]);
+      }
+      if (*abort) {   // no MMA of this warp may still run when TMEM is freed
+        mma_commit(&sb->drain_ld);
+        mbar_wait(&sb->drain_ld, 0, nullptr, 100000000ull);
       }
       if (*abort) {   // let copies in flight land before the CTA can exit
         mbar_wait(&sb->cb, 0, nullptr, 100000000ull);
@@ -420,9 +450,6 @@ __global__ void __launch_bounds__(kScThr, 1)
       // within a tile adds (bytes >> 4)
       const uint64_t ph_d = desc_kmajor_sw128(smem_u32(smem + kSmP));
       const uint64_t pl_d = desc_kmajor_sw128(smem_u32(smem + kSmP + 32 * 1024));
-      const uint64_t c_d = desc_kmajor_sw128(smem_u32(smem + kSmC));
-      const uint64_t sh_d = desc_kmajor_sw128(smem_u32(smem + kSmSin));
-      const uint64_t sl_d = desc_kmajor_sw128(smem_u32(smem + kSmSin + 16 * 1024));
       const uint64_t x_d[2] = {desc_mnmajor_sw128(smem_u32(smem + kSmX0), 1024),
                                desc_mnmajor_sw128(smem_u32(smem + kSmX1), 1024)};
       int pb = 0;   // P blocks consumed so far (slot pb % 4, use pb / 4)
@@ -431,7 +458,7 @@ __global__ void __launch_bounds__(kScThr, 1)
         if (!wait_ab(&sb->op_full[k], (hh >> 1) & 1, abort, err)) break;
         if (!wait_ab(&sb->y_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
         tc_fence_after();
-        const uint32_t yd = tmem + 256 + 128 * k, yo = yd + 64;
+        const uint32_t yd = tmem + 256 + 128 * k;
         const uint64_t xk = k == 0 ? x_d[0] : x_d[1];
         bool ok = true;
         for (int j = 0; j < NBLK; ++j, ++pb) {
@@ -454,20 +481,6 @@ __global__ void __launch_bounds__(kScThr, 1)
         }
         if (!ok) break;
         mma_commit(&sb->op_empty[k]);   // x(hh) is no longer read once these finish
-        // Y_off = C S_in^T (S_in as bf16 high part + remainder)
-        if (!wait_ab(&sb->sin_full, hh & 1, abort, err)) break;
-        tc_fence_after();
-        // two 64-column atoms of C (16 KB apart) and of S_in (8 KB apart)
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t cd = c_d + (uint64_t)(a * 1024 + 2 * j);
-            const uint64_t so = (uint64_t)(a * 512 + 2 * j);
-            mma_f16(yo, cd, sh_d + so, IDESC_Y, (a | j) != 0);
-            mma_f16(yo, cd, sl_d + so, IDESC_Y, 1u);
-          }
-        mma_commit(&sb->sin_empty);
         mma_commit(&sb->y_full[k]);
       }
       if (*abort) {
