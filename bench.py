@@ -495,6 +495,85 @@ def measure_fp8_peak():
     print(json.dumps(rec))
 
 
+def run_stack(args):
+    """The 23-block stack (NemotronH's Mamba2 layers, pre-norm residual):
+    decode of 128 rows from a 512-slot pool per layer, then a varlen prefill of
+    {4096, 1024, 512, 37} tokens from zero state; each step replayed from a
+    CUDA graph, with the plain glue (residual RMSNorm, then each block quantises
+    its bf16 input) and the fused glue (the RMSNorm writes the next block's
+    e4m3 input).  Prints one JSON line (not the headline metric)."""
+    import torch
+
+    import mamba2_ssm_mixer_gb300 as m2
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    L, Bt, slots_n, lens = 23, 128, 512, [4096, 1024, 512, 37]
+    blocks, norm_ws = [], []
+    for l in range(L):
+        Wt = synth.make_weights(4, l)
+        blocks.append(m2.Mamba2Mixer(dict(
+            in_proj=torch.from_numpy(Wt["in_proj"]).to(dev), s_w1=Wt["s_w1"],
+            out_proj=torch.from_numpy(Wt["out_proj"]).to(dev), s_w2=Wt["s_w2"],
+            conv_w=torch.from_numpy(Wt["conv_w"]).to(torch.bfloat16).to(dev), conv_b=None,
+            A_log=torch.from_numpy(Wt["A_log"]).to(dev), D=torch.from_numpy(Wt["D"]).to(dev),
+            dt_bias=torch.from_numpy(Wt["dt_bias"]).to(dev),
+            norm_w=torch.from_numpy(Wt["norm_w"]).to(torch.bfloat16).to(dev),
+            s_x=Wt["s_x"], s_y=Wt["s_y"], eps=Wt["eps"]), device=dev))
+        norm_ws.append(torch.from_numpy(synth.make_stack_norm_w(4, l)).to(torch.bfloat16).to(dev))
+    conv_pools = [synth.device_normal((slots_n, CONV, 3), 4, l, synth.T_CONV_STATE, 1.0, torch.bfloat16, dev)
+                  for l in range(L)]
+    ssm_pools = [synth.device_normal((slots_n, 64, 64, 128), 4, l, synth.T_SSM_STATE, 0.1, torch.float32, dev)
+                 for l in range(L)]
+    slot_idx = torch.from_numpy(synth.make_slot_idx(4, slots_n, Bt)).to(dev)
+    h_dec = torch.from_numpy(synth.make_hidden(4, Bt)).to(torch.bfloat16).to(dev)
+    h_pf = torch.from_numpy(synth.make_hidden(5, sum(lens))).to(torch.bfloat16).to(dev)
+    conv_st = [torch.zeros((len(lens), CONV, 3), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    ssm_st = [torch.zeros((len(lens), 64, 64, 128), dtype=torch.float32, device=dev) for _ in range(L)]
+    ws_dec = torch.empty(blocks[0].decode_workspace_size(Bt), dtype=torch.uint8, device=dev)
+    ws_pf = torch.empty(blocks[0].prefill_workspace_size(lens), dtype=torch.uint8, device=dev)
+
+    def measure(stack, fn):
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            fn(stack)
+        torch.cuda.current_stream(dev).wait_stream(cs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            fn(stack)
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a, b in ev:
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / args.steps
+
+    dec = lambda s: s.decode(h_dec, conv_pools, ssm_pools, slot_idx, workspace=ws_dec)
+    pf = lambda s: s.prefill(h_pf, lens, conv_st, ssm_st, workspace=ws_pf)
+    res = {}
+    for name, fused in (("plain", False), ("fused", True)):
+        st = m2.Mamba2Stack(blocks, norm_ws, 1e-5, fused=fused)
+        res[name] = dict(decode_ms=measure(st, dec), prefill_ms=measure(st, pf))
+    for b in blocks:
+        b.check()
+    dec_bytes = L * (38.7e6 + Bt * (4 * 2 ** 20 + 2 * CONV * 3 * 2))
+    best = res["fused"]
+    line = dict(case="stack", workload=f"23 Mamba2 blocks: decode {Bt} rows from {slots_n}-slot pools, "
+                                       f"then prefill {lens} from zero state", steps=args.steps,
+                launch="cuda_graph", results=res,
+                decode_tokens_per_s=Bt / (best["decode_ms"] * 1e-3),
+                decode_gbs=dec_bytes / (best["decode_ms"] * 1e-3) / 1e9,
+                prefill_tokens_per_s=sum(lens) / (best["prefill_ms"] * 1e-3),
+                decode_algorithmic_bytes=dec_bytes)
+    print(json.dumps(line))
+
+
 def run_case(args):
     """One kernel family at its bench-workload shape, for profiler captures
     (ncu -k <kernel> -c <n>): --case in_proj | out_proj | decode | prefill."""
@@ -529,7 +608,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill"], default=None,
+    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill", "stack"], default=None,
                     help="run one kernel family at the workload shape (for profiler captures); prints nothing")
     ap.add_argument("--measure-fp8-peak", action="store_true",
                     help="time cuBLAS e4m3 GEMMs and record the FP8 peak under profiles/")
@@ -541,6 +620,8 @@ def main():
         args.warmup = 3
     if args.measure_fp8_peak:
         measure_fp8_peak()
+    elif args.case == "stack":
+        run_stack(args)
     elif args.case:
         run_case(args)
     elif args.impl == "reference":

@@ -199,6 +199,16 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
                      const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state,
                      uint16_t* out, void* workspace, size_t ws_bytes, void* stream);
 
+/*
+ * m2_prefill with the block's input already quantised: hidden_q e4m3 [sum(T),
+ * 2688] device, 16-byte aligned, holding e4m3(x / s_x) for the handle's s_x
+ * (as fp8_quant or m2_rmsnorm_residual_quant write it).  The block's own
+ * input quant is skipped; everything else is m2_prefill.
+ */
+m2_status m2_prefill_q(m2_handle* h, const uint8_t* hidden_q, const int32_t* seqlens_host, int nseq,
+                       const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state,
+                       uint16_t* out, void* workspace, size_t ws_bytes, void* stream);
+
 /* Workspace bytes m2_decode needs for a batch of Bt rows. */
 m2_status m2_decode_workspace_size(const m2_handle* h, int Bt, size_t* bytes);
 
@@ -219,6 +229,12 @@ m2_status m2_decode_workspace_size(const m2_handle* h, int Bt, size_t* bytes);
 m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, float* ssm_pool,
                     int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
                     void* stream);
+
+/* m2_decode with the input already quantised (hidden_q e4m3 [Bt, 2688], as in
+ * m2_prefill_q). */
+m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* conv_pool, float* ssm_pool,
+                      int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
+                      void* stream);
 
 /*
  * Standalone static per-tensor activation quantisation (the kQuantFp8Static
@@ -290,6 +306,20 @@ m2_status fp8_linear_bf16(const uint16_t* x, float s_a, const uint8_t* w_q, floa
  */
 m2_status m2_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps,
                               uint16_t* normed, int T, int n, void* stream);
+
+/*
+ * The same step fused with the next block's static activation quant: h (and
+ * normed, if not NULL) as m2_rmsnorm_residual, and
+ *   q[t, :] = e4m3(normed[t, :] / s_q)        (round to nearest even, saturating)
+ * from the bf16 normed value, i.e. exactly the codes fp8_quant would write
+ * for it (the static per-tensor quant of PR #988, section "The Thor finding,
+ * measured"), so
+ * m2_prefill_q / m2_decode_q of the next block see the input m2_prefill /
+ * m2_decode would have quantised themselves, one HBM pass fewer.
+ * q e4m3 [T, n] device, 8-byte aligned; w is required; s_q > 0.
+ */
+m2_status m2_rmsnorm_residual_quant(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps, float s_q,
+                                    uint16_t* normed, uint8_t* q, int T, int n, void* stream);
 
 #ifdef __cplusplus
 }

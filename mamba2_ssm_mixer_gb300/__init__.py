@@ -32,7 +32,8 @@ STATUS_NAMES = {0: "M2_OK", 1: "M2_EINVAL", 2: "M2_ESHAPE", 3: "M2_ECUDA", 4: "M
 EXPORTED = ["m2_last_error", "m2_create", "m2_destroy", "m2_get_stats", "m2_set_taps", "m2_check",
             "m2_prefill_workspace_size", "m2_prefill", "m2_decode_workspace_size", "m2_decode",
             "fp8_quant", "fp8_linear_workspace_size", "fp8_linear", "fp8_linear_bf16",
-            "m2_rmsnorm_residual", "m2_profile_enable", "m2_profile_read", "fp8_linear_noalloc"]
+            "m2_rmsnorm_residual", "m2_profile_enable", "m2_profile_read", "fp8_linear_noalloc",
+            "m2_prefill_q", "m2_decode_q", "m2_rmsnorm_residual_quant"]
 
 STAGES = ["quant_in", "in_proj", "conv", "conv_state", "ssd_cumsum", "ssd_chunk_state", "ssd_state_pass",
           "ssd_chunk_scan", "norm_quant", "out_proj", "decode_fused", "dec_quant_in", "dec_in_proj",
@@ -91,6 +92,9 @@ _sigs = {
     "m2_profile_enable": ([_vp, _i], _i),
     "m2_profile_read": ([_vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint64)], _i),
     "fp8_linear_noalloc": ([_vp, _f, _vp, _f, _vp, _i, _i, _i, _vp], _i),
+    "m2_prefill_q": ([_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
+    "m2_decode_q": ([_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp], _i),
+    "m2_rmsnorm_residual_quant": ([_vp, _vp, _vp, _f, _f, _vp, _vp, _i, _i, _vp], _i),
 }
 for _name, (_args, _ret) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -167,6 +171,7 @@ class Mamba2Mixer:
             _check(_lib.m2_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(h)))
         self._h = h
         self._taps = None
+        self.s_x = float(weights["s_x"])   # the input quant scale (for pre-quantised inputs)
 
     def close(self):
         if getattr(self, "_h", None):
@@ -225,8 +230,11 @@ class Mamba2Mixer:
 
     def prefill(self, hidden, seqlens, conv_state, ssm_state, has_initial=None, out=None, workspace=None,
                 stream=None):
+        """hidden: bf16 [sum(T), 2688], or e4m3 codes (uint8) already quantised
+        with this block's s_x (m2_prefill_q)."""
         T = sum(seqlens)
-        _need(hidden, "hidden", torch.bfloat16, (T, HIDDEN))
+        quantised = hidden.dtype == torch.uint8
+        _need(hidden, "hidden", torch.uint8 if quantised else torch.bfloat16, (T, HIDDEN))
         _need(conv_state, "conv_state", torch.bfloat16, (len(seqlens), CONV_DIM, CONV_WIDTH - 1))
         _need(ssm_state, "ssm_state", torch.float32, (len(seqlens), NHEADS, HEADDIM, D_STATE))
         if out is None:
@@ -236,13 +244,17 @@ class Mamba2Mixer:
             workspace = torch.empty(self.prefill_workspace_size(seqlens), dtype=torch.uint8, device=hidden.device)
         arr = (ctypes.c_int32 * len(seqlens))(*seqlens)
         hi = None if has_initial is None else (ctypes.c_uint8 * len(seqlens))(*[int(bool(v)) for v in has_initial])
-        _check(_lib.m2_prefill(self._h, _ptr(hidden), arr, len(seqlens), hi, _ptr(conv_state), _ptr(ssm_state),
-                               _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+        fn = _lib.m2_prefill_q if quantised else _lib.m2_prefill
+        _check(fn(self._h, _ptr(hidden), arr, len(seqlens), hi, _ptr(conv_state), _ptr(ssm_state),
+                  _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
         return out
 
     def decode(self, hidden, conv_pool, ssm_pool, slot_idx, out=None, workspace=None, stream=None):
+        """hidden: bf16 [Bt, 2688], or e4m3 codes (uint8) already quantised with
+        this block's s_x (m2_decode_q)."""
         Bt = hidden.shape[0]
-        _need(hidden, "hidden", torch.bfloat16, (Bt, HIDDEN))
+        quantised = hidden.dtype == torch.uint8
+        _need(hidden, "hidden", torch.uint8 if quantised else torch.bfloat16, (Bt, HIDDEN))
         n_slots = conv_pool.shape[0]
         _need(conv_pool, "conv_pool", torch.bfloat16, (n_slots, CONV_DIM, CONV_WIDTH - 1))
         _need(ssm_pool, "ssm_pool", torch.float32, (n_slots, NHEADS, HEADDIM, D_STATE))
@@ -252,8 +264,9 @@ class Mamba2Mixer:
         _need(out, "out", torch.bfloat16, (Bt, HIDDEN))
         if workspace is None:
             workspace = torch.empty(self.decode_workspace_size(Bt), dtype=torch.uint8, device=hidden.device)
-        _check(_lib.m2_decode(self._h, _ptr(hidden), Bt, _ptr(conv_pool), _ptr(ssm_pool), n_slots, _ptr(slot_idx),
-                              _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
+        fn = _lib.m2_decode_q if quantised else _lib.m2_decode
+        _check(fn(self._h, _ptr(hidden), Bt, _ptr(conv_pool), _ptr(ssm_pool), n_slots, _ptr(slot_idx),
+                  _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
         return out
 
 
@@ -334,22 +347,51 @@ def m2_rmsnorm_residual(h: torch.Tensor, add: torch.Tensor | None, w: torch.Tens
     return normed
 
 
+def m2_rmsnorm_residual_quant(h: torch.Tensor, add: torch.Tensor | None, w: torch.Tensor, eps: float, s_q: float,
+                              q: torch.Tensor | None = None, normed: torch.Tensor | None = None, stream=None):
+    """h += add (if given); returns e4m3 codes of rmsnorm(h) * w / s_q (and
+    writes the bf16 normed row too when `normed` is given)."""
+    T, n = h.shape
+    _need(h, "h", torch.bfloat16)
+    if add is not None:
+        _need(add, "add", torch.bfloat16, (T, n))
+    _need(w, "w", torch.bfloat16, (n,))
+    if normed is not None:
+        _need(normed, "normed", torch.bfloat16, (T, n))
+    if q is None:
+        q = torch.empty((T, n), dtype=torch.uint8, device=h.device)
+    _need(q, "q", torch.uint8, (T, n))
+    _check(_lib.m2_rmsnorm_residual_quant(_ptr(h), _ptr(add), _ptr(w), eps, s_q, _ptr(normed), _ptr(q), T, n,
+                                          _stream(stream)))
+    return q
+
+
 class Mamba2Stack:
     """Pre-norm residual stack of mixer blocks: for each layer l,
     h <- h + block_l(rmsnorm(h) * norm_w[l]).  Host-side composition of the
     C ABI calls (one rmsnorm_residual and one block call per layer)."""
 
-    def __init__(self, blocks: list, norm_ws: list, eps: float = 1e-5):
+    def __init__(self, blocks: list, norm_ws: list, eps: float = 1e-5, fused: bool = False):
+        """fused: each layer's residual + RMSNorm also writes the next block's
+        e4m3 input (m2_rmsnorm_residual_quant), and the blocks run from it
+        (m2_prefill_q / m2_decode_q) instead of quantising a bf16 copy."""
         assert len(blocks) == len(norm_ws) and blocks
-        self.blocks, self.norm_ws, self.eps = blocks, norm_ws, eps
+        self.blocks, self.norm_ws, self.eps, self.fused = blocks, norm_ws, eps, fused
 
     def _run(self, hidden, call, stream):
         h = hidden.clone()
-        normed = torch.empty_like(h)
         out = torch.empty_like(h)
+        if self.fused:
+            x = torch.empty(h.shape, dtype=torch.uint8, device=h.device)
+        else:
+            x = torch.empty_like(h)
         for l, blk in enumerate(self.blocks):
-            m2_rmsnorm_residual(h, out if l else None, self.norm_ws[l], self.eps, normed, stream=stream)
-            call(l, blk, normed, out)
+            if self.fused:
+                m2_rmsnorm_residual_quant(h, out if l else None, self.norm_ws[l], self.eps, blk.s_x, q=x,
+                                          stream=stream)
+            else:
+                m2_rmsnorm_residual(h, out if l else None, self.norm_ws[l], self.eps, x, stream=stream)
+            call(l, blk, x, out)
         m2_rmsnorm_residual(h, out, None, self.eps, stream=stream, norm=False)
         return h
 

@@ -269,11 +269,14 @@ cudaError_t launch_gated_norm_quant(const uint16_t* y, const uint16_t* zx, const
 }
 
 // ---------------------------------------------------------------------------
-// Residual add + RMSNorm between stacked blocks.  One CTA per row.
+// Residual add + RMSNorm between stacked blocks, optionally with the next
+// block's static e4m3 activation quant of the normed row (the same bf16
+// normed value, then the same code as fp8_quant).  One CTA per row.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_rmsnorm_residual(uint16_t* __restrict__ h, const uint16_t* __restrict__ add,
                                                           const uint16_t* __restrict__ w, float eps,
-                                                          uint16_t* __restrict__ normed, int n) {
+                                                          uint16_t* __restrict__ normed, uint8_t* __restrict__ q,
+                                                          float s_q, float inv_q, int n) {
   __shared__ float red[8];
   pdl_wait();
   pdl_trigger();
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm_residual(uint16_t* __restrict__
   uint16_t* hr = h + (size_t)t * n;
   const int nv = n / 8;
   float ss = 0.f;
-  if (!normed) {   // residual add only
+  if (!normed && !q) {   // residual add only
     for (int v = threadIdx.x; v < nv; v += blockDim.x) {
       uint4 hv = reinterpret_cast<uint4*>(hr)[v];
       uint16_t* hb = reinterpret_cast<uint16_t*>(&hv);
@@ -322,14 +325,22 @@ __global__ void __launch_bounds__(256) k_rmsnorm_residual(uint16_t* __restrict__
     uint16_t* ob = reinterpret_cast<uint16_t*>(&ov);
 #pragma unroll
     for (int e = 0; e < 8; ++e) ob[e] = f2bfbits(bfbits2f(hb[e]) * r * bfbits2f(wb[e]));
-    reinterpret_cast<uint4*>(normed + (size_t)t * n)[v] = ov;
+    if (normed) reinterpret_cast<uint4*>(normed + (size_t)t * n)[v] = ov;
+    if (q) {
+      uint32_t c[2] = {0u, 0u};
+#pragma unroll
+      for (int e = 0; e < 8; e += 2)
+        c[e >> 2] |= (uint32_t)quant2_e4m3(bfbits2f(ob[e]), bfbits2f(ob[e + 1]), s_q, inv_q) << (8 * (e & 3));
+      reinterpret_cast<uint2*>(q + (size_t)t * n)[v] = make_uint2(c[0], c[1]);
+    }
   }
 }
 
 cudaError_t launch_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps,
-                                    uint16_t* normed, int T, int n, cudaStream_t st) {
+                                    uint16_t* normed, uint8_t* q, float s_q, int T, int n, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  return launch_pdl(k_rmsnorm_residual, dim3(T), dim3(256), 0, st, h, add, w, eps, normed, n);
+  return launch_pdl(k_rmsnorm_residual, dim3(T), dim3(256), 0, st, h, add, w, eps, normed, q, s_q,
+                    q ? exact_inverse(s_q) : 0.f, n);
 }
 
 }  // namespace m2

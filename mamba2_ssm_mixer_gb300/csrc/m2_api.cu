@@ -1,6 +1,7 @@
 // The C ABI of libm2 (declared in include/m2.h): argument validation, the
 // handle that owns the block's device weights, workspace carving, and the
 // launch sequence of prefill and decode.  All compute runs in the kernels.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -350,14 +351,17 @@ static m2_status copy_tap(void* dst, const void* src, size_t bytes, cudaStream_t
   return M2_OK;
 }
 
-m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlens_host, int nseq,
-                     const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state, uint16_t* out,
-                     void* workspace, size_t ws_bytes, void* stream) {
+// The block's prefill from bf16 hidden (quantised here) or from hidden_q,
+// already quantised with the handle's s_x (exactly one of the two given).
+static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_t* hidden_q,
+                              const int32_t* seqlens_host, int nseq, const uint8_t* has_initial,
+                              uint16_t* conv_state, float* ssm_state, uint16_t* out, void* workspace,
+                              size_t ws_bytes, void* stream) {
   g_err.clear();
-  if (!h || !hidden || !conv_state || !ssm_state || !out || !workspace)
+  if (!h || (!hidden && !hidden_q) || !conv_state || !ssm_state || !out || !workspace)
     return fail(M2_EINVAL, "m2_prefill: null argument");
   if ((uintptr_t)workspace % 256) return fail(M2_EINVAL, "m2_prefill: workspace must be 256-byte aligned");
-  if ((uintptr_t)hidden % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_state % 16)
+  if ((uintptr_t)hidden % 16 || (uintptr_t)hidden_q % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_state % 16)
     return fail(M2_EINVAL, "m2_prefill: hidden, out and ssm_state must be 16-byte aligned");
   SeqInfo local;
   m2_status s = build_seqinfo(seqlens_host, nseq, has_initial, &local);
@@ -371,8 +375,10 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
   const float sc1 = h->cfg.s_x * h->s_w1, sc2 = h->cfg.s_y * h->s_w2;
 
   int nl = 0;
-  M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
-  M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  const uint8_t* q = hidden_q ? hidden_q : w.q;
+  if (!hidden_q)
+    M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
+  M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(w.zx, bp, conv_state, local, w.u, st));
   M2_STAGE(h, st, M2_STAGE_CONV_STATE, 1, launch_conv_state_update(w.zx, conv_state, local, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1,
@@ -387,7 +393,7 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
            launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, h->taps_on ? h->taps.o : nullptr, st));
   M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   if (h->taps_on) {
-    if ((s = copy_tap(h->taps.q, w.q, (size_t)T * kH, st))) return s;
+    if ((s = copy_tap(h->taps.q, q, (size_t)T * kH, st))) return s;
     if ((s = copy_tap(h->taps.zx, w.zx, (size_t)T * kZ * 2, st))) return s;
     if ((s = copy_tap(h->taps.u, w.u, (size_t)T * kConv * 2, st))) return s;
     if ((s = copy_tap(h->taps.y, w.y, (size_t)T * kI * 2, st))) return s;
@@ -397,6 +403,22 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
   h->stats.conv_fwd_calls += 1;
   h->stats.chunk_scan_calls += 1;
   return M2_OK;
+}
+
+m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlens_host, int nseq,
+                     const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state, uint16_t* out,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  if (!hidden) return fail(M2_EINVAL, "m2_prefill: null argument");
+  return prefill_impl(h, hidden, nullptr, seqlens_host, nseq, has_initial, conv_state, ssm_state, out, workspace,
+                      ws_bytes, stream);
+}
+
+m2_status m2_prefill_q(m2_handle* h, const uint8_t* hidden_q, const int32_t* seqlens_host, int nseq,
+                       const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state, uint16_t* out,
+                       void* workspace, size_t ws_bytes, void* stream) {
+  if (!hidden_q) return fail(M2_EINVAL, "m2_prefill_q: null argument");
+  return prefill_impl(h, nullptr, hidden_q, seqlens_host, nseq, has_initial, conv_state, ssm_state, out, workspace,
+                      ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- decode
@@ -430,16 +452,16 @@ m2_status m2_decode_workspace_size(const m2_handle* h, int Bt, size_t* bytes) {
   return M2_OK;
 }
 
-m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, float* ssm_pool,
-                    int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
-                    void* stream) {
+static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t* hidden_q, int Bt,
+                             uint16_t* conv_pool, float* ssm_pool, int n_slots, const int32_t* slot_idx,
+                             uint16_t* out, void* workspace, size_t ws_bytes, void* stream) {
   g_err.clear();
-  if (!h || !hidden || !conv_pool || !ssm_pool || !slot_idx || !out || !workspace)
+  if (!h || (!hidden && !hidden_q) || !conv_pool || !ssm_pool || !slot_idx || !out || !workspace)
     return fail(M2_EINVAL, "m2_decode: null argument");
   if (Bt < 1 || Bt > 4096) return fail(M2_ESHAPE, "m2_decode: Bt %d not in [1, 4096]", Bt);
   if (n_slots < 1) return fail(M2_EINVAL, "m2_decode: n_slots %d < 1", n_slots);
   if ((uintptr_t)workspace % 256) return fail(M2_EINVAL, "m2_decode: workspace must be 256-byte aligned");
-  if ((uintptr_t)hidden % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_pool % 16)
+  if ((uintptr_t)hidden % 16 || (uintptr_t)hidden_q % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_pool % 16)
     return fail(M2_EINVAL, "m2_decode: hidden, out and ssm_pool must be 16-byte aligned");
   DecodeWs w = carve_decode(workspace, Bt);
   if (ws_bytes < w.total) return fail(M2_ENOMEM, "m2_decode: workspace %zu bytes < %zu needed", ws_bytes, w.total);
@@ -454,14 +476,16 @@ m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv
     dt.o = h->taps.o;
   }
   int nl = 0;
-  M2_STAGE(h, st, M2_STAGE_DEC_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)Bt * kH, h->cfg.s_x, w.q, st));
-  M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl, gemm_fp8(w.q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  const uint8_t* q = hidden_q ? hidden_q : w.q;
+  if (!hidden_q)
+    M2_STAGE(h, st, M2_STAGE_DEC_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)Bt * kH, h->cfg.s_x, w.q, st));
+  M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl, gemm_fp8(q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
            launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, n_slots, slot_idx, Bt, w.q2, h->err, dt, st));
   M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   if (h->taps_on) {
     m2_status s;
-    if ((s = copy_tap(h->taps.q, w.q, (size_t)Bt * kH, st))) return s;
+    if ((s = copy_tap(h->taps.q, q, (size_t)Bt * kH, st))) return s;
     if ((s = copy_tap(h->taps.zx, w.zx, (size_t)Bt * kZ * 2, st))) return s;
     if ((s = copy_tap(h->taps.q2, w.q2, (size_t)Bt * kI, st))) return s;
   }
@@ -469,6 +493,22 @@ m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv
   h->stats.conv_update_rows += (uint64_t)Bt;
   h->stats.state_update_rows += (uint64_t)Bt;
   return M2_OK;
+}
+
+m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, float* ssm_pool,
+                    int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  if (!hidden) return fail(M2_EINVAL, "m2_decode: null argument");
+  return decode_impl(h, hidden, nullptr, Bt, conv_pool, ssm_pool, n_slots, slot_idx, out, workspace, ws_bytes,
+                     stream);
+}
+
+m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* conv_pool, float* ssm_pool,
+                      int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
+                      void* stream) {
+  if (!hidden_q) return fail(M2_EINVAL, "m2_decode_q: null argument");
+  return decode_impl(h, nullptr, hidden_q, Bt, conv_pool, ssm_pool, n_slots, slot_idx, out, workspace, ws_bytes,
+                     stream);
 }
 
 // ---------------------------------------------------------------- standalone ops
@@ -543,7 +583,23 @@ m2_status m2_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* 
   if (!(eps > 0.f)) return fail(M2_EINVAL, "m2_rmsnorm_residual: eps must be positive");
   m2_status s = check_device();
   if (s) return s;
-  M2_CUDA(launch_rmsnorm_residual(h, add, w, eps, normed, T, n, static_cast<cudaStream_t>(stream)));
+  M2_CUDA(launch_rmsnorm_residual(h, add, w, eps, normed, nullptr, 1.f, T, n, static_cast<cudaStream_t>(stream)));
+  return M2_OK;
+}
+
+m2_status m2_rmsnorm_residual_quant(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps, float s_q,
+                                    uint16_t* normed, uint8_t* q, int T, int n, void* stream) {
+  g_err.clear();
+  if (T < 0 || n < 8 || n % 8)
+    return fail(M2_ESHAPE, "m2_rmsnorm_residual_quant: T %d, n %d (n must be a multiple of 8)", T, n);
+  if (T && (!h || !w || !q)) return fail(M2_EINVAL, "m2_rmsnorm_residual_quant: null pointer");
+  if ((uintptr_t)h % 16 || (uintptr_t)add % 16 || (uintptr_t)w % 16 || (uintptr_t)normed % 16 || (uintptr_t)q % 8)
+    return fail(M2_EINVAL, "m2_rmsnorm_residual_quant: h, add, w, normed must be 16-byte and q 8-byte aligned");
+  if (!(eps > 0.f)) return fail(M2_EINVAL, "m2_rmsnorm_residual_quant: eps must be positive");
+  if (!(s_q > 0.f) || !std::isfinite(s_q)) return fail(M2_EINVAL, "m2_rmsnorm_residual_quant: bad scale");
+  m2_status s = check_device();
+  if (s) return s;
+  M2_CUDA(launch_rmsnorm_residual(h, add, w, eps, normed, q, s_q, T, n, static_cast<cudaStream_t>(stream)));
   return M2_OK;
 }
 

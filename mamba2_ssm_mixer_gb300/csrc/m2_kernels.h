@@ -34,7 +34,7 @@ cudaError_t launch_conv_state_update(const uint16_t* zx, uint16_t* conv_state, c
 cudaError_t launch_gated_norm_quant(const uint16_t* y, const uint16_t* zx, const BlockParams& bp, int T,
                                     uint8_t* q2, uint16_t* o_tap, cudaStream_t st);
 cudaError_t launch_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps,
-                                    uint16_t* normed, int T, int n, cudaStream_t st);
+                                    uint16_t* normed, uint8_t* q, float s_q, int T, int n, cudaStream_t st);
 
 // ssd.cu
 // Per (chunk, head), for each token s of the chunk: the in-chunk cumulative
