@@ -574,6 +574,75 @@ def run_stack(args):
     print(json.dumps(line))
 
 
+def run_decode_bf16(args):
+    """Decode of 64 rows from a 256-slot pool whose SSM rows are a bf16 cache
+    (ssm_dtype = bf16: half the state bytes of the f32 pool), CUDA-graph
+    replay, L2 flushed before each step; prints one JSON line (not the
+    headline)."""
+    import torch
+
+    import mamba2_ssm_mixer_gb300 as m2
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    Wt = synth.make_weights(0)
+    w = dict(in_proj=torch.from_numpy(Wt["in_proj"]).to(dev), s_w1=Wt["s_w1"],
+             out_proj=torch.from_numpy(Wt["out_proj"]).to(dev), s_w2=Wt["s_w2"],
+             conv_w=torch.from_numpy(Wt["conv_w"]).to(torch.bfloat16).to(dev), conv_b=None,
+             A_log=torch.from_numpy(Wt["A_log"]).to(dev), D=torch.from_numpy(Wt["D"]).to(dev),
+             dt_bias=torch.from_numpy(Wt["dt_bias"]).to(dev),
+             norm_w=torch.from_numpy(Wt["norm_w"]).to(torch.bfloat16).to(dev),
+             s_x=Wt["s_x"], s_y=Wt["s_y"], eps=Wt["eps"])
+    res = {}
+    for name, dt_code, tdt in (("f32", m2.M2_DTYPE_F32, torch.float32), ("bf16", m2.M2_DTYPE_BF16, torch.bfloat16)):
+        blk = m2.Mamba2Mixer(w, device=dev, ssm_dtype=dt_code)
+        conv_pool = torch.from_numpy(synth.make_conv_state(2, N_SLOTS)).to(torch.bfloat16).to(dev)
+        ssm_pool = torch.from_numpy(synth.make_ssm_state(2, N_SLOTS)).to(tdt).to(dev)
+        slots = torch.from_numpy(synth.make_slot_idx(2, N_SLOTS, DEC_B)).to(dev)
+        h = torch.from_numpy(synth.make_hidden(2, DEC_B)).to(torch.bfloat16).to(dev)
+        out = torch.empty((DEC_B, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(blk.decode_workspace_size(DEC_B), dtype=torch.uint8, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        run = lambda: blk.decode(h, conv_pool, ssm_pool, slots, out=out, workspace=ws)
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            run()
+        torch.cuda.current_stream(dev).wait_stream(cs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            run()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(i & 0xFF)
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+        blk.profile(True)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            run()
+        torch.cuda.synchronize()
+        prof = blk.profile_read()
+        blk.profile(False)
+        blk.check()
+        row_state = 64 * 64 * 128 * (4 if name == "f32" else 2)
+        fused_ms = prof["decode_fused"][0] / args.steps
+        fused_bytes = DEC_B * (2 * row_state + 2 * CONV * 3 * 2 + Z * 2 + I)
+        res[name] = dict(step_ms=ms, tokens_per_s=DEC_B / (ms * 1e-3), decode_fused_ms=fused_ms,
+                         decode_fused_gbs=fused_bytes / (fused_ms * 1e-3) / 1e9,
+                         stages_ms={k: v[0] / args.steps for k, v in prof.items()})
+        blk.close()
+    print(json.dumps(dict(case="decode_bf16_state", workload=f"decode {DEC_B} rows from a {N_SLOTS}-slot pool, "
+                          "f32 vs bf16 SSM rows", launch="cuda_graph", results=res)))
+
+
 def run_case(args):
     """One kernel family at its bench-workload shape, for profiler captures
     (ncu -k <kernel> -c <n>): --case in_proj | out_proj | decode | prefill."""
@@ -608,7 +677,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill", "stack"], default=None,
+    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill", "stack", "decode_bf16"],
+                    default=None,
                     help="run one kernel family at the workload shape (for profiler captures); prints nothing")
     ap.add_argument("--measure-fp8-peak", action="store_true",
                     help="time cuBLAS e4m3 GEMMs and record the FP8 peak under profiles/")
@@ -622,6 +692,8 @@ def main():
         measure_fp8_peak()
     elif args.case == "stack":
         run_stack(args)
+    elif args.case == "decode_bf16":
+        run_decode_bf16(args)
     elif args.case:
         run_case(args)
     elif args.impl == "reference":

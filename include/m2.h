@@ -61,8 +61,12 @@ typedef struct m2_config {
   int d_state;      /* 128 */
   int conv_width;   /* 4 */
   int chunk_size;   /* SSD chunk length for prefill: 256 */
-  int ssm_dtype;    /* dtype of the recurrent state rows: must be M2_DTYPE_F32
-                       (PR #1288, "What it does": the ssm_dtype == f32 term) */
+  int ssm_dtype;    /* dtype of the recurrent state rows in the caller's pool
+                       and prefill state: M2_DTYPE_F32 (PR #1288, "What it
+                       does": the ssm_dtype == f32 term) or M2_DTYPE_BF16, a
+                       bf16 state cache: rows are widened to f32 when read,
+                       updated and reduced to y in f32, and rounded to bf16
+                       (nearest even) when written back */
   float eps;        /* gated RMSNorm epsilon (1e-5) */
   float s_x;        /* static input_scale of in_proj's activation (> 0) */
   float s_y;        /* static input_scale of out_proj's activation (> 0) */
@@ -189,14 +193,15 @@ m2_status m2_prefill_workspace_size(const m2_handle* h, const int32_t* seqlens_h
  *   conv_state   bf16 [nseq, 6144, 3] device, in/out: read for sequences with
  *                has_initial, always overwritten with the last 3 raw xBC
  *                inputs ([channel][tap], tap 0 oldest)
- *   ssm_state    f32 [nseq, 64, 64, 128] device, in/out likewise
+ *   ssm_state    [nseq, 64, 64, 128] device, f32 or bf16 (the handle's
+ *                ssm_dtype), in/out likewise
  *   out          bf16 [sum(T), 2688] device
  *   workspace    device, >= m2_prefill_workspace_size bytes, 256-byte aligned
  * Errors: M2_EINVAL, M2_ESHAPE (nseq > 256 or a length < 1), M2_ENOMEM
  * (workspace too small), M2_ECUDA.
  */
 m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlens_host, int nseq,
-                     const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state,
+                     const uint8_t* has_initial, uint16_t* conv_state, void* ssm_state,
                      uint16_t* out, void* workspace, size_t ws_bytes, void* stream);
 
 /*
@@ -206,7 +211,7 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
  * input quant is skipped; everything else is m2_prefill.
  */
 m2_status m2_prefill_q(m2_handle* h, const uint8_t* hidden_q, const int32_t* seqlens_host, int nseq,
-                       const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state,
+                       const uint8_t* has_initial, uint16_t* conv_state, void* ssm_state,
                        uint16_t* out, void* workspace, size_t ws_bytes, void* stream);
 
 /* Workspace bytes m2_decode needs for a batch of Bt rows. */
@@ -221,18 +226,18 @@ m2_status m2_decode_workspace_size(const m2_handle* h, int Bt, size_t* bytes);
  * output zeroed, and m2_check() reports M2_EINVAL.
  *   hidden     bf16 [Bt, 2688] device
  *   conv_pool  bf16 [n_slots, 6144, 3] device
- *   ssm_pool   f32  [n_slots, 64, 64, 128] device
+ *   ssm_pool   [n_slots, 64, 64, 128] device, f32 or bf16 (ssm_dtype)
  *   slot_idx   int32 [Bt] device
  *   out        bf16 [Bt, 2688] device
  * Errors: M2_EINVAL, M2_ESHAPE (Bt < 1 or Bt > 4096), M2_ENOMEM, M2_ECUDA.
  */
-m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, float* ssm_pool,
+m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, void* ssm_pool,
                     int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
                     void* stream);
 
 /* m2_decode with the input already quantised (hidden_q e4m3 [Bt, 2688], as in
  * m2_prefill_q). */
-m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* conv_pool, float* ssm_pool,
+m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* conv_pool, void* ssm_pool,
                       int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
                       void* stream);
 

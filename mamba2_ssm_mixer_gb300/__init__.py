@@ -172,6 +172,8 @@ class Mamba2Mixer:
         self._h = h
         self._taps = None
         self.s_x = float(weights["s_x"])   # the input quant scale (for pre-quantised inputs)
+        # dtype of the SSM state rows this block reads and writes
+        self.state_dtype = torch.bfloat16 if ssm_dtype == M2_DTYPE_BF16 else torch.float32
 
     def close(self):
         if getattr(self, "_h", None):
@@ -236,7 +238,7 @@ class Mamba2Mixer:
         quantised = hidden.dtype == torch.uint8
         _need(hidden, "hidden", torch.uint8 if quantised else torch.bfloat16, (T, HIDDEN))
         _need(conv_state, "conv_state", torch.bfloat16, (len(seqlens), CONV_DIM, CONV_WIDTH - 1))
-        _need(ssm_state, "ssm_state", torch.float32, (len(seqlens), NHEADS, HEADDIM, D_STATE))
+        _need(ssm_state, "ssm_state", self.state_dtype, (len(seqlens), NHEADS, HEADDIM, D_STATE))
         if out is None:
             out = torch.empty((T, HIDDEN), dtype=torch.bfloat16, device=hidden.device)
         _need(out, "out", torch.bfloat16, (T, HIDDEN))
@@ -257,7 +259,7 @@ class Mamba2Mixer:
         _need(hidden, "hidden", torch.uint8 if quantised else torch.bfloat16, (Bt, HIDDEN))
         n_slots = conv_pool.shape[0]
         _need(conv_pool, "conv_pool", torch.bfloat16, (n_slots, CONV_DIM, CONV_WIDTH - 1))
-        _need(ssm_pool, "ssm_pool", torch.float32, (n_slots, NHEADS, HEADDIM, D_STATE))
+        _need(ssm_pool, "ssm_pool", self.state_dtype, (n_slots, NHEADS, HEADDIM, D_STATE))
         _need(slot_idx, "slot_idx", torch.int32, (Bt,))
         if out is None:
             out = torch.empty((Bt, HIDDEN), dtype=torch.bfloat16, device=hidden.device)

@@ -5,15 +5,19 @@
 //
 //  - persistent CTAs (two per SM, so one streams while the other is in its
 //    conv or norm phase) walk the (row, group) work items;
-//  - a producer thread streams every head's f32 state (64 x 128 = 32 KB,
-//    contiguous in the pool) into a shared-memory ring with cp.async.bulk
-//    (TMA, 1-D) several heads ahead, so loads are always in flight;
+//  - a producer thread streams every head's state (64 x 128, contiguous in the
+//    pool: 32 KB in f32, 16 KB in bf16) into a shared-memory ring with
+//    cp.async.bulk (TMA, 1-D) several heads ahead, so loads are always in
+//    flight;
 //  - 8 consumer warps update the state in shared memory, reduce y, and one
 //    thread writes the updated 32 KB back with a bulk store;
 //  - conv, gate and norm for an item run on the consumer warps while the ring
 //    keeps streaming.
 // The pool rows are advanced in place through slot_idx: the gather and
-// scatter of vllm.cpp PR #1288 ("What it does") are addressing.  Every wait is
+// scatter of vllm.cpp PR #1288 ("What it does") are addressing.  A bf16 pool
+// (the non-f32 state cache of the same section's ssm_dtype term) is widened
+// to f32 as it is read, updated and reduced to y in f32, and rounded to bf16
+// (nearest even) as it is written back.  Every wait is
 // bounded; a wait that runs out sets the device error word and the CTA stops
 // issuing work, drains its copies and returns.
 #include "m2_kernels.h"
@@ -26,8 +30,7 @@ using namespace tc;
 
 namespace {
 
-constexpr int kStages = 3;                  // 3 x 32 KB ring per CTA, 2 CTAs per SM
-constexpr int kHeadBytes = kP * kN * 4;     // 32768
+constexpr int kRingBytes = 3 * kP * kN * 4;   // 96 KB ring per CTA, 2 CTAs per SM
 constexpr int kConsumers = 256;             // 8 warps
 constexpr int kThreadsT = kConsumers + 32;  // + producer warp
 
@@ -47,8 +50,22 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
 
+// Pool element types: 4 consecutive d_state entries as f32.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float4 ld4(const uint16_t* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                     __uint_as_float(w.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ void st4(uint16_t* p, float4 v) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+template <typename S>
 struct __align__(16) Smem {
-  float state[kStages][kP * kN];   // 96 KB ring
+  static constexpr int kStages = kRingBytes / (kP * kN * (int)sizeof(S));   // 3 (f32) or 6 (bf16)
+  S state[kStages][kP * kN];       // 96 KB ring
   float ux[kGroupCh];
   float4 ub[kN / 4];
   float4 uc[kN / 4];
@@ -61,15 +78,18 @@ struct __align__(16) Smem {
 
 }  // namespace
 
+template <typename S>
 __global__ void __launch_bounds__(kThreadsT, 2)
     k_decode_stream(const uint16_t* __restrict__ zx, const uint16_t* __restrict__ conv_w,
                     const uint16_t* __restrict__ conv_b, const float* __restrict__ A_log, const float* __restrict__ Dp,
                     const float* __restrict__ dt_bias, const uint16_t* __restrict__ norm_w, float eps, float s_y,
-                    uint16_t* __restrict__ conv_pool, float* __restrict__ ssm_pool, int n_slots,
+                    uint16_t* __restrict__ conv_pool, S* __restrict__ ssm_pool, int n_slots,
                     const int32_t* __restrict__ slot_idx, int Bt, uint8_t* __restrict__ q2, int* __restrict__ err,
                     DecodeTaps taps) {
+  constexpr int kStages = Smem<S>::kStages;
+  constexpr uint32_t kHeadBytes = kP * kN * sizeof(S);
   extern __shared__ uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_align<128>(smem_raw));
+  Smem<S>& sm = *reinterpret_cast<Smem<S>*>(smem_align<128>(smem_raw));
   volatile int* abort = &sm.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = Bt * kG;
@@ -99,7 +119,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         const int b = it / kG, g = it % kG;
         const int slot = slot_idx[b];
         if (slot < 0 || slot >= n_slots) continue;
-        const float* src = ssm_pool + ((size_t)slot * kNH + g * kHPG) * (kP * kN);
+        const S* src = ssm_pool + ((size_t)slot * kNH + g * kHPG) * (kP * kN);
         for (int hh = 0; hh < kHPG; ++hh) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
             *abort = 1;
@@ -174,7 +194,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     consumers_sync();
     const float4 bv = sm.ub[lane];
     const float4 cv = sm.uc[lane];
-    float* dst_base = ssm_pool + ((size_t)slot * kNH + g * kHPG) * (kP * kN);
+    S* dst_base = ssm_pool + ((size_t)slot * kNH + g * kHPG) * (kP * kN);
     for (int hh = 0; hh < kHPG; ++hh) {
       const int h = g * kHPG + hh;
       const bool ok = mbar_wait(&sm.full[stage], phase, abort);
@@ -182,19 +202,19 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         if (tid == 0) atomicOr(err, kErrTimeout);
         *abort = 1;
       }
-      float4* S = reinterpret_cast<float4*>(sm.state[stage]);
+      S* St = sm.state[stage];
       const float dt = sm.dts[hh], dA = sm.dAs[hh];
       float part[kP / 8];
 #pragma unroll
       for (int i = 0; i < kP / 8; ++i) {
         const int p = warp + 8 * i;
-        float4 s = S[p * (kN / 4) + lane];
+        float4 s = ld4(St + p * kN + 4 * lane);
         const float xd = dt * sm.ux[hh * kP + p];
         s.x = fmaf(dA, s.x, xd * bv.x);
         s.y = fmaf(dA, s.y, xd * bv.y);
         s.z = fmaf(dA, s.z, xd * bv.z);
         s.w = fmaf(dA, s.w, xd * bv.w);
-        S[p * (kN / 4) + lane] = s;
+        st4(St + p * kN + 4 * lane, s);   // f32, or rounded to bf16 for a bf16 pool
         part[i] = s.x * cv.x + s.y * cv.y + s.z * cv.z + s.w * cv.w;
       }
 #pragma unroll
@@ -257,17 +277,28 @@ __global__ void __launch_bounds__(kThreadsT, 2)
   }
 }
 
-cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,
-                                 int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
-                                 const DecodeTaps& taps, cudaStream_t st) {
-  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k_decode_stream), (int)(sizeof(Smem) + 128));
+template <typename S>
+static cudaError_t launch_decode_t(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, S* ssm_pool,
+                                   int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
+                                   const DecodeTaps& taps, cudaStream_t st) {
+  auto k = k_decode_stream<S>;
+  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k), (int)(sizeof(Smem<S>) + 128));
   if (e != cudaSuccess) return e;
   const int sms = device_sm_count();
   const int items = Bt * kG;
   const int grid = items < 2 * sms ? items : 2 * sms;
-  return launch_pdl(k_decode_stream, dim3(grid), dim3(kThreadsT), sizeof(Smem) + 128, st, zx, bp.conv_w, bp.conv_b,
-                    bp.A_log, bp.D, bp.dt_bias, bp.norm_w, bp.eps, bp.s_y, conv_pool, ssm_pool, n_slots, slot_idx, Bt,
-                    q2, err, taps);
+  return launch_pdl(k, dim3(grid), dim3(kThreadsT), sizeof(Smem<S>) + 128, st, zx, bp.conv_w, bp.conv_b, bp.A_log,
+                    bp.D, bp.dt_bias, bp.norm_w, bp.eps, bp.s_y, conv_pool, ssm_pool, n_slots, slot_idx, Bt, q2, err,
+                    taps);
+}
+
+cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, void* ssm_pool,
+                                 bool bf16_state, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
+                                 const DecodeTaps& taps, cudaStream_t st) {
+  if (bf16_state)
+    return launch_decode_t(zx, bp, conv_pool, static_cast<uint16_t*>(ssm_pool), n_slots, slot_idx, Bt, q2, err,
+                           taps, st);
+  return launch_decode_t(zx, bp, conv_pool, static_cast<float*>(ssm_pool), n_slots, slot_idx, Bt, q2, err, taps, st);
 }
 
 }  // namespace m2

@@ -153,8 +153,8 @@ m2_status m2_create(const m2_config* cfg, const m2_weights* w, m2_handle** out) 
                 cfg->hidden, cfg->d_inner, cfg->nheads, cfg->headdim, cfg->n_groups, cfg->d_state,
                 cfg->conv_width);
   if (cfg->chunk_size != kChunk) return fail(M2_ESHAPE, "m2_create: chunk_size %d is not 256", cfg->chunk_size);
-  if (cfg->ssm_dtype != M2_DTYPE_F32)
-    return fail(M2_EINVAL, "m2_create: ssm_dtype must be f32 (the recurrent rows are f32 working state)");
+  if (cfg->ssm_dtype != M2_DTYPE_F32 && cfg->ssm_dtype != M2_DTYPE_BF16)
+    return fail(M2_EINVAL, "m2_create: ssm_dtype must be M2_DTYPE_F32 or M2_DTYPE_BF16");
   if (!(cfg->eps > 0.f) || !(cfg->s_x > 0.f) || !(cfg->s_y > 0.f) || !(cfg->s_x < 3.0e38f) ||
       !(cfg->s_y < 3.0e38f))
     return fail(M2_EINVAL, "m2_create: eps and activation scales must be positive and finite");
@@ -355,7 +355,7 @@ static m2_status copy_tap(void* dst, const void* src, size_t bytes, cudaStream_t
 // already quantised with the handle's s_x (exactly one of the two given).
 static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_t* hidden_q,
                               const int32_t* seqlens_host, int nseq, const uint8_t* has_initial,
-                              uint16_t* conv_state, float* ssm_state, uint16_t* out, void* workspace,
+                              uint16_t* conv_state, void* ssm_state, uint16_t* out, void* workspace,
                               size_t ws_bytes, void* stream) {
   g_err.clear();
   if (!h || (!hidden && !hidden_q) || !conv_state || !ssm_state || !out || !workspace)
@@ -386,7 +386,8 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
            launch_ssd_chunk_state_tc(w.u, w.cumdt, local, w.states, h->err, st));
   M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
-           launch_ssd_state_pass(w.states, w.cumdt, local, w.sin_img, ssm_state, st));
+           launch_ssd_state_pass(w.states, w.cumdt, local, w.sin_img, ssm_state, h->cfg.ssm_dtype == M2_DTYPE_BF16,
+                                 st));
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
            launch_ssd_chunk_scan_tc(w.u, w.cumdt, w.sin_img, bp, local, w.y, h->err, st));
   M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
@@ -406,7 +407,7 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
 }
 
 m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlens_host, int nseq,
-                     const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state, uint16_t* out,
+                     const uint8_t* has_initial, uint16_t* conv_state, void* ssm_state, uint16_t* out,
                      void* workspace, size_t ws_bytes, void* stream) {
   if (!hidden) return fail(M2_EINVAL, "m2_prefill: null argument");
   return prefill_impl(h, hidden, nullptr, seqlens_host, nseq, has_initial, conv_state, ssm_state, out, workspace,
@@ -414,7 +415,7 @@ m2_status m2_prefill(m2_handle* h, const uint16_t* hidden, const int32_t* seqlen
 }
 
 m2_status m2_prefill_q(m2_handle* h, const uint8_t* hidden_q, const int32_t* seqlens_host, int nseq,
-                       const uint8_t* has_initial, uint16_t* conv_state, float* ssm_state, uint16_t* out,
+                       const uint8_t* has_initial, uint16_t* conv_state, void* ssm_state, uint16_t* out,
                        void* workspace, size_t ws_bytes, void* stream) {
   if (!hidden_q) return fail(M2_EINVAL, "m2_prefill_q: null argument");
   return prefill_impl(h, nullptr, hidden_q, seqlens_host, nseq, has_initial, conv_state, ssm_state, out, workspace,
@@ -453,7 +454,7 @@ m2_status m2_decode_workspace_size(const m2_handle* h, int Bt, size_t* bytes) {
 }
 
 static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t* hidden_q, int Bt,
-                             uint16_t* conv_pool, float* ssm_pool, int n_slots, const int32_t* slot_idx,
+                             uint16_t* conv_pool, void* ssm_pool, int n_slots, const int32_t* slot_idx,
                              uint16_t* out, void* workspace, size_t ws_bytes, void* stream) {
   g_err.clear();
   if (!h || (!hidden && !hidden_q) || !conv_pool || !ssm_pool || !slot_idx || !out || !workspace)
@@ -481,7 +482,8 @@ static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t
     M2_STAGE(h, st, M2_STAGE_DEC_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)Bt * kH, h->cfg.s_x, w.q, st));
   M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl, gemm_fp8(q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
-           launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, n_slots, slot_idx, Bt, w.q2, h->err, dt, st));
+           launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, h->cfg.ssm_dtype == M2_DTYPE_BF16, n_slots, slot_idx,
+                                Bt, w.q2, h->err, dt, st));
   M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   if (h->taps_on) {
     m2_status s;
@@ -495,7 +497,7 @@ static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t
   return M2_OK;
 }
 
-m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, float* ssm_pool,
+m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, void* ssm_pool,
                     int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
                     void* stream) {
   if (!hidden) return fail(M2_EINVAL, "m2_decode: null argument");
@@ -503,7 +505,7 @@ m2_status m2_decode(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv
                      stream);
 }
 
-m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* conv_pool, float* ssm_pool,
+m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* conv_pool, void* ssm_pool,
                       int n_slots, const int32_t* slot_idx, uint16_t* out, void* workspace, size_t ws_bytes,
                       void* stream) {
   if (!hidden_q) return fail(M2_EINVAL, "m2_decode_q: null argument");

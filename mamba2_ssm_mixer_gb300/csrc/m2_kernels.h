@@ -57,7 +57,7 @@ cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const S
 // Reads the chunk states, writes the state entering each chunk as S_in images
 // and the final state of each sequence to ssm_state.
 cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const SeqInfo& si, uint8_t* sin_img,
-                                  float* ssm_state, cudaStream_t st);
+                                  void* ssm_state, bool bf16_state, cudaStream_t st);
 
 // ssd_tc.cu (tensor-core chunk states and chunk scan)
 // Chunk states f32 [chunk][head][64][128].
@@ -68,8 +68,10 @@ cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const CumDt* cumdt, cons
                                      cudaStream_t st);
 
 // decode_tma.cu (persistent, TMA-streamed state)
-cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, float* ssm_pool,
-                                 int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
+// ssm_pool: f32 rows, or bf16 rows when bf16_state (widened to f32 when read,
+// rounded to bf16 when written back).
+cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, void* ssm_pool,
+                                 bool bf16_state, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
                                  const DecodeTaps& taps, cudaStream_t st);
 
 }  // namespace m2

@@ -107,10 +107,24 @@ __device__ __forceinline__ uint32_t sin_offset(int p, int n) {
                     (n & 7) * 2);
 }
 
+// The initial / final state rows: f32, or bf16 (widened when read, rounded
+// to nearest even when written).
+__device__ __forceinline__ float4 ld_state4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st_state4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float4 ld_state4(const uint16_t* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), __uint_as_float(w.y << 16),
+                     __uint_as_float(w.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ void st_state4(uint16_t* p, float4 v) {
+  *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+}
+
+template <typename SS>
 __global__ void __launch_bounds__(256) k_ssd_state_pass(const float* __restrict__ states,
                                                         const CumDt* __restrict__ cumdt, const SeqInfo si,
                                                         uint8_t* __restrict__ sin_img,
-                                                        float* __restrict__ ssm_state) {
+                                                        SS* __restrict__ ssm_state) {
   pdl_wait();
   pdl_trigger();
   const int s = blockIdx.x, h = blockIdx.y;
@@ -118,8 +132,8 @@ __global__ void __launch_bounds__(256) k_ssd_state_pass(const float* __restrict_
   const int p = (e4 * 4) / kN, n = (e4 * 4) % kN;
   const uint32_t off = sin_offset(p, n);
   const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
-  float4* fin = reinterpret_cast<float4*>(ssm_state + ((size_t)s * kNH + h) * (kP * kN)) + e4;
-  float4 run = init ? *fin : make_float4(0.f, 0.f, 0.f, 0.f);
+  SS* fin = ssm_state + ((size_t)s * kNH + h) * (kP * kN) + 4 * (size_t)e4;
+  float4 run = init ? ld_state4(fin) : make_float4(0.f, 0.f, 0.f, 0.f);
   const int c0 = si.cu_chunks[s], c1 = si.cu_chunks[s + 1];
   const int tbeg = si.cu_seqlens[s], tend = si.cu_seqlens[s + 1];
   for (int cb = c0; cb < c1; cb += 8) {
@@ -159,7 +173,7 @@ __global__ void __launch_bounds__(256) k_ssd_state_pass(const float* __restrict_
       }
     }
   }
-  *fin = run;
+  st_state4(fin, run);
 }
 
 cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, CumDt* cumdt,
@@ -169,9 +183,13 @@ cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const S
 }
 
 cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const SeqInfo& si, uint8_t* sin_img,
-                                  float* ssm_state, cudaStream_t st) {
-  return launch_pdl(k_ssd_state_pass, dim3(si.nseq, kNH, (kP * kN) / 4 / 256), dim3(256), 0, st, states, cumdt, si,
-                    sin_img, ssm_state);
+                                  void* ssm_state, bool bf16_state, cudaStream_t st) {
+  const dim3 grid(si.nseq, kNH, (kP * kN) / 4 / 256);
+  if (bf16_state)
+    return launch_pdl(k_ssd_state_pass<uint16_t>, grid, dim3(256), 0, st, states, cumdt, si, sin_img,
+                      static_cast<uint16_t*>(ssm_state));
+  return launch_pdl(k_ssd_state_pass<float>, grid, dim3(256), 0, st, states, cumdt, si, sin_img,
+                    static_cast<float*>(ssm_state));
 }
 
 }  // namespace m2

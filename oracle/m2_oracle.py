@@ -311,18 +311,31 @@ def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False, map_fn=
     return res
 
 
-def block_prefill(Wt, hidden, seqlens, conv_state=None, ssm_state=None, keep=False, map_fn=None):
-    """Prefill of packed sequences; missing states mean fresh sequences."""
+def _store_state(s, state_cache):
+    """The state as the caller's cache holds it: f32 rows are returned in full
+    precision (the tests compare against the exact value), bf16 rows rounded
+    to nearest even (a non-f32 mamba_ssm_cache_dtype, PR #1288 "What it does",
+    the ssm_dtype term: the recurrence itself runs in full precision, only
+    the stored rows are narrowed)."""
+    return bf16_round(s) if state_cache == "bf16" else s
+
+
+def block_prefill(Wt, hidden, seqlens, conv_state=None, ssm_state=None, keep=False, map_fn=None,
+                  state_cache="f32"):
+    """Prefill of packed sequences; missing states mean fresh sequences.
+    state_cache: "f32" or "bf16" (the final ssm states are rounded to bf16)."""
     H, I, nh, P, G, N, W = _dims(Wt)
     nseq = len(seqlens)
     if conv_state is None:
         conv_state = np.zeros((nseq, I + 2 * G * N, W - 1))
     if ssm_state is None:
         ssm_state = np.zeros((nseq, nh, P, N))
-    return block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=keep, map_fn=map_fn)
+    res = block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=keep, map_fn=map_fn)
+    res["ssm_state"] = _store_state(res["ssm_state"], state_cache)
+    return res
 
 
-def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False):
+def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False, state_cache="f32"):
     """One decode token per row, states gathered from a slot pool.
 
     Row b reads pool[slot_idx[b]] (decode rows always have prior state,
@@ -332,7 +345,9 @@ def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False):
     padding row: output zero, no state read or written.
     Returns dict(out [Bt, H], live (row numbers with a slot), conv_rows,
     ssm_rows (the new pool contents at slot_idx[live])).  Inputs are not
-    modified.
+    modified.  state_cache "bf16": the pool rows are bf16 values, widened
+    exactly when read; y uses the advanced state in full precision, and the
+    rows written back are rounded to bf16.
     """
     slot_idx = np.asarray(slot_idx)
     live = np.nonzero(slot_idx >= 0)[0]
@@ -346,7 +361,7 @@ def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False):
                          np.asarray(ssm_pool[rows], np.float64), keep=keep)
         out[live] = r["out"]
         res["conv_rows"] = r["conv_state"]
-        res["ssm_rows"] = r["ssm_state"]
+        res["ssm_rows"] = _store_state(r["ssm_state"], state_cache)
         if keep:
             res.update({k: r[k] for k in ("q", "zx", "u", "dt", "y", "o", "q2")})
     return res

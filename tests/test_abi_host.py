@@ -67,11 +67,13 @@ def test_create_refuses_other_geometry(m2, field, value):
     assert "geometry" in m2.last_error()
 
 
-def test_create_refuses_non_f32_ssm_state(m2):
-    """The paged arm needs f32 recurrent rows (the ssm_dtype == f32 term)."""
+@pytest.mark.parametrize("dtype", [2, 7, -1])
+def test_create_refuses_unknown_ssm_dtype(m2, dtype):
+    """State rows are f32 (the ssm_dtype == f32 term) or a bf16 cache; any
+    other code is refused on the host before any device work."""
     w, _keep = _weights(m2)
     h = ctypes.c_void_p()
-    st = m2._lib.m2_create(ctypes.byref(_cfg(m2, ssm_dtype=m2.M2_DTYPE_BF16)), ctypes.byref(w), ctypes.byref(h))
+    st = m2._lib.m2_create(ctypes.byref(_cfg(m2, ssm_dtype=dtype)), ctypes.byref(w), ctypes.byref(h))
     assert st == m2.M2_EINVAL and "ssm_dtype" in m2.last_error()
 
 

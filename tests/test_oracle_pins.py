@@ -527,3 +527,57 @@ def test_ssd_by_group_equals_sequential():
     y1, S1 = oracle.ssd_sequential(*args)
     y2, S2 = oracle.ssd_by_group(*args)
     assert np.array_equal(y1, y2) and np.array_equal(S1, S2)
+
+
+# ---------------------------------------------------------------- bf16 state cache
+
+def test_bf16_state_cache_changes_only_the_stored_rows(tiny_weights):
+    """A bf16 state cache holds bf16 values: reading them widens exactly, so
+    with a bf16-valued pool the output is the f32-cache output bit for bit and
+    the stored rows are those rows rounded to nearest even (torch's cast)."""
+    Wt = tiny_weights
+    rng = np.random.default_rng(96)
+    g = Wt["geo"]
+    nslots, Bt = 5, 3
+    conv = synth.as_bf16_values(rng.standard_normal((nslots, g.conv_dim, g.conv_width - 1)))
+    ssm = synth.as_bf16_values(rng.standard_normal((nslots, g.nheads, g.headdim, g.d_state)) * 0.1)
+    h = synth.make_hidden(96, Bt, g)
+    slots = np.array([4, 0, 2])
+    a = oracle.block_decode(Wt, h, conv, ssm, slots)
+    b = oracle.block_decode(Wt, h, conv, ssm, slots, state_cache="bf16")
+    np.testing.assert_array_equal(a["out"], b["out"])
+    ref = torch.from_numpy(a["ssm_rows"]).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    # the f64 rows pass through f32 in torch; an f64 -> bf16 rounding and an
+    # f64 -> f32 -> bf16 rounding agree except at double-rounding ties
+    assert np.mean(b["ssm_rows"] != ref) < 1e-4
+    assert np.array_equal(b["ssm_rows"], synth.as_bf16_values(b["ssm_rows"]))
+
+
+def test_bf16_state_cache_rounds_after_every_step(tiny_weights):
+    """Two decode steps through a bf16 cache = step, round, step, round; the
+    rounding is not deferred to the end (rows carried in full precision
+    differ)."""
+    Wt = tiny_weights
+    g = Wt["geo"]
+    rng = np.random.default_rng(97)
+    conv = synth.as_bf16_values(rng.standard_normal((1, g.conv_dim, g.conv_width - 1)))
+    ssm = synth.as_bf16_values(rng.standard_normal((1, g.nheads, g.headdim, g.d_state)) * 0.1)
+    h = synth.make_hidden(97, 2, g)
+    s = np.array([0])
+    r1 = oracle.block_decode(Wt, h[:1], conv, ssm, s, state_cache="bf16")
+    r2 = oracle.block_decode(Wt, h[1:], r1["conv_rows"], r1["ssm_rows"], s, state_cache="bf16")
+    f1 = oracle.block_decode(Wt, h[:1], conv, ssm, s)
+    f2 = oracle.block_decode(Wt, h[1:], f1["conv_rows"], f1["ssm_rows"], s)
+    np.testing.assert_array_equal(r1["ssm_rows"], oracle.bf16_round(f1["ssm_rows"]))
+    assert not np.array_equal(r2["ssm_rows"], oracle.bf16_round(f2["ssm_rows"]))
+    rel = np.linalg.norm(r2["ssm_rows"] - f2["ssm_rows"]) / np.linalg.norm(f2["ssm_rows"])
+    assert 1e-5 < rel < 1e-2                       # bf16-level, not a different state
+
+
+def test_bf16_state_cache_prefill_final_state(tiny_weights):
+    Wt = tiny_weights
+    h = synth.make_hidden(98, 9, Wt["geo"])
+    a = oracle.block_prefill(Wt, h, [9])
+    b = oracle.block_prefill(Wt, h, [9], state_cache="bf16")
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(b["ssm_state"], oracle.bf16_round(a["ssm_state"]))
