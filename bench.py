@@ -3,7 +3,9 @@
 
 One step = one paged decode of 64 rows from a 256-slot state pool plus one
 prefill of 4 x 2048 tokens (chunk 256, zero initial state), i.e. every stage
-of the block's hot path.  Inputs are synthetic (seeded), resident in HBM; L2
+of the block's hot path, issued as one m2_mixed call over the ordered batch
+(decode rows first; the two-call form m2_decode + m2_prefill is timed too and
+reported in the line's config).  Inputs are synthetic (seeded), resident in HBM; L2
 is flushed (256 MiB write) before every timed step and the flush is outside
 the per-step CUDA-event interval.  Prints ONE JSON line on rank 0.
 
@@ -50,10 +52,11 @@ def stage_work():
     kind 'flop' counts 2 per multiply-add; 'byte' counts each operand read or
     written once (intermediates counted where a stage must move them)."""
     T, B = T_PF, DEC_B
+    R = T + B                          # rows of the mixed call's quant and projections
     state = 64 * 64 * 128 * 4          # one f32 SSM state row (all heads): 2 MiB
     return {
-        "quant_in": ("byte", T * H * 3),
-        "in_proj": ("flop", 2.0 * T * Z * H),
+        "quant_in": ("byte", R * H * 3),
+        "in_proj": ("flop", 2.0 * R * Z * H),
         "conv": ("byte", T * CONV * 2 * 2),
         "conv_state": ("byte", 4 * CONV * 3 * 2),
         "ssd_cumsum": ("byte", T * 64 * (2 + 8)),
@@ -62,7 +65,7 @@ def stage_work():
         # causal C.B per group, (C.B o decay) x per head, C S_in per head
         "ssd_chunk_scan": ("flop", T * (8 * 257 * 128 + 64 * 257 * 64 + 64 * 2 * 64 * 128)),
         "norm_quant": ("byte", T * I * 5),
-        "out_proj": ("flop", 2.0 * T * H * I),
+        "out_proj": ("flop", 2.0 * R * H * I),
         "decode_fused": ("byte", B * (2 * state + 2 * CONV * 3 * 2 + Z * 2 + I)),
         "dec_quant_in": ("byte", B * H * 3),
         "dec_in_proj": ("byte", Z * H + B * H + B * Z * 2),
@@ -252,6 +255,9 @@ def build_workload(dev):
     ssm_st = torch.zeros((len(SEQLENS), 64, 64, 128), dtype=torch.float32, device=dev)
     ws_dec = torch.empty(blk.decode_workspace_size(DEC_B), dtype=torch.uint8, device=dev)
     ws_pf = torch.empty(blk.prefill_workspace_size(SEQLENS), dtype=torch.uint8, device=dev)
+    ws_mix = torch.empty(blk.mixed_workspace_size(DEC_B, SEQLENS), dtype=torch.uint8, device=dev)
+    h_mix = torch.cat([h_dec, h_pf])              # the ordered batch: decode rows, then prefill tokens
+    out_mix = torch.empty((DEC_B + T_PF, H), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -263,12 +269,17 @@ def build_workload(dev):
     def prefill():
         blk.prefill(h_pf, SEQLENS, conv_st, ssm_st, out=out_pf, workspace=ws_pf)
 
-    def step():
+    def step_separate():
         decode()
         prefill()
 
-    return dict(blk=blk, step=step, decode=decode, prefill=prefill, flush=flush, stream=stream, h_dec=h_dec,
-                h_pf=h_pf, out_dec=out_dec, out_pf=out_pf, h_dec_np=h_dec_np, h_pf_np=h_pf_np)
+    # the step as a serving loop issues it: one call over the whole batch
+    def step():
+        blk.mixed(h_mix, DEC_B, conv_pool, ssm_pool, slots, SEQLENS, conv_st, ssm_st, out=out_mix, workspace=ws_mix)
+
+    return dict(blk=blk, step=step, step_separate=step_separate, decode=decode, prefill=prefill, flush=flush,
+                stream=stream, h_dec=h_dec, h_pf=h_pf, out_dec=out_dec, out_pf=out_pf, h_dec_np=h_dec_np,
+                h_pf_np=h_pf_np, h_mix=h_mix, out_mix=out_mix)
 
 
 def run_ours(args, rank, world, local_rank):
@@ -344,6 +355,25 @@ def run_ours(args, rank, world, local_rank):
         dist.barrier()
     clocks = sampler.stop()
     blk.check()
+    # the same step as two calls (m2_decode + m2_prefill), for comparison
+    ms_separate = None
+    try:
+        step_sep = ctx["step_separate"]
+        cs2 = torch.cuda.Stream(dev)
+        cs2.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs2):
+            step_sep()
+        torch.cuda.current_stream(dev).wait_stream(cs2)
+        torch.cuda.synchronize()
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=cs2):
+            step_sep()
+        for _ in range(args.warmup):
+            g2.replay()
+        torch.cuda.synchronize()
+        ms_separate = timed(g2.replay, args.steps)
+    except Exception:  # pragma: no cover
+        ms_separate = None
     # per-stage times (events between kernels; a separate pass so the
     # brackets do not perturb the headline numbers)
     timed(step, args.steps, profile=True)
@@ -355,25 +385,22 @@ def run_ours(args, rank, world, local_rank):
     ms = max_over_ranks(ms, dist, dev)
 
     # ---- end to end: host buffers, copies inside the timed interval
-    hd_pin = torch.from_numpy(h_dec_np).to(torch.bfloat16).pin_memory()
-    hp_pin = torch.from_numpy(h_pf_np).to(torch.bfloat16).pin_memory()
-    od_pin = torch.empty((DEC_B, H), dtype=torch.bfloat16).pin_memory()
-    op_pin = torch.empty((T_PF, H), dtype=torch.bfloat16).pin_memory()
+    h_mix, out_mix = ctx["h_mix"], ctx["out_mix"]
+    hm_pin = torch.from_numpy(np.concatenate([h_dec_np, h_pf_np])).to(torch.bfloat16).pin_memory()
+    om_pin = torch.empty((DEC_B + T_PF, H), dtype=torch.bfloat16).pin_memory()
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         e2e_ev[i][0].record()
-        h_dec.copy_(hd_pin, non_blocking=True)
-        h_pf.copy_(hp_pin, non_blocking=True)
+        h_mix.copy_(hm_pin, non_blocking=True)
         step()
-        od_pin.copy_(out_dec, non_blocking=True)
-        op_pin.copy_(out_pf, non_blocking=True)
+        om_pin.copy_(out_mix, non_blocking=True)
         e2e_ev[i][1].record()
     torch.cuda.synchronize()
     e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
     e2e_ms = max_over_ranks(e2e_ms, dist, dev)
-    h2d = hd_pin.numel() * 2 + hp_pin.numel() * 2
-    d2h = od_pin.numel() * 2 + op_pin.numel() * 2
+    h2d = hm_pin.numel() * 2
+    d2h = om_pin.numel() * 2
 
     if rank != 0:
         if dist:
@@ -423,6 +450,9 @@ def run_ours(args, rank, world, local_rank):
                             parallelism="replicas" if world > 1 else "single GPU",
                             launch="cuda_graph" if ms_graph is not None else "eager",
                             ms_per_step_eager=ms_eager, ms_per_step_graph=ms_graph,
+                            step="one m2_mixed call over the ordered batch (64 decode rows, then 4 x 2048 "
+                                 "prefill tokens)",
+                            ms_per_step_two_calls_graph=ms_separate,
                             decode_stage_ms=sum(v[0] for k, v in prof.items()
                                                 if k in ("dec_quant_in", "dec_in_proj", "decode_fused",
                                                          "dec_out_proj")) / args.steps,

@@ -242,6 +242,28 @@ m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* c
                       void* stream);
 
 /*
+ * A mixed batch in one call (the decode / prefill row classification of
+ * vllm.cpp PR #1289's review thread, the correction of the G1(c) arm: a row
+ * with one query token and prior state is a decode; batches are ordered
+ * decodes first):
+ *   hidden  bf16 [Bt + sum(T), 2688]: rows [0, Bt) are decode rows, one token
+ *           each, as m2_decode; the rest are the packed prefill sequences,
+ *           as m2_prefill (seqlens_host, has_initial, conv_state, ssm_state)
+ *   out     bf16 [Bt + sum(T), 2688]
+ * The input quant and both projections run once over all rows; the decode
+ * rows advance their pool rows in place, the prefill rows run the chunked
+ * scan.  Bt = 0 or nseq = 0 is allowed (not both); the decode arguments may
+ * be NULL when Bt = 0, the prefill ones when nseq = 0.  Intermediate taps are
+ * not written by this call.  Errors as m2_decode and m2_prefill.
+ */
+m2_status m2_mixed_workspace_size(const m2_handle* h, int Bt, const int32_t* seqlens_host, int nseq,
+                                  size_t* bytes);
+m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, void* ssm_pool, int n_slots,
+                   const int32_t* slot_idx, const int32_t* seqlens_host, int nseq, const uint8_t* has_initial,
+                   uint16_t* conv_state, void* ssm_state, uint16_t* out, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/*
  * Standalone static per-tensor activation quantisation (the kQuantFp8Static
  * op of PR #988, section "The Thor finding, measured"):
  *   q[i] = e4m3_satfinite_rne(fp32(x[i]) / scale)   (IEEE fp32 division)

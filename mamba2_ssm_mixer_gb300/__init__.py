@@ -33,7 +33,7 @@ EXPORTED = ["m2_last_error", "m2_create", "m2_destroy", "m2_get_stats", "m2_set_
             "m2_prefill_workspace_size", "m2_prefill", "m2_decode_workspace_size", "m2_decode",
             "fp8_quant", "fp8_linear_workspace_size", "fp8_linear", "fp8_linear_bf16",
             "m2_rmsnorm_residual", "m2_profile_enable", "m2_profile_read", "fp8_linear_noalloc",
-            "m2_prefill_q", "m2_decode_q", "m2_rmsnorm_residual_quant"]
+            "m2_prefill_q", "m2_decode_q", "m2_rmsnorm_residual_quant", "m2_mixed_workspace_size", "m2_mixed"]
 
 STAGES = ["quant_in", "in_proj", "conv", "conv_state", "ssd_cumsum", "ssd_chunk_state", "ssd_state_pass",
           "ssd_chunk_scan", "norm_quant", "out_proj", "decode_fused", "dec_quant_in", "dec_in_proj",
@@ -95,6 +95,8 @@ _sigs = {
     "m2_prefill_q": ([_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
     "m2_decode_q": ([_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _sz, _vp], _i),
     "m2_rmsnorm_residual_quant": ([_vp, _vp, _vp, _f, _f, _vp, _vp, _i, _i, _vp], _i),
+    "m2_mixed_workspace_size": ([_vp, _i, _vp, _i, ctypes.POINTER(_sz)], _i),
+    "m2_mixed": ([_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
 }
 for _name, (_args, _ret) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -270,6 +272,48 @@ class Mamba2Mixer:
         _check(fn(self._h, _ptr(hidden), Bt, _ptr(conv_pool), _ptr(ssm_pool), n_slots, _ptr(slot_idx),
                   _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
         return out
+
+    def mixed_workspace_size(self, batch: int, seqlens) -> int:
+        return _mixed_ws_size(self, batch, list(seqlens))
+
+    def mixed(self, hidden, batch, conv_pool, ssm_pool, slot_idx, seqlens, conv_state, ssm_state,
+              has_initial=None, out=None, workspace=None, stream=None):
+        """One call over `batch` decode rows (hidden[:batch], states in the
+        slot pools) followed by packed prefill sequences (hidden[batch:])."""
+        seqlens = list(seqlens)
+        R = batch + sum(seqlens)
+        _need(hidden, "hidden", torch.bfloat16, (R, HIDDEN))
+        if batch:
+            n_slots = conv_pool.shape[0]
+            _need(conv_pool, "conv_pool", torch.bfloat16, (n_slots, CONV_DIM, CONV_WIDTH - 1))
+            _need(ssm_pool, "ssm_pool", self.state_dtype, (n_slots, NHEADS, HEADDIM, D_STATE))
+            _need(slot_idx, "slot_idx", torch.int32, (batch,))
+        else:
+            n_slots = 0
+        if seqlens:
+            _need(conv_state, "conv_state", torch.bfloat16, (len(seqlens), CONV_DIM, CONV_WIDTH - 1))
+            _need(ssm_state, "ssm_state", self.state_dtype, (len(seqlens), NHEADS, HEADDIM, D_STATE))
+        if out is None:
+            out = torch.empty((R, HIDDEN), dtype=torch.bfloat16, device=hidden.device)
+        _need(out, "out", torch.bfloat16, (R, HIDDEN))
+        if workspace is None:
+            workspace = torch.empty(self.mixed_workspace_size(batch, seqlens), dtype=torch.uint8,
+                                    device=hidden.device)
+        arr = (ctypes.c_int32 * max(len(seqlens), 1))(*seqlens)
+        hi = None if has_initial is None else (ctypes.c_uint8 * len(seqlens))(*[int(bool(v)) for v in has_initial])
+        _check(_lib.m2_mixed(self._h, _ptr(hidden), batch, _ptr(conv_pool) if batch else None,
+                             _ptr(ssm_pool) if batch else None, n_slots, _ptr(slot_idx) if batch else None,
+                             arr, len(seqlens), hi, _ptr(conv_state) if seqlens else None,
+                             _ptr(ssm_state) if seqlens else None, _ptr(out), _ptr(workspace), workspace.numel(),
+                             _stream(stream)))
+        return out
+
+
+def _mixed_ws_size(blk, Bt, seqlens):
+    n = ctypes.c_size_t()
+    arr = (ctypes.c_int32 * max(len(seqlens), 1))(*seqlens)
+    _check(_lib.m2_mixed_workspace_size(blk._h, Bt, arr, len(seqlens), ctypes.byref(n)))
+    return n.value
 
 
 def fp8_quant(x: torch.Tensor, scale: float, q: torch.Tensor | None = None, stream=None) -> torch.Tensor:

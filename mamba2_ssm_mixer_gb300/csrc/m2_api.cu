@@ -513,6 +513,128 @@ m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* c
                      stream);
 }
 
+// ---------------------------------------------------------------- mixed batch
+
+// One call over an ordered batch: Bt decode rows (one token each, state in
+// the slot pool) followed by nseq packed prefill sequences.  The input quant
+// and both projections run once over all Bt + T rows; the decode rows take
+// the paged state kernel, the prefill rows the SSD path.
+struct MixedWs {
+  PrefillWs pf;   // prefill-only buffers (u, cum/dt, states, S_in, y) of T tokens
+  uint8_t* q;     // [Bt + T, 2688]
+  uint16_t* zx;   // [Bt + T, 10304]
+  uint8_t* q2;    // [Bt + T, 4096]
+  void* gemm_ws;
+  size_t gemm_ws_bytes;
+  size_t total;
+};
+
+static MixedWs carve_mixed(void* base, int Bt, int T, int chunks) {
+  Carve c{static_cast<char*>(base)};
+  MixedWs w;
+  const size_t R = (size_t)Bt + T;
+  w.q = c.take<uint8_t>(R * kH);
+  w.zx = c.take<uint16_t>(R * kZ);
+  w.q2 = c.take<uint8_t>(R * kI);
+  w.pf = PrefillWs{};
+  w.pf.u = c.take<uint16_t>((size_t)T * kConv);
+  w.pf.cumdt = c.take<CumDt>((size_t)chunks * kNH);
+  w.pf.states = c.take<float>((size_t)chunks * kNH * kP * kN);
+  w.pf.sin_img = c.take<uint8_t>((size_t)chunks * kNH * kSinImageBytes);
+  w.pf.y = c.take<uint16_t>((size_t)T * kI);
+  size_t g1 = gemm_workspace_bytes((int)R, kZ, kH), g2 = gemm_workspace_bytes((int)R, kH, kI);
+  w.gemm_ws_bytes = g1 > g2 ? g1 : g2;
+  w.gemm_ws = c.take<char>(w.gemm_ws_bytes);
+  w.total = c.off;
+  return w;
+}
+
+m2_status m2_mixed_workspace_size(const m2_handle* h, int Bt, const int32_t* seqlens_host, int nseq,
+                                  size_t* bytes) {
+  if (!h || !bytes) return fail(M2_EINVAL, "m2_mixed_workspace_size: null argument");
+  if (Bt < 0 || Bt > 4096) return fail(M2_ESHAPE, "m2_mixed: Bt %d not in [0, 4096]", Bt);
+  SeqInfo si;
+  memset(&si, 0, sizeof si);
+  if (nseq > 0) {
+    m2_status s = build_seqinfo(seqlens_host, nseq, nullptr, &si);
+    if (s) return s;
+  } else if (nseq < 0) {
+    return fail(M2_ESHAPE, "m2_mixed: nseq %d < 0", nseq);
+  }
+  if (Bt + si.total_tokens < 1) return fail(M2_ESHAPE, "m2_mixed: empty batch");
+  *bytes = carve_mixed(nullptr, Bt, si.total_tokens, si.total_chunks).total;
+  return M2_OK;
+}
+
+m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_pool, void* ssm_pool, int n_slots,
+                   const int32_t* slot_idx, const int32_t* seqlens_host, int nseq, const uint8_t* has_initial,
+                   uint16_t* conv_state, void* ssm_state, uint16_t* out, void* workspace, size_t ws_bytes,
+                   void* stream) {
+  g_err.clear();
+  if (!h || !hidden || !out || !workspace) return fail(M2_EINVAL, "m2_mixed: null argument");
+  if (Bt < 0 || Bt > 4096) return fail(M2_ESHAPE, "m2_mixed: Bt %d not in [0, 4096]", Bt);
+  if (nseq < 0) return fail(M2_ESHAPE, "m2_mixed: nseq %d < 0", nseq);
+  if (Bt > 0 && (!conv_pool || !ssm_pool || !slot_idx || n_slots < 1))
+    return fail(M2_EINVAL, "m2_mixed: decode rows need conv_pool, ssm_pool, slot_idx and n_slots >= 1");
+  if (nseq > 0 && (!conv_state || !ssm_state)) return fail(M2_EINVAL, "m2_mixed: prefill rows need their states");
+  if ((uintptr_t)workspace % 256) return fail(M2_EINVAL, "m2_mixed: workspace must be 256-byte aligned");
+  if ((uintptr_t)hidden % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_pool % 16 || (uintptr_t)ssm_state % 16)
+    return fail(M2_EINVAL, "m2_mixed: hidden, out and the state rows must be 16-byte aligned");
+  SeqInfo local;
+  memset(&local, 0, sizeof local);
+  if (nseq > 0) {
+    m2_status s = build_seqinfo(seqlens_host, nseq, has_initial, &local);
+    if (s) return s;
+  }
+  const int T = local.total_tokens;
+  const int R = Bt + T;
+  if (R < 1) return fail(M2_ESHAPE, "m2_mixed: empty batch");
+  MixedWs w = carve_mixed(workspace, Bt, T, local.total_chunks);
+  if (ws_bytes < w.total) return fail(M2_ENOMEM, "m2_mixed: workspace %zu bytes < %zu needed", ws_bytes, w.total);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const BlockParams bp = h->params();
+  const float sc1 = h->cfg.s_x * h->s_w1, sc2 = h->cfg.s_y * h->s_w2;
+  const bool bf16_state = h->cfg.ssm_dtype == M2_DTYPE_BF16;
+  // rows [0, Bt) are the decode rows, [Bt, R) the prefill tokens
+  uint16_t* zx_pf = w.zx + (size_t)Bt * kZ;
+  uint8_t* q2_pf = w.q2 + (size_t)Bt * kI;
+  int nl = 0;
+  M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)R * kH, h->cfg.s_x, w.q, st));
+  M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
+           gemm_fp8(w.q, h->in_proj, w.zx, R, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  if (T > 0) {
+    M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(zx_pf, bp, conv_state, local, w.pf.u, st));
+    M2_STAGE(h, st, M2_STAGE_CONV_STATE, 1, launch_conv_state_update(zx_pf, conv_state, local, st));
+    M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, st));
+    M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
+             launch_ssd_chunk_state_tc(w.pf.u, w.pf.cumdt, local, w.pf.states, h->err, st));
+    M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
+             launch_ssd_state_pass(w.pf.states, w.pf.cumdt, local, w.pf.sin_img, ssm_state, bf16_state, st));
+    M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
+             launch_ssd_chunk_scan_tc(w.pf.u, w.pf.cumdt, w.pf.sin_img, bp, local, w.pf.y, h->err, st));
+    M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.pf.y, zx_pf, bp, T, q2_pf, nullptr, st));
+  }
+  if (Bt > 0) {
+    DecodeTaps dt{};
+    M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
+             launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err,
+                                  dt, st));
+  }
+  M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl,
+           gemm_fp8(w.q2, h->out_proj, out, R, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  if (T > 0) {
+    h->stats.prefill_calls += 1;
+    h->stats.conv_fwd_calls += 1;
+    h->stats.chunk_scan_calls += 1;
+  }
+  if (Bt > 0) {
+    h->stats.decode_calls += 1;
+    h->stats.conv_update_rows += (uint64_t)Bt;
+    h->stats.state_update_rows += (uint64_t)Bt;
+  }
+  return M2_OK;
+}
+
 // ---------------------------------------------------------------- standalone ops
 
 m2_status fp8_quant(const uint16_t* x, size_t n, float scale, uint8_t* q, void* stream) {
