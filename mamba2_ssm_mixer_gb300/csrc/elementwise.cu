@@ -10,23 +10,31 @@ namespace m2 {
 // ---------------------------------------------------------------------------
 // Static per-tensor activation quant (kQuantFp8Static of vllm.cpp PR #988,
 // "The Thor finding, measured"): q = e4m3_satfinite_rne(fp32(x) / s).
-// 8 bf16 in (16 B), 8 codes out (8 B) per thread; grid-stride.
+// 8 bf16 in (16 B), 8 codes out (8 B) per vector; grid-stride, two
+// independent vectors in flight per thread.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint2 quant8_e4m3(uint4 v, float scale, float inv) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[2] = {0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t two = quant2_e4m3(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u), scale, inv);
+    o[j >> 1] |= two << ((j & 1) * 16);
+  }
+  return make_uint2(o[0], o[1]);
+}
+
 __global__ void __launch_bounds__(256) k_quant_e4m3_vec(const uint4* __restrict__ x, size_t nvec, float scale,
                                                         float inv, uint2* __restrict__ q) {
   pdl_wait();
   pdl_trigger();
-  size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += stride) {
-    uint4 v = x[i];
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[2] = {0u, 0u};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t two = quant2_e4m3(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xFFFF0000u), scale, inv);
-      o[j >> 1] |= two << ((j & 1) * 16);
-    }
-    q[i] = make_uint2(o[0], o[1]);
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nvec; i += 2 * stride) {
+    const bool two = i + stride < nvec;
+    const uint4 a = x[i];
+    const uint4 b = two ? x[i + stride] : make_uint4(0, 0, 0, 0);
+    q[i] = quant8_e4m3(a, scale, inv);
+    if (two) q[i + stride] = quant8_e4m3(b, scale, inv);
   }
 }
 
@@ -91,6 +99,53 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
   return make_float2(bfbits2f((uint16_t)(v & 0xFFFFu)), bfbits2f((uint16_t)(v >> 16)));
 }
 
+// Packed pairs of floats (f32x2 arithmetic of the sm_100 family), element 0
+// in the low word: the conv runs a channel pair per thread.
+__device__ __forceinline__ uint64_t f2pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t bf2pk(uint32_t v) {   // bf16 pair -> f32 pair
+  return f2pk(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2f(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2f(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// silu(v) = v / (1 + 2^(-v log2 e)) for a pair, with the hardware's
+// approximate base-2 exponential and reciprocal (relative error ~1e-7; the
+// result is rounded to bf16 next), packed to a bf16 pair.
+__device__ __forceinline__ uint32_t silu2_bf16(uint64_t v) {
+  const uint64_t m = mul2f(v, f2pk(-1.4426950408889634f, -1.4426950408889634f));   // -log2(e)
+  float m0, m1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(m0), "=f"(m1) : "l"(m));
+  float e0, e1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(m0));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(m1));
+  const uint64_t d = add2f(f2pk(e0, e1), f2pk(1.f, 1.f));
+  float d0, d1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+  float r0, r1;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d0));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d1));
+  const uint64_t s = mul2f(v, f2pk(r0, r1));
+  float s0, s1;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(s));
+  return pack_bf16x2(s0, s1);
+}
+
 __global__ void __launch_bounds__(256) k_conv_silu_prefill(const uint16_t* __restrict__ zx,
                                                            const uint16_t* __restrict__ conv_w,
                                                            const uint16_t* __restrict__ conv_b,
@@ -117,19 +172,17 @@ __global__ void __launch_bounds__(256) k_conv_silu_prefill(const uint16_t* __res
   const int t_begin = t0 + half * (kCvT / 2);
   if (t_begin >= T) return;
   const int t_end = min(t_begin + kCvT / 2, T);
-  float w[2][kW], bias[2];
+  // weights and bias of the channel pair, packed per tap
+  uint64_t w[kW];
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    bias[e] = conv_b ? bfbits2f(conv_b[c + e]) : 0.f;
-#pragma unroll
-    for (int j = 0; j < kW; ++j) w[e][j] = bfbits2f(conv_w[(c + e) * kW + j]);
-  }
-  // staged input of token t (t0 - 3 <= t < t0 + 64)
-  auto row = [&](int t) { return bf2_to_f2(*reinterpret_cast<const uint32_t*>(&tile[t - t0 + kW - 1][2 * pr])); };
+  for (int j = 0; j < kW; ++j) w[j] = f2pk(bfbits2f(conv_w[c * kW + j]), bfbits2f(conv_w[(c + 1) * kW + j]));
+  const uint64_t bias = conv_b ? f2pk(bfbits2f(conv_b[c]), bfbits2f(conv_b[c + 1])) : f2pk(0.f, 0.f);
+  // staged input pair of token t (t0 - 3 <= t < t0 + 64)
+  auto row = [&](int t) { return bf2pk(*reinterpret_cast<const uint32_t*>(&tile[t - t0 + kW - 1][2 * pr])); };
   int s = seq_of_token(si, t_begin);
   int seq_start = si.cu_seqlens[s], seq_end = si.cu_seqlens[s + 1];
   // window[k] = input at time t - 3 + k (k = 0, 1, 2) for the next token t
-  float2 win[kW - 1];
+  uint64_t win[kW - 1];
   auto load_window = [&](int t) {
     const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
 #pragma unroll
@@ -140,35 +193,34 @@ __global__ void __launch_bounds__(256) k_conv_silu_prefill(const uint16_t* __res
       } else if (init) {
         const int tap = (kW - 1) + (tt - seq_start);   // 0..2
         const uint16_t* st = conv_state + ((size_t)s * kConv + c) * (kW - 1);
-        win[k] = make_float2(bfbits2f(st[tap]), bfbits2f(st[(kW - 1) + tap]));
+        win[k] = f2pk(bfbits2f(st[tap]), bfbits2f(st[(kW - 1) + tap]));
       } else {
-        win[k] = make_float2(0.f, 0.f);
+        win[k] = f2pk(0.f, 0.f);
       }
     }
   };
   load_window(t_begin);
-  for (int t = t_begin; t < t_end; ++t) {
+  uint32_t* urow = reinterpret_cast<uint32_t*>(u + (size_t)t_begin * kConv + c);
+  int t = t_begin;
+  while (t < t_end) {
     if (t == seq_end) {   // first token of the next sequence
       ++s;
       seq_start = seq_end;
       seq_end = si.cu_seqlens[s + 1];
       load_window(t);
     }
-    const float2 x = row(t);
-    float a0 = bias[0], a1 = bias[1];
-    a0 = fmaf(w[0][0], win[0].x, a0);
-    a1 = fmaf(w[1][0], win[0].y, a1);
-    a0 = fmaf(w[0][1], win[1].x, a0);
-    a1 = fmaf(w[1][1], win[1].y, a1);
-    a0 = fmaf(w[0][2], win[2].x, a0);
-    a1 = fmaf(w[1][2], win[2].y, a1);
-    a0 = fmaf(w[0][3], x.x, a0);
-    a1 = fmaf(w[1][3], x.y, a1);
-    *reinterpret_cast<uint32_t*>(u + (size_t)t * kConv + c) =
-        (uint32_t)f2bfbits(silu_fast(a0)) | ((uint32_t)f2bfbits(silu_fast(a1)) << 16);
-    win[0] = win[1];
-    win[1] = win[2];
-    win[2] = x;
+    // tokens of one sequence: no boundary test inside
+    const int seg_end = min(t_end, seq_end);
+#pragma unroll 4
+    for (; t < seg_end; ++t) {
+      const uint64_t x = row(t);
+      const uint64_t acc = fma2(w[3], x, fma2(w[2], win[2], fma2(w[1], win[1], fma2(w[0], win[0], bias))));
+      *urow = silu2_bf16(acc);
+      urow += kConv / 2;
+      win[0] = win[1];
+      win[1] = win[2];
+      win[2] = x;
+    }
   }
 }
 

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from helpers import assert_block_out, assert_state, bf16_dev, device_weights, f32_dev, to_np
+from helpers import assert_bf16_close, assert_block_out, assert_state, bf16_dev, device_weights, f32_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -76,7 +76,11 @@ def test_mixed_bench_shape_vs_separate_calls(block0):
     rows = slots.cpu().numpy()
     assert_state(to_np(sp2)[rows], to_np(sp1)[rows])
     assert_state(to_np(ss2), to_np(ss1))
-    assert torch.equal(cs1, cs2) and torch.equal(cp1, cp2)
+    # the decode rows' zx comes from the big GEMM here and from the split-K
+    # GEMM in m2_decode (different summation order), so the raw xBC taps the
+    # conv windows carry may differ in their last bit
+    assert_bf16_close(to_np(cp2)[rows], to_np(cp1)[rows], atol=1e-3, what="decode conv rows")
+    assert_bf16_close(to_np(cs2), to_np(cs1), atol=1e-3, what="prefill conv state")
 
 
 def test_mixed_with_one_kind_equals_the_plain_call(block0):
