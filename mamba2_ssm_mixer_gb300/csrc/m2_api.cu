@@ -93,6 +93,10 @@ struct m2_handle {
   float* dt_bias = nullptr;
   uint16_t* norm_w = nullptr;
   int* err = nullptr;
+  // second stream and fork/join events of m2_mixed (decode rows run beside
+  // the prefill rows' scan)
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
   m2_stats stats;
   bool taps_on = false;
   m2_taps taps;
@@ -186,6 +190,9 @@ m2_status m2_create(const m2_config* cfg, const m2_weights* w, m2_handle** out) 
   if (!s) {
     cudaError_t e = cudaMalloc((void**)&h->err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->fork_ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->join_ev, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) s = fail(M2_ECUDA, "m2_create: %s", cudaGetErrorString(e));
   }
@@ -212,6 +219,9 @@ void m2_destroy(m2_handle* h) {
   cudaFree(h->dt_bias);
   cudaFree(h->norm_w);
   cudaFree(h->err);
+  if (h->fork_ev) cudaEventDestroy(h->fork_ev);
+  if (h->join_ev) cudaEventDestroy(h->join_ev);
+  if (h->side) cudaStreamDestroy(h->side);
   for (auto& r : h->recs) {
     cudaEventDestroy(r.a);
     cudaEventDestroy(r.b);
@@ -602,6 +612,20 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
   M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)R * kH, h->cfg.s_x, w.q, st));
   M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
            gemm_fp8(w.q, h->in_proj, w.zx, R, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  // With both kinds of rows, the decode rows' state stream (HBM-bound) runs on
+  // a second stream beside the prefill rows' scan (latency-bound, whose last
+  // waves leave SMs idle); the out_proj waits for both.  Stage profiling
+  // keeps everything on the caller's stream.
+  const bool fork = Bt > 0 && T > 0 && !h->prof_on;
+  if (fork) {
+    M2_CUDA(cudaEventRecord(h->fork_ev, st));
+    M2_CUDA(cudaStreamWaitEvent(h->side, h->fork_ev, 0));
+    DecodeTaps dt{};
+    M2_CUDA(launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err, dt,
+                                 h->side));
+    h->stats.kernel_launches += 1;
+    M2_CUDA(cudaEventRecord(h->join_ev, h->side));
+  }
   if (T > 0) {
     M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(zx_pf, bp, conv_state, local, w.pf.u, st));
     M2_STAGE(h, st, M2_STAGE_CONV_STATE, 1, launch_conv_state_update(zx_pf, conv_state, local, st));
@@ -614,7 +638,9 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
              launch_ssd_chunk_scan_tc(w.pf.u, w.pf.cumdt, w.pf.sin_img, bp, local, w.pf.y, h->err, st));
     M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.pf.y, zx_pf, bp, T, q2_pf, nullptr, st));
   }
-  if (Bt > 0) {
+  if (fork) {
+    M2_CUDA(cudaStreamWaitEvent(st, h->join_ev, 0));
+  } else if (Bt > 0) {
     DecodeTaps dt{};
     M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
              launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err,
