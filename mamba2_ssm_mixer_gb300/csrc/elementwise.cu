@@ -1,5 +1,6 @@
 // Memory-bound kernels of the mixer block: static e4m3 activation quant,
-// causal conv1d + SiLU (prefill) and its state hand-off, gated group RMSNorm
+// causal conv1d + SiLU (prefill; its state hand-off runs in the SSD cumsum
+// kernel, after every old window has been read), gated group RMSNorm
 // with the out_proj quant fused into its epilogue, and the residual RMSNorm
 // used between stacked blocks.
 #include "launch_util.h"
@@ -224,44 +225,11 @@ __global__ void __launch_bounds__(256) k_conv_silu_prefill(const uint16_t* __res
   }
 }
 
-// New conv window of each sequence: the last 3 raw xBC inputs of
-// [old state, x], oldest first.  Runs after the conv so reads of the old
-// state never race with this write; one thread owns one channel's 3 taps.
-__global__ void __launch_bounds__(256) k_conv_state_update(const uint16_t* __restrict__ zx,
-                                                           uint16_t* __restrict__ conv_state, const SeqInfo si) {
-  pdl_wait();
-  pdl_trigger();
-  const int s = blockIdx.y;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= kConv) return;
-  const int T = si.cu_seqlens[s + 1] - si.cu_seqlens[s];
-  const int t0 = si.cu_seqlens[s];
-  const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
-  uint16_t* st = conv_state + ((size_t)s * kConv + c) * (kW - 1);
-  uint16_t old[kW - 1];
-#pragma unroll
-  for (int k = 0; k < kW - 1; ++k) old[k] = init ? st[k] : (uint16_t)0;
-  uint16_t nw[kW - 1];
-#pragma unroll
-  for (int k = 0; k < kW - 1; ++k) {
-    int idx = T + k;   // index into [old(3), x(T)]
-    nw[k] = idx < kW - 1 ? old[idx] : zx[(size_t)(t0 + idx - (kW - 1)) * kZ + kOffXBC + c];
-  }
-#pragma unroll
-  for (int k = 0; k < kW - 1; ++k) st[k] = nw[k];
-}
-
 cudaError_t launch_conv_silu_prefill(const uint16_t* zx, const BlockParams& bp, const uint16_t* conv_state,
                                      const SeqInfo& si, uint16_t* u, cudaStream_t st) {
   static_assert(kConv % kCvC == 0, "conv tiles cover the channels exactly");
   dim3 grid(kConv / kCvC, (si.total_tokens + kCvT - 1) / kCvT);
   return launch_pdl(k_conv_silu_prefill, grid, dim3(kCvC), 0, st, zx, bp.conv_w, bp.conv_b, conv_state, si, u);
-}
-
-cudaError_t launch_conv_state_update(const uint16_t* zx, uint16_t* conv_state, const SeqInfo& si,
-                                     cudaStream_t st) {
-  dim3 grid((kConv + 255) / 256, si.nseq);
-  return launch_pdl(k_conv_state_update, grid, dim3(256), 0, st, zx, conv_state, si);
 }
 
 // ---------------------------------------------------------------------------

@@ -390,9 +390,8 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
     M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
   M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
   M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(w.zx, bp, conv_state, local, w.u, st));
-  M2_STAGE(h, st, M2_STAGE_CONV_STATE, 1, launch_conv_state_update(w.zx, conv_state, local, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1,
-           launch_ssd_cumsum(w.zx, bp, local, w.cumdt, h->taps_on ? h->taps.dt : nullptr, st));
+           launch_ssd_cumsum(w.zx, bp, local, w.cumdt, h->taps_on ? h->taps.dt : nullptr, conv_state, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
            launch_ssd_chunk_state_tc(w.u, w.cumdt, local, w.states, h->err, st));
   M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
@@ -628,8 +627,8 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
   }
   if (T > 0) {
     M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(zx_pf, bp, conv_state, local, w.pf.u, st));
-    M2_STAGE(h, st, M2_STAGE_CONV_STATE, 1, launch_conv_state_update(zx_pf, conv_state, local, st));
-    M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, st));
+    M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1,
+             launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, conv_state, st));
     M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
              launch_ssd_chunk_state_tc(w.pf.u, w.pf.cumdt, local, w.pf.states, h->err, st));
     M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,

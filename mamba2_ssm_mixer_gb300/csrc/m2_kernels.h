@@ -29,8 +29,7 @@ struct BlockParams {
 cudaError_t launch_quant_e4m3(const uint16_t* x, size_t n, float scale, uint8_t* q, cudaStream_t st);
 cudaError_t launch_conv_silu_prefill(const uint16_t* zx, const BlockParams& bp, const uint16_t* conv_state,
                                      const SeqInfo& si, uint16_t* u, cudaStream_t st);
-cudaError_t launch_conv_state_update(const uint16_t* zx, uint16_t* conv_state, const SeqInfo& si,
-                                     cudaStream_t st);
+
 cudaError_t launch_gated_norm_quant(const uint16_t* y, const uint16_t* zx, const BlockParams& bp, int T,
                                     uint8_t* q2, uint16_t* o_tap, cudaStream_t st);
 cudaError_t launch_rmsnorm_residual(uint16_t* h, const uint16_t* add, const uint16_t* w, float eps,
@@ -52,8 +51,10 @@ static_assert(sizeof(CumDt) == 4096, "one cum/dt record is 4 KB (one bulk copy)"
 constexpr int kSinImageBytes = 2 * 64 * 128 * 2;
 
 // dt_tok (optional, may be null): dt as [T, 64] for the intermediate taps.
+// conv_state (may be null): also writes each sequence's new conv window
+// (the last 3 raw xBC inputs), after the conv has read the old one.
 cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, CumDt* cumdt,
-                              float* dt_tok, cudaStream_t st);
+                              float* dt_tok, uint16_t* conv_state, cudaStream_t st);
 // Reads the chunk states, writes the state entering each chunk as S_in images
 // and the final state of each sequence to ssm_state.
 cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const SeqInfo& si, uint8_t* sin_img,
