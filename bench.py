@@ -712,7 +712,8 @@ def run_case(args):
     if args.case in ("in_proj", "out_proj"):
         rng = torch.Generator(device=dev)
         rng.manual_seed(1)
-        M, N, K = (T_PF, Z, H) if args.case == "in_proj" else (T_PF, H, I)
+        R = T_PF + DEC_B                              # the mixed step's rows
+        M, N, K = (R, Z, H) if args.case == "in_proj" else (R, H, I)
         a = torch.randint(0, 0x7E, (M, K), generator=rng, device=dev, dtype=torch.int32).to(torch.uint8)
         w = torch.randint(0, 0x7E, (N, K), generator=rng, device=dev, dtype=torch.int32).to(torch.uint8)
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
