@@ -403,9 +403,13 @@ def run_ours(args, rank, world, local_rank):
         e.record(comp)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    t_start.record(comp)
     up.wait_stream(comp)
-    for i in range(args.steps):
+    for i in range(args.warmup + args.steps):   # the first W iterations warm the copy paths up
+        if i == args.warmup:
+            comp.wait_stream(down)
+            comp.wait_stream(up)
+            t_start.record(comp)
+            up.wait_stream(comp)
         b = i & 1
         with torch.cuda.stream(up):                  # upload into buffer b once step i-2 is done with it
             up.wait_event(done[b])
