@@ -96,7 +96,7 @@ struct m2_handle {
   // second stream and fork/join events of m2_mixed (decode rows run beside
   // the prefill rows' scan)
   cudaStream_t side = nullptr;
-  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr, cum_ev = nullptr;
   m2_stats stats;
   bool taps_on = false;
   m2_taps taps;
@@ -193,6 +193,7 @@ m2_status m2_create(const m2_config* cfg, const m2_weights* w, m2_handle** out) 
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->fork_ev, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->join_ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h->cum_ev, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) s = fail(M2_ECUDA, "m2_create: %s", cudaGetErrorString(e));
   }
@@ -221,6 +222,7 @@ void m2_destroy(m2_handle* h) {
   cudaFree(h->err);
   if (h->fork_ev) cudaEventDestroy(h->fork_ev);
   if (h->join_ev) cudaEventDestroy(h->join_ev);
+  if (h->cum_ev) cudaEventDestroy(h->cum_ev);
   if (h->side) cudaStreamDestroy(h->side);
   for (auto& r : h->recs) {
     cudaEventDestroy(r.a);
@@ -389,14 +391,27 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
   if (!hidden_q)
     M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
   M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  // the cumsum reads only the in_proj output: it runs on the second stream
+  // beside the conv (serially while stage profiling)
+  float* dt_tap = h->taps_on ? h->taps.dt : nullptr;
+  if (!h->prof_on) {
+    M2_CUDA(cudaEventRecord(h->fork_ev, st));
+    M2_CUDA(cudaStreamWaitEvent(h->side, h->fork_ev, 0));
+    M2_CUDA(launch_ssd_cumsum(w.zx, bp, local, w.cumdt, dt_tap, h->side));
+    h->stats.kernel_launches += 1;
+    M2_CUDA(cudaEventRecord(h->cum_ev, h->side));
+  }
   M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(w.zx, bp, conv_state, local, w.u, st));
-  M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1,
-           launch_ssd_cumsum(w.zx, bp, local, w.cumdt, h->taps_on ? h->taps.dt : nullptr, conv_state, st));
+  if (h->prof_on) {
+    M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(w.zx, bp, local, w.cumdt, dt_tap, st));
+  } else {
+    M2_CUDA(cudaStreamWaitEvent(st, h->cum_ev, 0));
+  }
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
            launch_ssd_chunk_state_tc(w.u, w.cumdt, local, w.states, h->err, st));
   M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
            launch_ssd_state_pass(w.states, w.cumdt, local, w.sin_img, ssm_state, h->cfg.ssm_dtype == M2_DTYPE_BF16,
-                                 st));
+                                 w.zx, conv_state, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
            launch_ssd_chunk_scan_tc(w.u, w.cumdt, w.sin_img, bp, local, w.y, h->err, st));
   M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
@@ -611,33 +626,45 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
   M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)R * kH, h->cfg.s_x, w.q, st));
   M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
            gemm_fp8(w.q, h->in_proj, w.zx, R, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
-  // With both kinds of rows, the decode rows' state stream (HBM-bound) runs on
-  // a second stream beside the prefill rows' scan (latency-bound, whose last
-  // waves leave SMs idle); the out_proj waits for both.  Stage profiling
-  // keeps everything on the caller's stream.
-  const bool fork = Bt > 0 && T > 0 && !h->prof_on;
+  // A second stream runs, beside the prefill rows' conv and scan, the
+  // prefill cumsum (it reads only the in_proj output) and then the decode
+  // rows' state stream (HBM-bound; the scan is latency-bound and its last
+  // waves leave SMs idle).  The chunk states wait for the cumsum, the out_proj
+  // for the decode rows.  Stage profiling keeps everything on the caller's
+  // stream.
+  const bool fork = !h->prof_on && T > 0;
+  const bool fork_decode = fork && Bt > 0;
   if (fork) {
     M2_CUDA(cudaEventRecord(h->fork_ev, st));
     M2_CUDA(cudaStreamWaitEvent(h->side, h->fork_ev, 0));
-    DecodeTaps dt{};
-    M2_CUDA(launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err, dt,
-                                 h->side));
+    M2_CUDA(launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, h->side));
+    M2_CUDA(cudaEventRecord(h->cum_ev, h->side));
     h->stats.kernel_launches += 1;
-    M2_CUDA(cudaEventRecord(h->join_ev, h->side));
+    if (fork_decode) {
+      DecodeTaps dt{};
+      M2_CUDA(launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err,
+                                   dt, h->side));
+      h->stats.kernel_launches += 1;
+      M2_CUDA(cudaEventRecord(h->join_ev, h->side));
+    }
   }
   if (T > 0) {
     M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(zx_pf, bp, conv_state, local, w.pf.u, st));
-    M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1,
-             launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, conv_state, st));
+    if (fork) {
+      M2_CUDA(cudaStreamWaitEvent(st, h->cum_ev, 0));
+    } else {
+      M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, st));
+    }
     M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
              launch_ssd_chunk_state_tc(w.pf.u, w.pf.cumdt, local, w.pf.states, h->err, st));
     M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
-             launch_ssd_state_pass(w.pf.states, w.pf.cumdt, local, w.pf.sin_img, ssm_state, bf16_state, st));
+             launch_ssd_state_pass(w.pf.states, w.pf.cumdt, local, w.pf.sin_img, ssm_state, bf16_state, zx_pf,
+                                   conv_state, st));
     M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
              launch_ssd_chunk_scan_tc(w.pf.u, w.pf.cumdt, w.pf.sin_img, bp, local, w.pf.y, h->err, st));
     M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.pf.y, zx_pf, bp, T, q2_pf, nullptr, st));
   }
-  if (fork) {
+  if (fork_decode) {
     M2_CUDA(cudaStreamWaitEvent(st, h->join_ev, 0));
   } else if (Bt > 0) {
     DecodeTaps dt{};

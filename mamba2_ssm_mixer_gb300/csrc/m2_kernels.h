@@ -51,14 +51,15 @@ static_assert(sizeof(CumDt) == 4096, "one cum/dt record is 4 KB (one bulk copy)"
 constexpr int kSinImageBytes = 2 * 64 * 128 * 2;
 
 // dt_tok (optional, may be null): dt as [T, 64] for the intermediate taps.
-// conv_state (may be null): also writes each sequence's new conv window
-// (the last 3 raw xBC inputs), after the conv has read the old one.
 cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, CumDt* cumdt,
-                              float* dt_tok, uint16_t* conv_state, cudaStream_t st);
+                              float* dt_tok, cudaStream_t st);
 // Reads the chunk states, writes the state entering each chunk as S_in images
 // and the final state of each sequence to ssm_state.
+// conv_state (may be null): also writes each sequence's new conv window
+// (the last 3 raw xBC inputs of zx), after the conv has read the old one.
 cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const SeqInfo& si, uint8_t* sin_img,
-                                  void* ssm_state, bool bf16_state, cudaStream_t st);
+                                  void* ssm_state, bool bf16_state, const uint16_t* zx, uint16_t* conv_state,
+                                  cudaStream_t st);
 
 // ssd_tc.cu (tensor-core chunk states and chunk scan)
 // Chunk states f32 [chunk][head][64][128].

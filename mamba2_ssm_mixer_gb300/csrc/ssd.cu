@@ -52,15 +52,10 @@ __device__ __forceinline__ FF ff_add(FF a, FF b) {
 }
 }  // namespace
 
-// Also hands each sequence's conv window over (CausalConv1dFwd's state
-// output): the CTAs of a sequence's last chunk write the last 3 raw xBC
-// inputs of [old state, x], oldest first, 96 channels per head index.  The
-// conv kernel, which reads the old windows, has finished by then (stream
-// order).
+// Depends only on the in_proj output, so it may run beside the conv.
 __global__ void __launch_bounds__(256) k_ssd_cumsum(const uint16_t* __restrict__ zx, const float* __restrict__ A_log,
                                                     const float* __restrict__ dt_bias, const SeqInfo si,
-                                                    CumDt* __restrict__ cumdt, float* __restrict__ dt_tok,
-                                                    uint16_t* __restrict__ conv_state) {
+                                                    CumDt* __restrict__ cumdt, float* __restrict__ dt_tok) {
   __shared__ FF wsum[8];
   __shared__ FF cums[kChunk];
   pdl_wait();
@@ -100,25 +95,6 @@ __global__ void __launch_bounds__(256) k_ssd_cumsum(const uint16_t* __restrict__
   r.lo[i] = v.lo;
   r.dt[i] = dt;
   r.colf[i] = colf;
-
-  constexpr int kChPerHead = kConv / kNH;   // 96
-  if (conv_state && i < kChPerHead && c == si.cu_chunks[cp.seq + 1] - 1) {
-    const int s = cp.seq, ch = h * kChPerHead + i;
-    const int T = si.cu_seqlens[s + 1] - si.cu_seqlens[s];
-    const int t0 = si.cu_seqlens[s];
-    const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
-    uint16_t* st = conv_state + ((size_t)s * kConv + ch) * (kW - 1);
-    uint16_t old[kW - 1], nw[kW - 1];
-#pragma unroll
-    for (int k = 0; k < kW - 1; ++k) old[k] = init ? st[k] : (uint16_t)0;
-#pragma unroll
-    for (int k = 0; k < kW - 1; ++k) {
-      const int idx = T + k;   // index into [old(3), x(T)]
-      nw[k] = idx < kW - 1 ? old[idx] : zx[(size_t)(t0 + idx - (kW - 1)) * kZ + kOffXBC + ch];
-    }
-#pragma unroll
-    for (int k = 0; k < kW - 1; ++k) st[k] = nw[k];
-  }
 }
 
 // 3. sequential state passing over the chunks of each sequence: the state
@@ -145,14 +121,37 @@ __device__ __forceinline__ void st_state4(uint16_t* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 
+// The blocks of slice 0 also hand each sequence's conv window over
+// (CausalConv1dFwd's state output): the last 3 raw xBC inputs of [old state,
+// x], oldest first, 96 channels per head index.  The conv kernel, which reads
+// the old windows, has finished before this kernel starts (stream order).
 template <typename SS>
 __global__ void __launch_bounds__(256) k_ssd_state_pass(const float* __restrict__ states,
                                                         const CumDt* __restrict__ cumdt, const SeqInfo si,
                                                         uint8_t* __restrict__ sin_img,
-                                                        SS* __restrict__ ssm_state) {
+                                                        SS* __restrict__ ssm_state, const uint16_t* __restrict__ zx,
+                                                        uint16_t* __restrict__ conv_state) {
   pdl_wait();
   pdl_trigger();
   const int s = blockIdx.x, h = blockIdx.y;
+  constexpr int kChPerHead = kConv / kNH;   // 96
+  if (conv_state && blockIdx.z == 0 && threadIdx.x < kChPerHead) {
+    const int ch = h * kChPerHead + threadIdx.x;
+    const int T = si.cu_seqlens[s + 1] - si.cu_seqlens[s];
+    const int t0 = si.cu_seqlens[s];
+    const bool init = (si.has_init[s >> 5] >> (s & 31)) & 1u;
+    uint16_t* st = conv_state + ((size_t)s * kConv + ch) * (kW - 1);
+    uint16_t old[kW - 1], nw[kW - 1];
+#pragma unroll
+    for (int k = 0; k < kW - 1; ++k) old[k] = init ? st[k] : (uint16_t)0;
+#pragma unroll
+    for (int k = 0; k < kW - 1; ++k) {
+      const int idx = T + k;   // index into [old(3), x(T)]
+      nw[k] = idx < kW - 1 ? old[idx] : zx[(size_t)(t0 + idx - (kW - 1)) * kZ + kOffXBC + ch];
+    }
+#pragma unroll
+    for (int k = 0; k < kW - 1; ++k) st[k] = nw[k];
+  }
   const int e4 = blockIdx.z * 256 + threadIdx.x;   // float4 index inside [P, N]
   const int p = (e4 * 4) / kN, n = (e4 * 4) % kN;
   const uint32_t off = sin_offset(p, n);
@@ -202,20 +201,21 @@ __global__ void __launch_bounds__(256) k_ssd_state_pass(const float* __restrict_
 }
 
 cudaError_t launch_ssd_cumsum(const uint16_t* zx, const BlockParams& bp, const SeqInfo& si, CumDt* cumdt,
-                              float* dt_tok, uint16_t* conv_state, cudaStream_t st) {
-  static_assert(kConv % kNH == 0, "the conv window hand-off splits the channels over the heads");
+                              float* dt_tok, cudaStream_t st) {
   return launch_pdl(k_ssd_cumsum, dim3(si.total_chunks, kNH), dim3(256), 0, st, zx, bp.A_log, bp.dt_bias, si, cumdt,
-                    dt_tok, conv_state);
+                    dt_tok);
 }
 
 cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const SeqInfo& si, uint8_t* sin_img,
-                                  void* ssm_state, bool bf16_state, cudaStream_t st) {
+                                  void* ssm_state, bool bf16_state, const uint16_t* zx, uint16_t* conv_state,
+                                  cudaStream_t st) {
+  static_assert(kConv % kNH == 0, "the conv window hand-off splits the channels over the heads");
   const dim3 grid(si.nseq, kNH, (kP * kN) / 4 / 256);
   if (bf16_state)
     return launch_pdl(k_ssd_state_pass<uint16_t>, grid, dim3(256), 0, st, states, cumdt, si, sin_img,
-                      static_cast<uint16_t*>(ssm_state));
+                      static_cast<uint16_t*>(ssm_state), zx, conv_state);
   return launch_pdl(k_ssd_state_pass<float>, grid, dim3(256), 0, st, states, cumdt, si, sin_img,
-                    static_cast<float*>(ssm_state));
+                    static_cast<float*>(ssm_state), zx, conv_state);
 }
 
 }  // namespace m2
