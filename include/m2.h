@@ -49,6 +49,8 @@ enum {
 };
 
 enum { M2_DTYPE_F32 = 0, M2_DTYPE_BF16 = 1 };
+/* Arithmetic of the two projections (m2_config.arm). */
+enum { M2_ARM_W8A8 = 0, M2_ARM_W8A16 = 1 };
 enum { M2_LAYOUT_OUT_IN = 0 };   /* weights stored [out, in] (torch Linear) */
 
 /* Model geometry and static per-tensor scales. */
@@ -70,6 +72,22 @@ typedef struct m2_config {
   float eps;        /* gated RMSNorm epsilon (1e-5) */
   float s_x;        /* static input_scale of in_proj's activation (> 0) */
   float s_y;        /* static input_scale of out_proj's activation (> 0) */
+  int arm;          /* M2_ARM_W8A8 (0, the device arm: e4m3 activations with
+                       the static input_scales above, e4m3 weights) or
+                       M2_ARM_W8A16, the host reference arm of PR #1288,
+                       section "The comparison is not bit-comparable, and that
+                       is the point": input_scale is carried and not applied,
+                       so both projections take their bf16 activations as they
+                       are (the hidden input and the gated-norm output) against
+                       weights dequantised to bf16 once at m2_create,
+                       w = bf16(dec(code) * weight_scale), product in f32,
+                       round to nearest even (PR #1289, commit "the FP8 W8A8
+                       seam": DenseBf16 expands the fp8 tower to bf16).  Both
+                       arms accumulate in f32 and round the result to bf16.
+                       The W8A16 arm serves m2_prefill and m2_decode only; the
+                       pre-quantised and mixed-batch calls refuse it with
+                       M2_EINVAL.  The handle then also holds the bf16 weights
+                       (2 bytes per weight more). */
 } m2_config;
 
 /*
@@ -322,6 +340,30 @@ m2_status fp8_linear_noalloc(const uint8_t* a_q, float s_a, const uint8_t* w_q, 
  */
 m2_status fp8_linear_bf16(const uint16_t* x, float s_a, const uint8_t* w_q, float s_w, uint16_t* y,
                           int M, int N, int K, void* workspace, size_t ws_bytes, void* stream);
+
+/*
+ * Weight dequantisation of the W8A16 arm (what m2_create does to both
+ * projections when cfg->arm is M2_ARM_W8A16):
+ *   out[i] = bf16( dec(q[i]) * scale )      (product in f32, round to nearest even)
+ * q e4m3 [n] (8-byte aligned), out bf16 [n] (16-byte aligned), both device;
+ * scale positive and finite.  Bit-exact.  NaN codes give NaN.
+ * Errors: M2_EINVAL.
+ */
+m2_status fp8_dequant(const uint8_t* q, size_t n, float scale, uint16_t* out, void* stream);
+
+/* Workspace bytes bf16_linear needs for an M x N x K problem (0 for many). */
+m2_status bf16_linear_workspace_size(int M, int N, int K, size_t* bytes);
+
+/*
+ * The W8A16 arm's linear layer (vt::MatmulBT on dequantised weights, PR
+ * #1289, GB10 counter-measurement commit):
+ *   y[m, n] = bf16( scale * sum_k x[m, k] * w[n, k] )
+ * x bf16 [M, K], w bf16 [N, K] ([out, in]), y bf16 [M, N], all device, on the
+ * tensor cores with f32 accumulation.  K must be a multiple of 16 and all
+ * pointers 16-byte aligned.  Errors: M2_EINVAL, M2_ESHAPE, M2_ENOMEM.
+ */
+m2_status bf16_linear(const uint16_t* x, const uint16_t* w, float scale, uint16_t* y, int M, int N, int K,
+                      void* workspace, size_t ws_bytes, void* stream);
 
 /*
  * Between stacked blocks (pre-norm residual stack):

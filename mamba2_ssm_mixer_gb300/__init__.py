@@ -24,6 +24,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 M2_OK, M2_EINVAL, M2_ESHAPE, M2_ECUDA, M2_ETIMEOUT, M2_EDEVICE, M2_ENOMEM = range(7)
 M2_DTYPE_F32, M2_DTYPE_BF16 = 0, 1
+M2_ARM_W8A8, M2_ARM_W8A16 = 0, 1
 M2_LAYOUT_OUT_IN = 0
 
 STATUS_NAMES = {0: "M2_OK", 1: "M2_EINVAL", 2: "M2_ESHAPE", 3: "M2_ECUDA", 4: "M2_ETIMEOUT",
@@ -33,7 +34,8 @@ EXPORTED = ["m2_last_error", "m2_create", "m2_destroy", "m2_get_stats", "m2_set_
             "m2_prefill_workspace_size", "m2_prefill", "m2_decode_workspace_size", "m2_decode",
             "fp8_quant", "fp8_linear_workspace_size", "fp8_linear", "fp8_linear_bf16",
             "m2_rmsnorm_residual", "m2_profile_enable", "m2_profile_read", "fp8_linear_noalloc",
-            "m2_prefill_q", "m2_decode_q", "m2_rmsnorm_residual_quant", "m2_mixed_workspace_size", "m2_mixed"]
+            "m2_prefill_q", "m2_decode_q", "m2_rmsnorm_residual_quant", "m2_mixed_workspace_size", "m2_mixed",
+            "fp8_dequant", "bf16_linear_workspace_size", "bf16_linear"]
 
 STAGES = ["quant_in", "in_proj", "conv", "conv_state", "ssd_cumsum", "ssd_chunk_state", "ssd_state_pass",
           "ssd_chunk_scan", "norm_quant", "out_proj", "decode_fused", "dec_quant_in", "dec_in_proj",
@@ -51,7 +53,7 @@ class m2_config(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int), ("d_inner", ctypes.c_int), ("nheads", ctypes.c_int),
                 ("headdim", ctypes.c_int), ("n_groups", ctypes.c_int), ("d_state", ctypes.c_int),
                 ("conv_width", ctypes.c_int), ("chunk_size", ctypes.c_int), ("ssm_dtype", ctypes.c_int),
-                ("eps", ctypes.c_float), ("s_x", ctypes.c_float), ("s_y", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("s_x", ctypes.c_float), ("s_y", ctypes.c_float), ("arm", ctypes.c_int)]
 
 
 class m2_weights(ctypes.Structure):
@@ -97,6 +99,9 @@ _sigs = {
     "m2_rmsnorm_residual_quant": ([_vp, _vp, _vp, _f, _f, _vp, _vp, _i, _i, _vp], _i),
     "m2_mixed_workspace_size": ([_vp, _i, _vp, _i, ctypes.POINTER(_sz)], _i),
     "m2_mixed": ([_vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i),
+    "fp8_dequant": ([_vp, _sz, _f, _vp, _vp], _i),
+    "bf16_linear_workspace_size": ([_i, _i, _i, ctypes.POINTER(_sz)], _i),
+    "bf16_linear": ([_vp, _vp, _f, _vp, _i, _i, _i, _vp, _sz, _vp], _i),
 }
 for _name, (_args, _ret) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -146,26 +151,28 @@ ZX_WIDTH = D_INNER + CONV_DIM + NHEADS
 
 
 def make_config(s_x: float, s_y: float, eps: float = 1e-5, chunk_size: int = 256,
-                ssm_dtype: int = M2_DTYPE_F32) -> m2_config:
+                ssm_dtype: int = M2_DTYPE_F32, arm: int = M2_ARM_W8A8) -> m2_config:
     return m2_config(HIDDEN, D_INNER, NHEADS, HEADDIM, N_GROUPS, D_STATE, CONV_WIDTH, chunk_size, ssm_dtype,
-                     eps, s_x, s_y)
+                     eps, s_x, s_y, arm)
 
 
 class Mamba2Mixer:
     """One mixer block.  ``weights`` maps names to CPU or CUDA tensors:
     in_proj uint8 [10304, 2688], s_w1, out_proj uint8 [2688, 4096], s_w2,
     conv_w bf16 [6144, 4], conv_b bf16 [6144] or None, A_log, D, dt_bias f32 [64],
-    norm_w bf16 [4096]; plus s_x, s_y (activation scales) and eps."""
+    norm_w bf16 [4096]; plus s_x, s_y (activation scales) and eps.
+    arm: M2_ARM_W8A8 (e4m3 activations) or M2_ARM_W8A16 (bf16 activations
+    against weights dequantised to bf16; prefill and decode only)."""
 
     def __init__(self, weights: dict, device=None, layout: int = M2_LAYOUT_OUT_IN,
-                 ssm_dtype: int = M2_DTYPE_F32, chunk_size: int = 256):
+                 ssm_dtype: int = M2_DTYPE_F32, chunk_size: int = 256, arm: int = M2_ARM_W8A8):
         self.device = torch.device(device if device is not None else "cuda")
         with torch.cuda.device(self.device):
             keep = {}
             for k in ("in_proj", "out_proj", "conv_w", "conv_b", "A_log", "D", "dt_bias", "norm_w"):
                 v = weights.get(k)
                 keep[k] = None if v is None else v.contiguous()
-            cfg = make_config(weights["s_x"], weights["s_y"], weights.get("eps", 1e-5), chunk_size, ssm_dtype)
+            cfg = make_config(weights["s_x"], weights["s_y"], weights.get("eps", 1e-5), chunk_size, ssm_dtype, arm)
             w = m2_weights(_ptr(keep["in_proj"]), weights["s_w1"], _ptr(keep["out_proj"]), weights["s_w2"],
                            _ptr(keep["conv_w"]), _ptr(keep["conv_b"]), _ptr(keep["A_log"]), _ptr(keep["D"]),
                            _ptr(keep["dt_bias"]), _ptr(keep["norm_w"]), layout)
@@ -174,6 +181,7 @@ class Mamba2Mixer:
         self._h = h
         self._taps = None
         self.s_x = float(weights["s_x"])   # the input quant scale (for pre-quantised inputs)
+        self.arm = arm
         # dtype of the SSM state rows this block reads and writes
         self.state_dtype = torch.bfloat16 if ssm_dtype == M2_DTYPE_BF16 else torch.float32
 
@@ -373,6 +381,39 @@ def fp8_linear_bf16(x: torch.Tensor, s_a: float, w_q: torch.Tensor, s_w: float, 
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
     _check(_lib.fp8_linear_bf16(_ptr(x), s_a, _ptr(w_q), s_w, _ptr(y), M, N, K, _ptr(workspace),
                                 workspace.numel(), _stream(stream)))
+    return y
+
+
+def fp8_dequant(q: torch.Tensor, scale: float, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """bf16(dec(q) * scale), the W8A16 arm's weight dequantisation."""
+    _need(q, "q", torch.uint8)
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    _need(out, "out", torch.bfloat16, tuple(q.shape))
+    _check(_lib.fp8_dequant(_ptr(q), q.numel(), scale, _ptr(out), _stream(stream)))
+    return out
+
+
+def bf16_linear_workspace_size(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.bf16_linear_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
+def bf16_linear(x: torch.Tensor, w: torch.Tensor, scale: float = 1.0, y: torch.Tensor | None = None,
+                workspace=None, stream=None) -> torch.Tensor:
+    """y = bf16(scale * x @ w^T), bf16 operands on the tensor cores (W8A16 arm)."""
+    M, K = x.shape
+    N = w.shape[0]
+    _need(x, "x", torch.bfloat16, (M, K))
+    _need(w, "w", torch.bfloat16, (N, K))
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, "y", torch.bfloat16, (M, N))
+    if workspace is None:
+        workspace = torch.empty(max(bf16_linear_workspace_size(M, N, K), 1), dtype=torch.uint8, device=x.device)
+    _check(_lib.bf16_linear(_ptr(x), _ptr(w), scale, _ptr(y), M, N, K, _ptr(workspace), workspace.numel(),
+                            _stream(stream)))
     return y
 
 

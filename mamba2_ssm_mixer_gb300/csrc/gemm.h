@@ -1,22 +1,34 @@
-// W8A8 GEMM dispatch: y[M,N] = bf16(scale * A[M,K] . B[N,K]^T), e4m3 operands.
+// GEMM dispatch: y[M,N] = bf16(scale * A[M,K] . B[N,K]^T) on the tensor
+// cores, operands e4m3 codes (W8A8) or bf16 values (the W8A16 arm).
 #pragma once
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
 
 namespace m2 {
-// Scratch bytes gemm_fp8 needs for this shape (split-K partials).
+// Scratch bytes gemm_fp8 / gemm_bf16 need for this shape (split-K partials).
 size_t gemm_workspace_bytes(int M, int N, int K);
+size_t gemm_workspace_bytes_bf16(int M, int N, int K);
 // *launches receives the number of kernels launched.
 // err: device error word for bounded-wait timeouts (may be null).
 cudaError_t gemm_fp8(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale,
                      void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches);
+cudaError_t gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, int N, int K, float scale,
+                      void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches);
 
-// tensor-core kernels (gemm_tc.cu)
-size_t gemm_tc_skinny_workspace(int Mtok, int N, int K);
+// tensor-core kernels (gemm_tc.cu); Kbytes = K x operand size
+size_t gemm_tc_skinny_workspace(int Mtok, int N, int Kbytes);
 cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
                            void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches);
+cudaError_t gemm_tc_skinny_bf16(const uint16_t* X, const uint16_t* W, uint16_t* y, int Mtok, int N, int K,
+                                float scale, void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches);
 cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
                         cudaStream_t st);
+cudaError_t gemm_tc_big_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, int N, int K, float scale,
+                             int* err, cudaStream_t st);
 constexpr int kSkinnyMaxRows = 256;
+
+// W8A16 weight preparation (dequant.cu): out[i] = bf16(dec(q[i]) * scale),
+// the product formed in f32 and rounded to nearest even.
+cudaError_t launch_dequant_e4m3_bf16(const uint8_t* q, size_t n, float scale, uint16_t* out, cudaStream_t st);
 }  // namespace m2

@@ -1,14 +1,17 @@
-// Tensor-core W8A8 GEMMs for sm_103a: y = bf16(scale * A . B^T) with e4m3
-// operands stored K-major ([rows, K] row-major), f32 accumulation in TMEM.
+// Tensor-core GEMMs for sm_103a: y = bf16(scale * A . B^T) with operands
+// stored K-major ([rows, K] row-major), f32 accumulation in TMEM.  The
+// operands are e4m3 codes (W8A8, tcgen05.mma kind::f8f6f4, 32 per MMA) or
+// bf16 values (the W8A16 arm, kind::f16, 16 per MMA); either way one MMA
+// consumes 32 bytes of each 128-byte swizzled K-slice.
 //
-// k_gemm_fp8_tc  (prefill, many rows): persistent CTAs, one per SM, each
+// k_gemm_tc  (prefill, many rows): persistent CTAs, one per SM, each
 //   walking 128 x BN output tiles.  Warp roles: warp 0 issues TMA loads of
 //   128-byte-swizzled K-slices into a STAGES-deep shared-memory ring, warp 1
-//   issues tcgen05.mma (128 x BN x 32 per instruction) into one of two TMEM
-//   accumulators, warps 2-5 drain the other accumulator (tcgen05.ld), scale,
-//   round to bf16 and store, so the epilogue of tile i overlaps the MMAs of
-//   tile i+1.
-// k_gemm_fp8_tc_skinny (decode, few rows): the weight matrix is the MMA's
+//   issues tcgen05.mma (128 x BN x 32 bytes of K per instruction) into one of
+//   two TMEM accumulators, warps 2-5 drain the other accumulator
+//   (tcgen05.ld), scale, round to bf16 and store, so the epilogue of tile i
+//   overlaps the MMAs of tile i+1.
+// k_gemm_tc_skinny (decode, few rows): the weight matrix is the MMA's
 //   128-row A operand and the few activation rows are its N operand
 //   (D^T = W . X^T), with the K dimension split across CTAs so every SM
 //   streams weights; f32 partials are summed by k_splitk_reduce.
@@ -30,6 +33,15 @@ namespace {
 
 constexpr int kBM = 128;        // MMA M (rows of the A operand per tile)
 constexpr int kBK = 128;        // K bytes per pipeline stage (one 128-byte swizzle row)
+
+// One MMA over 32 bytes of K: 32 e4m3 codes or 16 bf16 values.
+template <bool kBf16>
+__device__ __forceinline__ void mma_k32b(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if constexpr (kBf16)
+    mma_f16(d_tmem, a, b, idesc, acc);
+  else
+    mma_f8f6f4(d_tmem, a, b, idesc, acc);
+}
 constexpr int kThreads = 192;   // 6 warps: producer, MMA, 4 x epilogue
 
 struct __align__(8) Ctl {
@@ -52,10 +64,10 @@ __device__ __forceinline__ void raise_abort(Ctl* ctl, int* err) {
 // ---------------------------------------------------------------------------
 // Persistent prefill GEMM.
 // ---------------------------------------------------------------------------
-template <int BN, int STAGES>
+template <int BN, int STAGES, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_fp8_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  uint16_t* __restrict__ C, int M, int N, int K, float scale, int* err) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              uint16_t* __restrict__ C, int M, int N, int K, float scale, int* err) {
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
   static_assert(STAGES <= 8, "STAGES");
   constexpr uint32_t A_BYTES = kBM * kBK;
@@ -63,7 +75,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                  : (2 * BN <= 256) ? 256 : 512;
-  constexpr uint32_t IDESC = idesc_f32acc(kBM, BN, 0u);
+  constexpr uint32_t IDESC = idesc_f32acc(kBM, BN, kBf16 ? 1u : 0u);   // operand format: e4m3 0, bf16 1
+  constexpr int ES = kBf16 ? 2 : 1;                                      // bytes per operand element
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align<1024>(smem_raw);
@@ -73,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + BN - 1) / BN;
   const int num_tiles = tiles_m * tiles_n;
-  const int kblocks = (K + kBK - 1) / kBK;
+  const int kblocks = (K * ES + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -119,8 +132,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sA = smem + stage * STAGE_BYTES;
           mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
-          tma_load_2d(sA, &tmA, &ctl->full[stage], kb * kBK, m0);
-          tma_load_2d(sA + A_BYTES, &tmB, &ctl->full[stage], kb * kBK, n0);
+          tma_load_2d(sA, &tmA, &ctl->full[stage], kb * (kBK / ES), m0);
+          tma_load_2d(sA + A_BYTES, &tmB, &ctl->full[stage], kb * (kBK / ES), n0);
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == STAGES) stage = 0, phase ^= 1u;
@@ -158,8 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t adesc = desc_kmajor_sw128(a_addr);
           const uint64_t bdesc = desc_kmajor_sw128(a_addr + A_BYTES);
 #pragma unroll
-          for (int k = 0; k < kBK / 32; ++k)   // 32 e4m3 per MMA: +32 bytes = +2 in the address field
-            mma_f8f6f4(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+          for (int k = 0; k < kBK / 32; ++k)   // 32 bytes of K per MMA: +2 in the address field
+            mma_k32b<kBf16>(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
           mma_commit(&ctl->empty[stage]);
           if (++stage == STAGES) stage = 0, phase ^= 1u;
         }
@@ -231,17 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 //   k-blocks [kb0, kb1) of this split.  splits == 1: bf16 y[m, n] directly;
 //   else f32 partial[split][m][n].
 // ---------------------------------------------------------------------------
-template <int BNT, int STAGES>
+template <int BNT, int STAGES, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_fp8_tc_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                         uint16_t* __restrict__ y, float* __restrict__ partial, int Mtok, int N, int K,
-                         int kb_per_split, float scale, int* err) {
+    k_gemm_tc_skinny(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                     uint16_t* __restrict__ y, float* __restrict__ partial, int Mtok, int N, int K,
+                     int kb_per_split, float scale, int* err) {
   static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= 256, "BNT");
   constexpr uint32_t A_BYTES = kBM * kBK;
   constexpr uint32_t B_BYTES = BNT * kBK;
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
   constexpr uint32_t TMEM_COLS = (BNT <= 32) ? 32 : (BNT <= 64) ? 64 : (BNT <= 128) ? 128 : 256;
-  constexpr uint32_t IDESC = idesc_f32acc(kBM, BNT, 0u);
+  constexpr uint32_t IDESC = idesc_f32acc(kBM, BNT, kBf16 ? 1u : 0u);
+  constexpr int ES = kBf16 ? 2 : 1;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align<1024>(smem_raw);
@@ -251,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n0 = blockIdx.x * kBM;
   const int split = blockIdx.y;
-  const int kblocks = (K + kBK - 1) / kBK;
+  const int kblocks = (K * ES + kBK - 1) / kBK;
   const int kb0 = split * kb_per_split;
   const int kb1 = min(kblocks, kb0 + kb_per_split);
 
@@ -291,8 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint8_t* sA = smem + stage * STAGE_BYTES;
         mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
-        tma_load_2d(sA, &tmW, &ctl->full[stage], kb * kBK, n0);
-        tma_load_2d(sA + A_BYTES, &tmX, &ctl->full[stage], kb * kBK, 0);
+        tma_load_2d(sA, &tmW, &ctl->full[stage], kb * (kBK / ES), n0);
+        tma_load_2d(sA + A_BYTES, &tmX, &ctl->full[stage], kb * (kBK / ES), 0);
         issued[stage] = true;
         issued_phase[stage] = phase;
         if (++stage == STAGES) stage = 0, phase ^= 1u;
@@ -318,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t bdesc = desc_kmajor_sw128(a_addr + A_BYTES);
 #pragma unroll
         for (int k = 0; k < kBK / 32; ++k)
-          mma_f8f6f4(tmem_base, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb != kb0) || (k != 0));
+          mma_k32b<kBf16>(tmem_base, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb != kb0) || (k != 0));
         mma_commit(&ctl->empty[stage]);
         if (++stage == STAGES) stage = 0, phase ^= 1u;
       }
@@ -413,15 +427,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Row-major [rows, K] e4m3 matrix, box of box_rows x 128 bytes, 128B swizzle.
-cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows) {
+// Row-major [rows, K] matrix of e4m3 codes (es = 1) or bf16 values (es = 2),
+// box of box_rows x 128 bytes, 128B swizzle.
+cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K, int box_rows, int es) {
   auto fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * es};
+  cuuint32_t box[2] = {(cuuint32_t)(kBK / es), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+  const CUtensorMapDataType dt = es == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -434,30 +450,32 @@ cudaError_t set_smem(Kern k, size_t bytes) {
   return ensure_smem_optin(reinterpret_cast<const void*>(k), (int)bytes);
 }
 
-template <int BN, int STAGES>
-cudaError_t launch_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
+template <int BN, int STAGES, bool kBf16>
+cudaError_t launch_big(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, int* err,
                        cudaStream_t st) {
   CUtensorMap ta, tb;
   cudaError_t e;
-  if ((e = make_map(&ta, A, M, K, kBM)) != cudaSuccess) return e;
-  if ((e = make_map(&tb, B, N, K, BN)) != cudaSuccess) return e;
+  constexpr int es = kBf16 ? 2 : 1;
+  if ((e = make_map(&ta, A, M, K, kBM, es)) != cudaSuccess) return e;
+  if ((e = make_map(&tb, B, N, K, BN, es)) != cudaSuccess) return e;
   const size_t smem = 1024 + (size_t)STAGES * (kBM + BN) * kBK + sizeof(Ctl);
-  auto k = k_gemm_fp8_tc<BN, STAGES>;
+  auto k = k_gemm_tc<BN, STAGES, kBf16>;
   if ((e = set_smem(k, smem)) != cudaSuccess) return e;
   const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, ta, tb, y, M, N, K, scale, err);
 }
 
-template <int BNT, int STAGES>
-cudaError_t launch_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, float* partial, int Mtok, int N, int K,
+template <int BNT, int STAGES, bool kBf16>
+cudaError_t launch_skinny(const void* X, const void* W, uint16_t* y, float* partial, int Mtok, int N, int K,
                           int splits, int kps, float scale, int* err, cudaStream_t st) {
   CUtensorMap tw, tx;
   cudaError_t e;
-  if ((e = make_map(&tw, W, N, K, kBM)) != cudaSuccess) return e;
-  if ((e = make_map(&tx, X, Mtok, K, BNT)) != cudaSuccess) return e;
+  constexpr int es = kBf16 ? 2 : 1;
+  if ((e = make_map(&tw, W, N, K, kBM, es)) != cudaSuccess) return e;
+  if ((e = make_map(&tx, X, Mtok, K, BNT, es)) != cudaSuccess) return e;
   const size_t smem = 1024 + (size_t)STAGES * (kBM + BNT) * kBK + sizeof(Ctl);
-  auto k = k_gemm_fp8_tc_skinny<BNT, STAGES>;
+  auto k = k_gemm_tc_skinny<BNT, STAGES, kBf16>;
   if ((e = set_smem(k, smem)) != cudaSuccess) return e;
   dim3 grid((N + kBM - 1) / kBM, splits);
   return launch_pdl(k, grid, dim3(kThreads), smem, st, tw, tx, y, splits > 1 ? partial : nullptr, Mtok, N, K, kps,
@@ -466,12 +484,12 @@ cudaError_t launch_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, float
 
 }  // namespace
 
-// Split plan of the skinny GEMM for (Mtok, N, K): splits and k-blocks each.
-// All CTAs fit in one wave (CTAs per SM from the shared-memory footprint) and
-// each split streams at least 4 k-blocks, so the f32 partials stay small next
-// to the weights.
-void skinny_plan(int Mtok, int N, int K, int* splits, int* kps) {
-  const int kblocks = (K + kBK - 1) / kBK;
+// Split plan of the skinny GEMM for (Mtok, N, Kbytes = K x operand size):
+// splits and k-blocks each.  All CTAs fit in one wave (CTAs per SM from the
+// shared-memory footprint) and each split streams at least 4 k-blocks, so the
+// f32 partials stay small next to the weights.
+void skinny_plan(int Mtok, int N, int Kbytes, int* splits, int* kps) {
+  const int kblocks = (Kbytes + kBK - 1) / kBK;
   const int nt = (N + kBM - 1) / kBM;
   const int bnt = (Mtok + 15) / 16 * 16;
   const int stages = bnt <= 64 ? 4 : (bnt <= 128 ? 3 : 2);   // 2 CTAs per SM from 32 rows up
@@ -488,25 +506,28 @@ void skinny_plan(int Mtok, int N, int K, int* splits, int* kps) {
   *kps = per;
 }
 
-size_t gemm_tc_skinny_workspace(int Mtok, int N, int K) {
+size_t gemm_tc_skinny_workspace(int Mtok, int N, int Kbytes) {
   int s, kps;
-  skinny_plan(Mtok, N, K, &s, &kps);
+  skinny_plan(Mtok, N, Kbytes, &s, &kps);
   return s > 1 ? (size_t)s * Mtok * N * sizeof(float) : 0;
 }
 
-cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
-                           void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches) {
+namespace {
+
+template <bool kBf16>
+cudaError_t skinny_t(const void* X, const void* W, uint16_t* y, int Mtok, int N, int K, float scale, void* ws,
+                     size_t ws_bytes, int* err, cudaStream_t st, int* launches) {
   int splits, kps;
-  skinny_plan(Mtok, N, K, &splits, &kps);
+  skinny_plan(Mtok, N, K * (kBf16 ? 2 : 1), &splits, &kps);
   float* partial = static_cast<float*>(ws);
   if (splits > 1 && (!ws || ws_bytes < (size_t)splits * Mtok * N * sizeof(float))) return cudaErrorInvalidValue;
   const int bnt = (Mtok + 15) / 16 * 16;
   cudaError_t e;
-  if (bnt <= 16) e = launch_skinny<16, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
-  else if (bnt <= 32) e = launch_skinny<32, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
-  else if (bnt <= 64) e = launch_skinny<64, 4>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
-  else if (bnt <= 128) e = launch_skinny<128, 3>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
-  else if (bnt <= 256) e = launch_skinny<256, 2>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  if (bnt <= 16) e = launch_skinny<16, 4, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 32) e = launch_skinny<32, 4, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 64) e = launch_skinny<64, 4, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 128) e = launch_skinny<128, 3, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 256) e = launch_skinny<256, 2, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
   else return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   *launches = 1;
@@ -522,12 +543,35 @@ cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int 
   return e;
 }
 
-cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
-                        cudaStream_t st) {
+template <bool kBf16>
+cudaError_t big_t(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, int* err,
+                  cudaStream_t st) {
   // Tile width: full 256-column tiles unless a narrower tile fills the last
   // wave better (N = 2688 = 14 x 192).
-  if (N % 192 == 0 && N % 256 != 0) return launch_big<192, 5>(A, B, y, M, N, K, scale, err, st);
-  return launch_big<256, 4>(A, B, y, M, N, K, scale, err, st);
+  if (N % 192 == 0 && N % 256 != 0) return launch_big<192, 5, kBf16>(A, B, y, M, N, K, scale, err, st);
+  return launch_big<256, 4, kBf16>(A, B, y, M, N, K, scale, err, st);
+}
+
+}  // namespace
+
+cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
+                           void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches) {
+  return skinny_t<false>(X, W, y, Mtok, N, K, scale, ws, ws_bytes, err, st, launches);
+}
+
+cudaError_t gemm_tc_skinny_bf16(const uint16_t* X, const uint16_t* W, uint16_t* y, int Mtok, int N, int K,
+                                float scale, void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches) {
+  return skinny_t<true>(X, W, y, Mtok, N, K, scale, ws, ws_bytes, err, st, launches);
+}
+
+cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
+                        cudaStream_t st) {
+  return big_t<false>(A, B, y, M, N, K, scale, err, st);
+}
+
+cudaError_t gemm_tc_big_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, int N, int K, float scale,
+                             int* err, cudaStream_t st) {
+  return big_t<true>(A, B, y, M, N, K, scale, err, st);
 }
 
 }  // namespace m2

@@ -86,6 +86,10 @@ struct m2_handle {
   uint8_t* in_proj = nullptr;
   uint8_t* out_proj = nullptr;
   float s_w1 = 0, s_w2 = 0;
+  // W8A16 arm: both projections dequantised to bf16 at creation
+  uint16_t* in_proj_bf16 = nullptr;
+  uint16_t* out_proj_bf16 = nullptr;
+  bool w8a16() const { return cfg.arm == M2_ARM_W8A16; }
   uint16_t* conv_w = nullptr;
   uint16_t* conv_b = nullptr;
   float* A_log = nullptr;
@@ -159,6 +163,8 @@ m2_status m2_create(const m2_config* cfg, const m2_weights* w, m2_handle** out) 
   if (cfg->chunk_size != kChunk) return fail(M2_ESHAPE, "m2_create: chunk_size %d is not 256", cfg->chunk_size);
   if (cfg->ssm_dtype != M2_DTYPE_F32 && cfg->ssm_dtype != M2_DTYPE_BF16)
     return fail(M2_EINVAL, "m2_create: ssm_dtype must be M2_DTYPE_F32 or M2_DTYPE_BF16");
+  if (cfg->arm != M2_ARM_W8A8 && cfg->arm != M2_ARM_W8A16)
+    return fail(M2_EINVAL, "m2_create: arm must be M2_ARM_W8A8 or M2_ARM_W8A16");
   if (!(cfg->eps > 0.f) || !(cfg->s_x > 0.f) || !(cfg->s_y > 0.f) || !(cfg->s_x < 3.0e38f) ||
       !(cfg->s_y < 3.0e38f))
     return fail(M2_EINVAL, "m2_create: eps and activation scales must be positive and finite");
@@ -187,6 +193,13 @@ m2_status m2_create(const m2_config* cfg, const m2_weights* w, m2_handle** out) 
   if (!s) s = upload(h, (void**)&h->D, w->D, kNH * 4);
   if (!s) s = upload(h, (void**)&h->dt_bias, w->dt_bias, kNH * 4);
   if (!s) s = upload(h, (void**)&h->norm_w, w->norm_w, (size_t)kI * 2);
+  if (!s && h->w8a16()) {
+    cudaError_t e = cudaMalloc((void**)&h->in_proj_bf16, (size_t)kZ * kH * 2);
+    if (e == cudaSuccess) e = cudaMalloc((void**)&h->out_proj_bf16, (size_t)kH * kI * 2);
+    if (e == cudaSuccess) e = launch_dequant_e4m3_bf16(h->in_proj, (size_t)kZ * kH, h->s_w1, h->in_proj_bf16, 0);
+    if (e == cudaSuccess) e = launch_dequant_e4m3_bf16(h->out_proj, (size_t)kH * kI, h->s_w2, h->out_proj_bf16, 0);
+    if (e != cudaSuccess) s = fail(M2_ECUDA, "m2_create: W8A16 weights: %s", cudaGetErrorString(e));
+  }
   if (!s) {
     cudaError_t e = cudaMalloc((void**)&h->err, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(h->err, 0, sizeof(int));
@@ -213,6 +226,8 @@ void m2_destroy(m2_handle* h) {
   cudaDeviceSynchronize();
   cudaFree(h->in_proj);
   cudaFree(h->out_proj);
+  cudaFree(h->in_proj_bf16);
+  cudaFree(h->out_proj_bf16);
   cudaFree(h->conv_w);
   cudaFree(h->conv_b);
   cudaFree(h->A_log);
@@ -325,15 +340,16 @@ struct PrefillWs {
   uint8_t* sin_img;
   uint16_t* y;
   uint8_t* q2;
+  uint16_t* o;   // W8A16 arm: the gated-norm output, out_proj's bf16 input
   void* gemm_ws;
   size_t gemm_ws_bytes;
   size_t total;
 };
 
-static PrefillWs carve_prefill(void* base, int T, int chunks) {
+static PrefillWs carve_prefill(void* base, int T, int chunks, bool w8a16) {
   Carve c{static_cast<char*>(base)};
   PrefillWs w;
-  w.q = c.take<uint8_t>((size_t)T * kH);
+  w.q = w8a16 ? nullptr : c.take<uint8_t>((size_t)T * kH);
   w.zx = c.take<uint16_t>((size_t)T * kZ);
   w.u = c.take<uint16_t>((size_t)T * kConv);
   w.cumdt = c.take<CumDt>((size_t)chunks * kNH);
@@ -341,7 +357,9 @@ static PrefillWs carve_prefill(void* base, int T, int chunks) {
   w.sin_img = c.take<uint8_t>((size_t)chunks * kNH * kSinImageBytes);
   w.y = c.take<uint16_t>((size_t)T * kI);
   w.q2 = c.take<uint8_t>((size_t)T * kI);
-  size_t g1 = gemm_workspace_bytes(T, kZ, kH), g2 = gemm_workspace_bytes(T, kH, kI);
+  w.o = w8a16 ? c.take<uint16_t>((size_t)T * kI) : nullptr;
+  size_t g1 = w8a16 ? gemm_workspace_bytes_bf16(T, kZ, kH) : gemm_workspace_bytes(T, kZ, kH);
+  size_t g2 = w8a16 ? gemm_workspace_bytes_bf16(T, kH, kI) : gemm_workspace_bytes(T, kH, kI);
   w.gemm_ws_bytes = g1 > g2 ? g1 : g2;
   w.gemm_ws = c.take<char>(w.gemm_ws_bytes);
   w.total = c.off;
@@ -353,7 +371,7 @@ m2_status m2_prefill_workspace_size(const m2_handle* h, const int32_t* seqlens_h
   SeqInfo si;
   m2_status s = build_seqinfo(seqlens_host, nseq, nullptr, &si);
   if (s) return s;
-  *bytes = carve_prefill(nullptr, si.total_tokens, si.total_chunks).total;
+  *bytes = carve_prefill(nullptr, si.total_tokens, si.total_chunks, h->w8a16()).total;
   return M2_OK;
 }
 
@@ -375,11 +393,14 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
   if ((uintptr_t)workspace % 256) return fail(M2_EINVAL, "m2_prefill: workspace must be 256-byte aligned");
   if ((uintptr_t)hidden % 16 || (uintptr_t)hidden_q % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_state % 16)
     return fail(M2_EINVAL, "m2_prefill: hidden, out and ssm_state must be 16-byte aligned");
+  if (hidden_q && h->w8a16())
+    return fail(M2_EINVAL, "m2_prefill_q: the W8A16 arm takes bf16 activations (input_scale is not applied)");
   SeqInfo local;
   m2_status s = build_seqinfo(seqlens_host, nseq, has_initial, &local);
   if (s) return s;
   const int T = local.total_tokens;
-  PrefillWs w = carve_prefill(workspace, T, local.total_chunks);
+  const bool w8a16 = h->w8a16();
+  PrefillWs w = carve_prefill(workspace, T, local.total_chunks, w8a16);
   if (ws_bytes < w.total)
     return fail(M2_ENOMEM, "m2_prefill: workspace %zu bytes < %zu needed", ws_bytes, w.total);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -388,9 +409,15 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
 
   int nl = 0;
   const uint8_t* q = hidden_q ? hidden_q : w.q;
-  if (!hidden_q)
-    M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
-  M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl, gemm_fp8(q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  if (w8a16) {
+    M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
+             gemm_bf16(hidden, h->in_proj_bf16, w.zx, T, kZ, kH, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  } else {
+    if (!hidden_q)
+      M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
+    M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
+             gemm_fp8(q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  }
   // the cumsum reads only the in_proj output: it runs on the second stream
   // beside the conv (serially while stage profiling)
   float* dt_tap = h->taps_on ? h->taps.dt : nullptr;
@@ -414,11 +441,23 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
                                  w.zx, conv_state, st));
   M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
            launch_ssd_chunk_scan_tc(w.u, w.cumdt, w.sin_img, bp, local, w.y, h->err, st));
-  M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
-           launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, h->taps_on ? h->taps.o : nullptr, st));
-  M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  if (w8a16) {
+    // the bf16 normed output feeds out_proj (the e4m3 codes are written too, unused)
+    M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, w.o, st));
+    M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl,
+             gemm_bf16(w.o, h->out_proj_bf16, out, T, kH, kI, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  } else {
+    M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
+             launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, h->taps_on ? h->taps.o : nullptr, st));
+    M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl,
+             gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  }
   if (h->taps_on) {
-    if ((s = copy_tap(h->taps.q, q, (size_t)T * kH, st))) return s;
+    if (w8a16) {
+      if ((s = copy_tap(h->taps.o, w.o, (size_t)T * kI * 2, st))) return s;
+    } else {
+      if ((s = copy_tap(h->taps.q, q, (size_t)T * kH, st))) return s;
+    }
     if ((s = copy_tap(h->taps.zx, w.zx, (size_t)T * kZ * 2, st))) return s;
     if ((s = copy_tap(h->taps.u, w.u, (size_t)T * kConv * 2, st))) return s;
     if ((s = copy_tap(h->taps.y, w.y, (size_t)T * kI * 2, st))) return s;
@@ -452,18 +491,21 @@ struct DecodeWs {
   uint8_t* q;
   uint16_t* zx;
   uint8_t* q2;
+  uint16_t* o;   // W8A16 arm: the gated-norm output, out_proj's bf16 input
   void* gemm_ws;
   size_t gemm_ws_bytes;
   size_t total;
 };
 
-static DecodeWs carve_decode(void* base, int Bt) {
+static DecodeWs carve_decode(void* base, int Bt, bool w8a16) {
   Carve c{static_cast<char*>(base)};
   DecodeWs w;
-  w.q = c.take<uint8_t>((size_t)Bt * kH);
+  w.q = w8a16 ? nullptr : c.take<uint8_t>((size_t)Bt * kH);
   w.zx = c.take<uint16_t>((size_t)Bt * kZ);
   w.q2 = c.take<uint8_t>((size_t)Bt * kI);
-  size_t g1 = gemm_workspace_bytes(Bt, kZ, kH), g2 = gemm_workspace_bytes(Bt, kH, kI);
+  w.o = w8a16 ? c.take<uint16_t>((size_t)Bt * kI) : nullptr;
+  size_t g1 = w8a16 ? gemm_workspace_bytes_bf16(Bt, kZ, kH) : gemm_workspace_bytes(Bt, kZ, kH);
+  size_t g2 = w8a16 ? gemm_workspace_bytes_bf16(Bt, kH, kI) : gemm_workspace_bytes(Bt, kH, kI);
   w.gemm_ws_bytes = g1 > g2 ? g1 : g2;
   w.gemm_ws = c.take<char>(w.gemm_ws_bytes);
   w.total = c.off;
@@ -473,7 +515,7 @@ static DecodeWs carve_decode(void* base, int Bt) {
 m2_status m2_decode_workspace_size(const m2_handle* h, int Bt, size_t* bytes) {
   if (!h || !bytes) return fail(M2_EINVAL, "m2_decode_workspace_size: null argument");
   if (Bt < 1 || Bt > 4096) return fail(M2_ESHAPE, "m2_decode: Bt %d not in [1, 4096]", Bt);
-  *bytes = carve_decode(nullptr, Bt).total;
+  *bytes = carve_decode(nullptr, Bt, h->w8a16()).total;
   return M2_OK;
 }
 
@@ -488,7 +530,10 @@ static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t
   if ((uintptr_t)workspace % 256) return fail(M2_EINVAL, "m2_decode: workspace must be 256-byte aligned");
   if ((uintptr_t)hidden % 16 || (uintptr_t)hidden_q % 16 || (uintptr_t)out % 16 || (uintptr_t)ssm_pool % 16)
     return fail(M2_EINVAL, "m2_decode: hidden, out and ssm_pool must be 16-byte aligned");
-  DecodeWs w = carve_decode(workspace, Bt);
+  if (hidden_q && h->w8a16())
+    return fail(M2_EINVAL, "m2_decode_q: the W8A16 arm takes bf16 activations (input_scale is not applied)");
+  const bool w8a16 = h->w8a16();
+  DecodeWs w = carve_decode(workspace, Bt, w8a16);
   if (ws_bytes < w.total) return fail(M2_ENOMEM, "m2_decode: workspace %zu bytes < %zu needed", ws_bytes, w.total);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const BlockParams bp = h->params();
@@ -502,16 +547,36 @@ static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t
   }
   int nl = 0;
   const uint8_t* q = hidden_q ? hidden_q : w.q;
-  if (!hidden_q)
-    M2_STAGE(h, st, M2_STAGE_DEC_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)Bt * kH, h->cfg.s_x, w.q, st));
-  M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl, gemm_fp8(q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  if (w8a16) {
+    M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl,
+             gemm_bf16(hidden, h->in_proj_bf16, w.zx, Bt, kZ, kH, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+    // the kernel writes the bf16 normed rows through its o output, which
+    // skips padding rows: those stay zero, so their output rows are zero
+    M2_CUDA(cudaMemsetAsync(w.o, 0, (size_t)Bt * kI * 2, st));
+    dt.o = w.o;
+  } else {
+    if (!hidden_q)
+      M2_STAGE(h, st, M2_STAGE_DEC_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)Bt * kH, h->cfg.s_x, w.q, st));
+    M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl,
+             gemm_fp8(q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  }
   M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
            launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, h->cfg.ssm_dtype == M2_DTYPE_BF16, n_slots, slot_idx,
                                 Bt, w.q2, h->err, dt, st));
-  M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl, gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  if (w8a16) {
+    M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl,
+             gemm_bf16(w.o, h->out_proj_bf16, out, Bt, kH, kI, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  } else {
+    M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl,
+             gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  }
   if (h->taps_on) {
     m2_status s;
-    if ((s = copy_tap(h->taps.q, q, (size_t)Bt * kH, st))) return s;
+    if (w8a16) {
+      if ((s = copy_tap(h->taps.o, w.o, (size_t)Bt * kI * 2, st))) return s;
+    } else {
+      if ((s = copy_tap(h->taps.q, q, (size_t)Bt * kH, st))) return s;
+    }
     if ((s = copy_tap(h->taps.zx, w.zx, (size_t)Bt * kZ * 2, st))) return s;
     if ((s = copy_tap(h->taps.q2, w.q2, (size_t)Bt * kI, st))) return s;
   }
@@ -576,6 +641,7 @@ static MixedWs carve_mixed(void* base, int Bt, int T, int chunks) {
 m2_status m2_mixed_workspace_size(const m2_handle* h, int Bt, const int32_t* seqlens_host, int nseq,
                                   size_t* bytes) {
   if (!h || !bytes) return fail(M2_EINVAL, "m2_mixed_workspace_size: null argument");
+  if (h->w8a16()) return fail(M2_EINVAL, "m2_mixed: not offered for the W8A16 arm (use m2_prefill and m2_decode)");
   if (Bt < 0 || Bt > 4096) return fail(M2_ESHAPE, "m2_mixed: Bt %d not in [0, 4096]", Bt);
   SeqInfo si;
   memset(&si, 0, sizeof si);
@@ -596,6 +662,7 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
                    void* stream) {
   g_err.clear();
   if (!h || !hidden || !out || !workspace) return fail(M2_EINVAL, "m2_mixed: null argument");
+  if (h->w8a16()) return fail(M2_EINVAL, "m2_mixed: not offered for the W8A16 arm (use m2_prefill and m2_decode)");
   if (Bt < 0 || Bt > 4096) return fail(M2_ESHAPE, "m2_mixed: Bt %d not in [0, 4096]", Bt);
   if (nseq < 0) return fail(M2_ESHAPE, "m2_mixed: nseq %d < 0", nseq);
   if (Bt > 0 && (!conv_pool || !ssm_pool || !slot_idx || n_slots < 1))
@@ -745,6 +812,44 @@ m2_status fp8_linear_bf16(const uint16_t* x, float s_a, const uint8_t* w_q, floa
   M2_CUDA(launch_quant_e4m3(x, (size_t)M * K, s_a, q, st));
   int nl = 0;
   M2_CUDA(gemm_fp8(q, w_q, y, M, N, K, s_a * s_w, static_cast<char*>(workspace) + qbytes, ws_bytes - qbytes, nullptr, st, &nl));
+  return M2_OK;
+}
+
+m2_status fp8_dequant(const uint8_t* q, size_t n, float scale, uint16_t* out, void* stream) {
+  g_err.clear();
+  if ((!q || !out) && n) return fail(M2_EINVAL, "fp8_dequant: null pointer");
+  if ((uintptr_t)q % 8 || (uintptr_t)out % 16)
+    return fail(M2_EINVAL, "fp8_dequant: q must be 8-byte and out 16-byte aligned");
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return fail(M2_EINVAL, "fp8_dequant: scale must be positive and finite");
+  m2_status s = check_device();
+  if (s) return s;
+  M2_CUDA(launch_dequant_e4m3_bf16(q, n, scale, out, static_cast<cudaStream_t>(stream)));
+  return M2_OK;
+}
+
+m2_status bf16_linear_workspace_size(int M, int N, int K, size_t* bytes) {
+  if (!bytes) return fail(M2_EINVAL, "bf16_linear_workspace_size: null argument");
+  if (M < 0 || N < 1 || K < 16 || K % 16) return fail(M2_ESHAPE, "bf16_linear_workspace_size: bad shape");
+  *bytes = gemm_workspace_bytes_bf16(M, N, K);
+  return M2_OK;
+}
+
+m2_status bf16_linear(const uint16_t* x, const uint16_t* w, float scale, uint16_t* y, int M, int N, int K,
+                      void* workspace, size_t ws_bytes, void* stream) {
+  g_err.clear();
+  if (M < 0 || N < 1 || K < 16) return fail(M2_ESHAPE, "bf16_linear: M %d, N %d, K %d out of range", M, N, K);
+  if (K % 16) return fail(M2_ESHAPE, "bf16_linear: K %d must be a multiple of 16", K);
+  if (M && (!x || !w || !y)) return fail(M2_EINVAL, "bf16_linear: null pointer");
+  if ((uintptr_t)x % 16 || (uintptr_t)w % 16 || (uintptr_t)y % 16)
+    return fail(M2_EINVAL, "bf16_linear: pointers must be 16-byte aligned");
+  if (!(scale > 0.f) || !(scale < 3.0e38f)) return fail(M2_EINVAL, "bf16_linear: scale must be positive and finite");
+  m2_status s = check_device();
+  if (s) return s;
+  const size_t need = gemm_workspace_bytes_bf16(M, N, K);
+  if (ws_bytes < need || (need && !workspace))
+    return fail(M2_ENOMEM, "bf16_linear: workspace %zu bytes < %zu needed", ws_bytes, need);
+  int nl = 0;
+  M2_CUDA(gemm_bf16(x, w, y, M, N, K, scale, workspace, ws_bytes, nullptr, static_cast<cudaStream_t>(stream), &nl));
   return M2_OK;
 }
 

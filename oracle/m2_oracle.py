@@ -122,6 +122,33 @@ def fp8_linear(a_q, s_a: float, w_q, s_w: float) -> np.ndarray:
     return bf16_round(float(s_a) * float(s_w) * acc)
 
 
+def dequant_e4m3_bf16(w_q, s_w: float) -> np.ndarray:
+    """Weight dequantisation of the W8A16 arm: w = bf16(dec(W) * s_w).
+
+    PR #1289, commit "the FP8 W8A8 seam": the host arm's DenseBf16 expands the
+    fp8 weights into a bf16 buffer: each code's value times the tensor's
+    per-tensor weight_scale.  The pages do not say in
+    what precision the product is formed; the reading taken here: the
+    product is rounded to float32 (nearest even), then to bf16 (nearest even).
+    dec(W) has at most 4 significant bits and s_w (a float32) 24, so the
+    float64 product below is exact before those two roundings.
+    """
+    return bf16_round(f32(e4m3_decode(w_q) * float(np.float32(s_w))))
+
+
+def bf16_linear(x, w) -> np.ndarray:
+    """W8A16 linear layer: y = bf16(x @ w^T) for bf16 activations x [M, K] and
+    dequantised bf16 weights w [N, K] ([out, in]).
+
+    PR #1288, section "The comparison is not bit-comparable, and that is the
+    point": the host reference carries input_scale and does not apply it, so
+    the activation enters the product as it is; PR #1289, GB10
+    counter-measurement commit: the dequantised weights go to a plain matmul
+    (vt::MatmulBT).  Exact accumulation (float64), output bf16.
+    """
+    return bf16_round(np.asarray(x, np.float64) @ np.asarray(w, np.float64).T)
+
+
 def silu(v):
     v = np.asarray(v, dtype=np.float64)
     return v / (1.0 + np.exp(-v))
@@ -264,7 +291,7 @@ def _dims(Wt):
     return g.hidden, g.d_inner, g.nheads, g.headdim, g.n_groups, g.d_state, g.conv_width
 
 
-def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False, map_fn=None):
+def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False, map_fn=None, arm="w8a8"):
     """Run the mixer block over packed sequences with carried states.
 
     hidden: [sum(T), H] bf16 values.  conv_state: [nseq, conv_dim, W-1];
@@ -274,12 +301,21 @@ def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False, map_fn=
     Returns dict with out [sum(T), H] (bf16 values), conv_state, ssm_state
     (final, per sequence) and, when keep=True, the intermediates.  map_fn, if
     given, runs the recurrence group by group through it (ssd_by_group).
+    arm: "w8a8" (the device arm: both projections fp8_linear on e4m3
+    activations) or "w8a16" (the host reference arm: bf16 activations
+    against dequantised bf16 weights, bf16_linear); everything between the
+    projections is the same.
     """
+    assert arm in ("w8a8", "w8a16")
     H, I, nh, P, G, N, W = _dims(Wt)
     conv_dim = I + 2 * G * N
     hidden = np.asarray(hidden, np.float64)
-    q = quant_static_e4m3(hidden, Wt["s_x"])
-    zx = fp8_linear(q, Wt["s_x"], Wt["in_proj"], Wt["s_w1"])
+    if arm == "w8a16":
+        q = None
+        zx = bf16_linear(hidden, dequant_e4m3_bf16(Wt["in_proj"], Wt["s_w1"]))
+    else:
+        q = quant_static_e4m3(hidden, Wt["s_x"])
+        zx = fp8_linear(q, Wt["s_x"], Wt["in_proj"], Wt["s_w1"])
     z, xbc, dt_raw = split_zxbcdt(zx, I, conv_dim, nh)
     A = -np.exp(np.asarray(Wt["A_log"], np.float64))
     dt = softplus(dt_raw + np.asarray(Wt["dt_bias"], np.float64)[None, :])
@@ -303,8 +339,12 @@ def block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=False, map_fn=
         y[sl] = bf16_round(ys.reshape(T, I))
         start += T
     o = bf16_round(gated_rmsnorm_group(y, z, Wt["norm_w"], G, Wt["eps"]))
-    q2 = quant_static_e4m3(o, Wt["s_y"])
-    out = fp8_linear(q2, Wt["s_y"], Wt["out_proj"], Wt["s_w2"])
+    if arm == "w8a16":
+        q2 = None
+        out = bf16_linear(o, dequant_e4m3_bf16(Wt["out_proj"], Wt["s_w2"]))
+    else:
+        q2 = quant_static_e4m3(o, Wt["s_y"])
+        out = fp8_linear(q2, Wt["s_y"], Wt["out_proj"], Wt["s_w2"])
     res = dict(out=out, conv_state=conv_out, ssm_state=ssm_out)
     if keep:
         res.update(q=q, zx=zx, u=u, dt=dt, y=y, o=o, q2=q2)
@@ -321,21 +361,22 @@ def _store_state(s, state_cache):
 
 
 def block_prefill(Wt, hidden, seqlens, conv_state=None, ssm_state=None, keep=False, map_fn=None,
-                  state_cache="f32"):
+                  state_cache="f32", arm="w8a8"):
     """Prefill of packed sequences; missing states mean fresh sequences.
-    state_cache: "f32" or "bf16" (the final ssm states are rounded to bf16)."""
+    state_cache: "f32" or "bf16" (the final ssm states are rounded to bf16);
+    arm: "w8a8" or "w8a16" (block_tokens)."""
     H, I, nh, P, G, N, W = _dims(Wt)
     nseq = len(seqlens)
     if conv_state is None:
         conv_state = np.zeros((nseq, I + 2 * G * N, W - 1))
     if ssm_state is None:
         ssm_state = np.zeros((nseq, nh, P, N))
-    res = block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=keep, map_fn=map_fn)
+    res = block_tokens(Wt, hidden, seqlens, conv_state, ssm_state, keep=keep, map_fn=map_fn, arm=arm)
     res["ssm_state"] = _store_state(res["ssm_state"], state_cache)
     return res
 
 
-def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False, state_cache="f32"):
+def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False, state_cache="f32", arm="w8a8"):
     """One decode token per row, states gathered from a slot pool.
 
     Row b reads pool[slot_idx[b]] (decode rows always have prior state,
@@ -347,7 +388,8 @@ def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False, state_ca
     ssm_rows (the new pool contents at slot_idx[live])).  Inputs are not
     modified.  state_cache "bf16": the pool rows are bf16 values, widened
     exactly when read; y uses the advanced state in full precision, and the
-    rows written back are rounded to bf16.
+    rows written back are rounded to bf16.  arm: "w8a8" or "w8a16"
+    (block_tokens).
     """
     slot_idx = np.asarray(slot_idx)
     live = np.nonzero(slot_idx >= 0)[0]
@@ -358,7 +400,7 @@ def block_decode(Wt, hidden, conv_pool, ssm_pool, slot_idx, keep=False, state_ca
         rows = slot_idx[live]
         r = block_tokens(Wt, np.asarray(hidden, np.float64)[live], [1] * len(live),
                          np.asarray(conv_pool[rows], np.float64),
-                         np.asarray(ssm_pool[rows], np.float64), keep=keep)
+                         np.asarray(ssm_pool[rows], np.float64), keep=keep, arm=arm)
         out[live] = r["out"]
         res["conv_rows"] = r["conv_state"]
         res["ssm_rows"] = _store_state(r["ssm_state"], state_cache)

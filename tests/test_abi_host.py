@@ -113,3 +113,29 @@ def test_standalone_ops_refuse_bad_arguments(m2):
     n = ctypes.c_size_t()
     assert m2._lib.fp8_linear_workspace_size(8, 8, 20, ctypes.byref(n)) == m2.M2_ESHAPE
     assert m2._lib.fp8_linear_workspace_size(8, 10304, 2688, ctypes.byref(n)) == m2.M2_OK
+
+
+@pytest.mark.parametrize("arm", [2, -1, 16])
+def test_create_refuses_unknown_arm(m2, arm):
+    """The projections run W8A8 (the device arm) or W8A16 (the host reference
+    arm, input_scale carried and not applied); any other code is refused."""
+    w, _keep = _weights(m2)
+    h = ctypes.c_void_p()
+    st = m2._lib.m2_create(ctypes.byref(_cfg(m2, arm=arm)), ctypes.byref(w), ctypes.byref(h))
+    assert st == m2.M2_EINVAL and "arm" in m2.last_error() and not h.value
+
+
+def test_w8a16_ops_refuse_bad_arguments(m2):
+    assert m2._lib.fp8_dequant(None, 16, 1.0, None, None) == m2.M2_EINVAL
+    assert m2._lib.fp8_dequant(16, 16, 0.0, 16, None) == m2.M2_EINVAL
+    assert m2._lib.fp8_dequant(8, 16, 1.0, 24, None) == m2.M2_EINVAL       # out not 16-byte aligned
+    assert m2._lib.bf16_linear(None, None, 1.0, None, 4, 4, 24, None, 0, None) == m2.M2_ESHAPE
+    assert m2._lib.bf16_linear(None, None, 1.0, None, 4, 4, 32, None, 0, None) == m2.M2_EINVAL
+    assert m2._lib.bf16_linear(16, 16, 0.0, 16, 4, 4, 32, None, 0, None) == m2.M2_EINVAL
+    n, n8 = ctypes.c_size_t(), ctypes.c_size_t()
+    assert m2._lib.bf16_linear_workspace_size(8, 8, 20, ctypes.byref(n)) == m2.M2_ESHAPE
+    # split-K partials of a decode-sized problem: f32 [splits, M, N]
+    assert m2._lib.bf16_linear_workspace_size(64, 10304, 2688, ctypes.byref(n)) == m2.M2_OK
+    assert m2._lib.fp8_linear_workspace_size(64, 10304, 2688, ctypes.byref(n8)) == m2.M2_OK
+    assert n.value % (64 * 10304 * 4) == 0 and n8.value % (64 * 10304 * 4) == 0
+    assert m2._lib.bf16_linear_workspace_size(4096, 10304, 2688, ctypes.byref(n)) == m2.M2_OK and n.value == 0

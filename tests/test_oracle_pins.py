@@ -581,3 +581,128 @@ def test_bf16_state_cache_prefill_final_state(tiny_weights):
     b = oracle.block_prefill(Wt, h, [9], state_cache="bf16")
     np.testing.assert_array_equal(a["out"], b["out"])
     np.testing.assert_array_equal(b["ssm_state"], oracle.bf16_round(a["ssm_state"]))
+
+
+# ---------------------------------------------------------------- W8A16 arm
+
+def test_dequant_power_of_two_scale_is_exact():
+    """With a power-of-two weight scale the dequantised weight is the code's
+    value (the published OCP table) times the scale, exactly."""
+    rows = [(c, v) for c, v in _golden_e4m3() if not math.isnan(v)]
+    codes = np.array([c for c, _ in rows], np.uint8)
+    vals = np.array([v for _, v in rows])
+    for k in (-9, -3, 0, 2):
+        got = oracle.dequant_e4m3_bf16(codes, 2.0 ** k)
+        assert np.array_equal(got, vals * 2.0 ** k), k
+
+
+@pytest.mark.parametrize("scale", [0.0123 / 448, 1.7e-4, 3.3, 0.02 / 448 * 3.7])
+def test_dequant_matches_torch_float32_product(scale):
+    """The reading taken: product in float32, then bf16 (both nearest even).
+    torch does the same two roundings with its own kernels."""
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]
+    t = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32) * torch.tensor(scale, dtype=torch.float32)
+    ref = t.to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.dequant_e4m3_bf16(codes, scale)
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_linear_integer_valued_is_exact():
+    rng = np.random.default_rng(21)
+    x_i = rng.integers(-8, 9, (9, 2688))
+    w_i = rng.integers(-8, 9, (40, 2688))
+    exact = x_i.astype(np.int64) @ w_i.astype(np.int64).T
+    ref = torch.from_numpy(exact.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.abs(exact).max() < 2 ** 24
+    assert np.array_equal(oracle.bf16_linear(x_i.astype(np.float64), w_i.astype(np.float64)), ref)
+
+
+def test_bf16_linear_orientation_vs_torch():
+    rng = np.random.default_rng(22)
+    x = oracle.bf16_round(rng.standard_normal((5, 64)))
+    w = oracle.bf16_round(rng.standard_normal((7, 64)) * 0.02)
+    ref = torch.nn.functional.linear(torch.from_numpy(x), torch.from_numpy(w)).numpy()
+    got = oracle.bf16_linear(x, w)
+    assert got.shape == (5, 7)
+    np.testing.assert_allclose(got, ref, rtol=2 ** -8, atol=0)
+
+
+def _pow2_scales(Wt, s_w1=2.0 ** -6, s_w2=2.0 ** -5):
+    W = dict(Wt)
+    W["s_w1"], W["s_w2"] = s_w1, s_w2
+    return W
+
+
+def test_w8a16_in_proj_on_grid_equals_w8a8(tiny_weights):
+    """Activations already on the e4m3 grid (times s_x) and power-of-two
+    weight scales: quantising changes nothing and dequantising is exact, so
+    the two arms' in_proj outputs are the same bf16 values."""
+    Wt = _pow2_scales(tiny_weights)
+    rng = np.random.default_rng(94)
+    codes = rng.integers(0, 256, (6, TINY.hidden)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0
+    h = oracle.e4m3_decode(codes) * Wt["s_x"]
+    a = oracle.block_prefill(Wt, h, [6], keep=True, arm="w8a8")
+    b = oracle.block_prefill(Wt, h, [6], keep=True, arm="w8a16")
+    assert np.array_equal(a["zx"], b["zx"])
+    assert b["q"] is None and b["q2"] is None
+
+
+def test_w8a16_activation_is_not_quantised(tiny_weights):
+    """A one-hot input row far outside the e4m3 range: the W8A16 in_proj row
+    is that value times one dequantised weight column (a single product,
+    rounded once to bf16); the W8A8 arm saturates it at 448 s_x instead."""
+    Wt = tiny_weights
+    k, v = 5, 1000.3 * Wt["s_x"]
+    h = np.zeros((1, TINY.hidden))
+    h[0, k] = v
+    b = oracle.block_prefill(Wt, h, [1], keep=True, arm="w8a16")
+    col = oracle.dequant_e4m3_bf16(Wt["in_proj"][:, k], Wt["s_w1"])
+    assert np.array_equal(b["zx"][0], oracle.bf16_round(v * col))
+    a = oracle.block_prefill(Wt, h, [1], keep=True, arm="w8a8")
+    assert np.array_equal(a["zx"][0], oracle.bf16_round(448.0 * Wt["s_x"] * Wt["s_w1"]
+                                                       * oracle.e4m3_decode(Wt["in_proj"][:, k])))
+    assert not np.array_equal(a["zx"], b["zx"])
+
+
+def test_w8a16_decode_after_prefill_equals_longer_prefill(tiny_weights):
+    Wt = tiny_weights
+    T, t0 = 10, 6
+    h = synth.make_hidden(95, T, TINY)
+    full = oracle.block_prefill(Wt, h, [T], arm="w8a16")
+    part = oracle.block_prefill(Wt, h[:t0], [t0], arm="w8a16")
+    conv_pool, ssm_pool = part["conv_state"].copy(), part["ssm_state"].copy()
+    outs = [part["out"]]
+    for t in range(t0, T):
+        r = oracle.block_decode(Wt, h[t:t + 1], conv_pool, ssm_pool, np.array([0]), arm="w8a16")
+        conv_pool[0], ssm_pool[0] = r["conv_rows"][0], r["ssm_rows"][0]
+        outs.append(r["out"])
+    np.testing.assert_allclose(np.concatenate(outs), full["out"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ssm_pool[0], full["ssm_state"][0], rtol=1e-10, atol=1e-13)
+
+
+def test_w8a16_and_w8a8_arms_separate_by_the_activation_quant(tiny_weights):
+    """The two arms are not bit-comparable: they differ by the e4m3
+    activation quantisation (a few percent), and by nothing larger."""
+    Wt = tiny_weights
+    h = synth.make_hidden(96, 12, TINY)
+    a = oracle.block_prefill(Wt, h, [12], arm="w8a8")["out"]
+    b = oracle.block_prefill(Wt, h, [12], arm="w8a16")["out"]
+    sep = np.linalg.norm(a - b) / np.linalg.norm(b)
+    assert 1e-3 < sep < 0.2, sep
+
+
+def test_dequant_rounds_through_float32_many_scales():
+    """Over a million (code, scale) products a few dozen land where rounding
+    the product to float32 first moves it onto a bf16 tie; torch's float32
+    multiply and bf16 conversion decide those the same way the oracle does."""
+    rng = np.random.default_rng(23)
+    scales = (10 ** rng.uniform(-5, -1, 4000)).astype(np.float32)
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]
+    t = (torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float32)[None, :]
+         * torch.from_numpy(scales)[:, None])
+    ref = t.to(torch.bfloat16).to(torch.float64).numpy()
+    got = np.stack([oracle.dequant_e4m3_bf16(codes, float(s)) for s in scales])
+    assert np.array_equal(got, ref)
