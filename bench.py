@@ -705,6 +705,96 @@ def run_decode_bf16(args):
                           "f32 vs bf16 SSM rows", launch="cuda_graph", results=res)))
 
 
+def run_arms(args):
+    """The two projection arms on the bench workload (decode 64 rows from the
+    256-slot pool, then prefill 4 x 2048 from zero state, as two calls: the
+    W8A16 arm has no mixed call), CUDA-graph replay, L2 flushed before each
+    step; per-arm step time and projection throughput against the measured
+    peak of the operand type.  Prints one JSON line (not the headline)."""
+    import torch
+
+    import mamba2_ssm_mixer_gb300 as m2
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    Wt = synth.make_weights(0)
+    w = dict(in_proj=torch.from_numpy(Wt["in_proj"]).to(dev), s_w1=Wt["s_w1"],
+             out_proj=torch.from_numpy(Wt["out_proj"]).to(dev), s_w2=Wt["s_w2"],
+             conv_w=torch.from_numpy(Wt["conv_w"]).to(torch.bfloat16).to(dev), conv_b=None,
+             A_log=torch.from_numpy(Wt["A_log"]).to(dev), D=torch.from_numpy(Wt["D"]).to(dev),
+             dt_bias=torch.from_numpy(Wt["dt_bias"]).to(dev),
+             norm_w=torch.from_numpy(Wt["norm_w"]).to(torch.bfloat16).to(dev),
+             s_x=Wt["s_x"], s_y=Wt["s_y"], eps=Wt["eps"])
+    pk = peaks() or {}
+    bf16_peak = pk.get("bf16_tflops_sustained")
+    fp8_peak = None
+    try:
+        fp8_peak = float(json.load(open(os.path.join(ROOT, "profiles", "fp8_gemm_peak.json")))["fp8_tflops_sustained"])
+    except Exception:
+        pass
+    res = {}
+    for name, arm in (("w8a8", m2.M2_ARM_W8A8), ("w8a16", m2.M2_ARM_W8A16)):
+        blk = m2.Mamba2Mixer(w, device=dev, arm=arm)
+        conv_pool = torch.from_numpy(synth.make_conv_state(2, N_SLOTS)).to(torch.bfloat16).to(dev)
+        ssm_pool = torch.from_numpy(synth.make_ssm_state(2, N_SLOTS)).to(dev)
+        slots = torch.from_numpy(synth.make_slot_idx(2, N_SLOTS, DEC_B)).to(dev)
+        h_dec = torch.from_numpy(synth.make_hidden(2, DEC_B)).to(torch.bfloat16).to(dev)
+        h_pf = torch.from_numpy(synth.make_hidden(3, T_PF)).to(torch.bfloat16).to(dev)
+        out_dec = torch.empty((DEC_B, H), dtype=torch.bfloat16, device=dev)
+        out_pf = torch.empty((T_PF, H), dtype=torch.bfloat16, device=dev)
+        conv_st = torch.zeros((len(SEQLENS), CONV, 3), dtype=torch.bfloat16, device=dev)
+        ssm_st = torch.zeros((len(SEQLENS), 64, 64, 128), dtype=torch.float32, device=dev)
+        ws_dec = torch.empty(blk.decode_workspace_size(DEC_B), dtype=torch.uint8, device=dev)
+        ws_pf = torch.empty(blk.prefill_workspace_size(SEQLENS), dtype=torch.uint8, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+        def run():
+            blk.decode(h_dec, conv_pool, ssm_pool, slots, out=out_dec, workspace=ws_dec)
+            blk.prefill(h_pf, SEQLENS, conv_st, ssm_st, out=out_pf, workspace=ws_pf)
+
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            run()
+        torch.cuda.current_stream(dev).wait_stream(cs)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            run()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(i & 0xFF)
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+        blk.profile(True)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            run()
+        torch.cuda.synchronize()
+        prof = blk.profile_read()
+        blk.profile(False)
+        blk.check()
+        st = {k: v[0] / args.steps for k, v in prof.items()}
+        peak = bf16_peak if name == "w8a16" else fp8_peak
+        proj = {}
+        for stage, flop in (("in_proj", 2.0 * T_PF * Z * H), ("out_proj", 2.0 * T_PF * H * I)):
+            tf = flop / (st[stage] * 1e-3) / 1e12
+            proj[stage] = dict(ms=st[stage], tflops=tf, peak=peak, frac=(tf / peak) if peak else None)
+        res[name] = dict(step_ms=ms, tokens_per_s=(DEC_B + T_PF) / (ms * 1e-3), prefill_projections=proj,
+                         stages_ms=st)
+        blk.close()
+    print(json.dumps(dict(case="arms_w8a8_vs_w8a16", workload=f"decode {DEC_B} rows from a {N_SLOTS}-slot pool, "
+                          f"then prefill {SEQLENS} from zero state (two calls)", launch="cuda_graph",
+                          peaks=dict(fp8_tflops="measured cuBLAS e4m3 sustained", bf16_tflops="measured sustained"),
+                          results=res)))
+
+
 def run_case(args):
     """One kernel family at its bench-workload shape, for profiler captures
     (ncu -k <kernel> -c <n>): --case in_proj | out_proj | decode | prefill."""
@@ -740,7 +830,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill", "stack", "decode_bf16"],
+    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill", "stack", "decode_bf16", "arms"],
                     default=None,
                     help="run one kernel family at the workload shape (for profiler captures); prints nothing")
     ap.add_argument("--measure-fp8-peak", action="store_true",
@@ -757,6 +847,8 @@ def main():
         run_stack(args)
     elif args.case == "decode_bf16":
         run_decode_bf16(args)
+    elif args.case == "arms":
+        run_arms(args)
     elif args.case:
         run_case(args)
     elif args.impl == "reference":
