@@ -156,3 +156,51 @@ def test_w8a16_refuses_prequantised_and_mixed_calls(block_w8a16):
     with pytest.raises(m2.M2Error) as e:
         blk.mixed_workspace_size(1, [4])
     assert e.value.status == m2.M2_EINVAL and "W8A16" in str(e.value)
+
+
+def test_w8a16_with_bf16_state_cache_carry():
+    """The two options together: the W8A16 arm over a bf16 state cache, prefill
+    then one-token decodes from the returned states (the carry case)."""
+    Wt = synth.make_weights(0)
+    blk = m2.Mamba2Mixer(device_weights(Wt), arm=m2.M2_ARM_W8A16, ssm_dtype=m2.M2_DTYPE_BF16)
+    T, t0 = 40, 33
+    h = synth.make_hidden(6, T)
+    conv = torch.zeros((1, 6144, 3), dtype=torch.bfloat16, device="cuda")
+    ssm = torch.zeros((1, 64, 64, 128), dtype=torch.bfloat16, device="cuda")
+    outs = [to_np(blk.prefill(bf16_dev(h[:t0]), [t0], conv, ssm))]
+    slot = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for t in range(t0, T):
+        outs.append(to_np(blk.decode(bf16_dev(h[t:t + 1]), conv, ssm, slot)))
+    torch.cuda.synchronize()
+    blk.check()
+    r = oracle.block_prefill(Wt, h[:t0], [t0], state_cache="bf16", arm="w8a16")
+    rc, rs, ro = r["conv_state"], r["ssm_state"], [r["out"]]
+    for t in range(t0, T):
+        d = oracle.block_decode(Wt, h[t:t + 1], rc, rs, np.array([0]), state_cache="bf16", arm="w8a16")
+        rc, rs = d["conv_rows"], d["ssm_rows"]
+        ro.append(d["out"])
+    assert_block_out(np.concatenate(outs), np.concatenate(ro))
+    assert_state(ssm.to(torch.float32).cpu().numpy()[0], rs[0])
+    blk.close()
+
+
+def test_w8a16_short_prefill_takes_the_few_row_gemm(block_w8a16):
+    """A prefill of at most 256 tokens runs both projections on the split-K
+    few-row kernel (bf16 operands); checked at the block level with taps."""
+    Wt, blk = block_w8a16
+    lens = [100, 20]
+    T = sum(lens)
+    h = synth.make_hidden(8, T)
+    conv = torch.zeros((2, 6144, 3), dtype=torch.bfloat16, device="cuda")
+    ssm = torch.zeros((2, 64, 64, 128), dtype=torch.float32, device="cuda")
+    taps = dict(zx=torch.empty((T, 10304), dtype=torch.bfloat16, device="cuda"))
+    blk.set_taps(**taps)
+    out = blk.prefill(bf16_dev(h), lens, conv, ssm)
+    blk.set_taps()
+    torch.cuda.synchronize()
+    blk.check()
+    ref = oracle.block_prefill(Wt, h, lens, keep=True, arm="w8a16")
+    wd = oracle.dequant_e4m3_bf16(Wt["in_proj"], Wt["s_w1"])
+    assert_bf16_close(to_np(taps["zx"]), ref["zx"], atol=2.0 ** -16 * (np.abs(h) @ np.abs(wd).T), what="zx")
+    assert_block_out(to_np(out), ref["out"])
+    assert_state(to_np(ssm), ref["ssm_state"])
