@@ -795,6 +795,119 @@ def run_arms(args):
                           results=res)))
 
 
+def run_configs(args):
+    """The single-block workloads one by one (W8A8 arm, f32 state rows), each
+    replayed from a CUDA graph with L2 flushed before every step:
+      0: prefill of one 32-token sequence from zero state;
+      1: decode of one row (its own conv and SSM state);
+      2: paged decode of 64 rows from a 256-slot pool;
+      3: prefill of 4 x 2048 tokens from zero state.
+    Per workload: time per call, tokens/s, launches, and the achieved rate
+    against its roof: algorithmic bytes (each fp8 weight once, each state row
+    read and written once, hidden in, output out) over HBM for 0-2, the
+    projections' FLOP over the measured e4m3 rate for 3.  Prints one JSON line
+    (not the headline)."""
+    import torch
+
+    import mamba2_ssm_mixer_gb300 as m2
+    import synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    Wt = synth.make_weights(0)
+    w = dict(in_proj=torch.from_numpy(Wt["in_proj"]).to(dev), s_w1=Wt["s_w1"],
+             out_proj=torch.from_numpy(Wt["out_proj"]).to(dev), s_w2=Wt["s_w2"],
+             conv_w=torch.from_numpy(Wt["conv_w"]).to(torch.bfloat16).to(dev), conv_b=None,
+             A_log=torch.from_numpy(Wt["A_log"]).to(dev), D=torch.from_numpy(Wt["D"]).to(dev),
+             dt_bias=torch.from_numpy(Wt["dt_bias"]).to(dev),
+             norm_w=torch.from_numpy(Wt["norm_w"]).to(torch.bfloat16).to(dev),
+             s_x=Wt["s_x"], s_y=Wt["s_y"], eps=Wt["eps"])
+    blk = m2.Mamba2Mixer(w, device=dev)
+    pk = peaks() or {}
+    hbm = pk.get("hbm_gbs")
+    fp8_peak = None
+    try:
+        fp8_peak = float(json.load(open(os.path.join(ROOT, "profiles", "fp8_gemm_peak.json")))["fp8_tflops_sustained"])
+    except Exception:
+        pass
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    W_BYTES = Z * H + H * I
+    STATE_ROW = 64 * 64 * 128 * 4
+    CONV_ROW = CONV * 3 * 2
+
+    def timed(run):
+        cs = torch.cuda.Stream(dev)
+        cs.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(cs):
+            run()
+        torch.cuda.current_stream(dev).wait_stream(cs)
+        torch.cuda.synchronize()
+        before = blk.stats()["kernel_launches"]
+        run()
+        torch.cuda.synchronize()
+        launches = blk.stats()["kernel_launches"] - before
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            run()
+        for _ in range(args.warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i, (a, b) in enumerate(ev):
+            flush.fill_(i & 0xFF)
+            a.record()
+            g.replay()
+            b.record()
+        torch.cuda.synchronize()
+        blk.check()
+        return sum(a.elapsed_time(b) for a, b in ev) / args.steps, launches
+
+    res = {}
+    # 0 and 3: prefill from zero state
+    for cfg, lens in ((0, [32]), (3, SEQLENS)):
+        T = sum(lens)
+        h = torch.from_numpy(synth.make_hidden(cfg, T)).to(torch.bfloat16).to(dev)
+        out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+        conv = torch.zeros((len(lens), CONV, 3), dtype=torch.bfloat16, device=dev)
+        ssm = torch.zeros((len(lens), 64, 64, 128), dtype=torch.float32, device=dev)
+        ws = torch.empty(blk.prefill_workspace_size(lens), dtype=torch.uint8, device=dev)
+        ms, nl = timed(lambda: blk.prefill(h, lens, conv, ssm, out=out, workspace=ws))
+        r = dict(workload=f"prefill {lens} from zero state", ms=ms, tokens_per_s=T / (ms * 1e-3), launches=nl)
+        if cfg == 0:
+            byts = W_BYTES + T * H * 2 * 2 + len(lens) * (STATE_ROW + CONV_ROW)
+            r.update(algorithmic_bytes=byts, gbs=byts / (ms * 1e-3) / 1e9,
+                     frac_of_hbm=(byts / (ms * 1e-3) / 1e9 / hbm) if hbm else None)
+        else:
+            flop = 2.0 * T * (Z * H + H * I)
+            blk.profile(True)
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                blk.prefill(h, lens, conv, ssm, out=out, workspace=ws)
+            torch.cuda.synchronize()
+            st = blk.profile_read()
+            blk.profile(False)
+            gemm_ms = (st["in_proj"][0] + st["out_proj"][0]) / args.steps
+            tf = flop / (gemm_ms * 1e-3) / 1e12
+            r.update(projection_flop=flop, projections_ms=gemm_ms, projections_tflops=tf,
+                     frac_of_fp8=(tf / fp8_peak) if fp8_peak else None)
+        res[str(cfg)] = r
+    # 1 and 2: decode
+    for cfg, n_slots, Bt in ((1, 1, 1), (2, N_SLOTS, DEC_B)):
+        conv_pool = torch.from_numpy(synth.make_conv_state(cfg, n_slots)).to(torch.bfloat16).to(dev)
+        ssm_pool = torch.from_numpy(synth.make_ssm_state(cfg, n_slots)).to(dev)
+        slots = torch.from_numpy(synth.make_slot_idx(cfg, n_slots, Bt)).to(dev)
+        h = torch.from_numpy(synth.make_hidden(cfg, Bt)).to(torch.bfloat16).to(dev)
+        out = torch.empty((Bt, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(blk.decode_workspace_size(Bt), dtype=torch.uint8, device=dev)
+        ms, nl = timed(lambda: blk.decode(h, conv_pool, ssm_pool, slots, out=out, workspace=ws))
+        byts = W_BYTES + Bt * (2 * STATE_ROW + 2 * CONV_ROW + 2 * H * 2)
+        res[str(cfg)] = dict(workload=f"decode {Bt} row(s) from a {n_slots}-slot pool", ms=ms,
+                             tokens_per_s=Bt / (ms * 1e-3), launches=nl, algorithmic_bytes=byts,
+                             gbs=byts / (ms * 1e-3) / 1e9, frac_of_hbm=(byts / (ms * 1e-3) / 1e9 / hbm) if hbm else None)
+    blk.close()
+    print(json.dumps(dict(case="configs", launch="cuda_graph", l2="flushed before each step",
+                          peaks=dict(hbm_gbs=hbm, fp8_tflops=fp8_peak), results=res)))
+
+
 def run_case(args):
     """One kernel family at its bench-workload shape, for profiler captures
     (ncu -k <kernel> -c <n>): --case in_proj | out_proj | decode | prefill."""
@@ -830,7 +943,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill", "stack", "decode_bf16", "arms"],
+    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill", "stack", "decode_bf16", "arms",
+                                       "configs"],
                     default=None,
                     help="run one kernel family at the workload shape (for profiler captures); prints nothing")
     ap.add_argument("--measure-fp8-peak", action="store_true",
@@ -849,6 +963,8 @@ def main():
         run_decode_bf16(args)
     elif args.case == "arms":
         run_arms(args)
+    elif args.case == "configs":
+        run_configs(args)
     elif args.case:
         run_case(args)
     elif args.impl == "reference":
