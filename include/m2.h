@@ -129,7 +129,7 @@ enum {
   M2_STAGE_QUANT_IN = 0,       /* static e4m3 quant of the block input     */
   M2_STAGE_IN_PROJ = 1,        /* W8A8 in_proj GEMM                        */
   M2_STAGE_CONV = 2,           /* prefill causal conv1d + SiLU             */
-  M2_STAGE_CONV_STATE = 3,     /* (unused: the hand-off runs in stage 4)   */
+  M2_STAGE_CONV_STATE = 3,     /* (unused: the hand-off runs in stage 6)   */
   M2_STAGE_SSD_CUMSUM = 4,     /* dt softplus and in-chunk log-decay sums  */
   M2_STAGE_SSD_CHUNK_STATE = 5,
   M2_STAGE_SSD_STATE_PASS = 6,

@@ -1,6 +1,6 @@
 // Memory-bound kernels of the mixer block: static e4m3 activation quant,
-// causal conv1d + SiLU (prefill; its state hand-off runs in the SSD cumsum
-// kernel, after every old window has been read), gated group RMSNorm
+// causal conv1d + SiLU (prefill; its state hand-off runs in the SSD state
+// pass, after every old window has been read), gated group RMSNorm
 // with the out_proj quant fused into its epilogue, and the residual RMSNorm
 // used between stacked blocks.
 #include "launch_util.h"
