@@ -492,9 +492,7 @@ void skinny_plan(int Mtok, int N, int Kbytes, int* splits, int* kps) {
   const int kblocks = (Kbytes + kBK - 1) / kBK;
   const int nt = (N + kBM - 1) / kBM;
   const int bnt = (Mtok + 15) / 16 * 16;
-  // up to 64 rows: one CTA per SM with an 8-deep ring (the whole K range of a
-  // weight block in flight in few round trips); above: 2 CTAs per SM
-  const int stages = bnt <= 64 ? 8 : (bnt <= 128 ? 3 : 2);
+  const int stages = bnt <= 64 ? 4 : (bnt <= 128 ? 3 : 2);   // 2 CTAs per SM from 32 rows up
   const int smem = 1024 + stages * (kBM + bnt) * kBK + 256;
   int per_sm = (228 * 1024) / (smem + 1024);
   if (per_sm < 1) per_sm = 1;
@@ -525,9 +523,9 @@ cudaError_t skinny_t(const void* X, const void* W, uint16_t* y, int Mtok, int N,
   if (splits > 1 && (!ws || ws_bytes < (size_t)splits * Mtok * N * sizeof(float))) return cudaErrorInvalidValue;
   const int bnt = (Mtok + 15) / 16 * 16;
   cudaError_t e;
-  if (bnt <= 16) e = launch_skinny<16, 8, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
-  else if (bnt <= 32) e = launch_skinny<32, 8, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
-  else if (bnt <= 64) e = launch_skinny<64, 8, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  if (bnt <= 16) e = launch_skinny<16, 4, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 32) e = launch_skinny<32, 4, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
+  else if (bnt <= 64) e = launch_skinny<64, 4, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
   else if (bnt <= 128) e = launch_skinny<128, 3, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
   else if (bnt <= 256) e = launch_skinny<256, 2, kBf16>(X, W, y, partial, Mtok, N, K, splits, kps, scale, err, st);
   else return cudaErrorInvalidValue;
