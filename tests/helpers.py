@@ -99,9 +99,21 @@ def assert_state(got, ref, what="ssm_state"):
     return rl
 
 
+# Near zero the e4m3 grid is uniform: codes 0-15 (subnormals and the lowest
+# binade) are 2^-9 apart, so an absolute difference of the quantised input
+# crosses several codes there.  The normed activation out_proj quantises
+# agrees with the oracle to ~2e-4 absolute at |o| ~ 1 (rel L2 2e-4), i.e.
+# ~3.3 steps of 2^-9 in units of o / s_y (s_y = 1/32); four steps are admitted.
+E4M3_NEAR_ZERO_STEPS = 4
+
+
 def assert_e4m3_close(got_codes, ref_codes, max_frac=2e-3, what="q2"):
     """Codes of an e4m3 quant whose bf16 input may differ by rounding between
-    the two sides: equal almost everywhere, and at most one code apart."""
+    the two sides: equal almost everywhere, and each differing pair either
+    adjacent (same sign, magnitude codes one apart, or +-0) or, near zero
+    where the grid spacing is absolute, within E4M3_NEAR_ZERO_STEPS steps of
+    2^-9 in value."""
+    import oracle
     g = np.asarray(got_codes).astype(np.int64)
     r = np.asarray(ref_codes).astype(np.int64)
     assert g.shape == r.shape and g.size > 0
@@ -109,10 +121,12 @@ def assert_e4m3_close(got_codes, ref_codes, max_frac=2e-3, what="q2"):
     frac = diff.mean()
     assert frac <= max_frac, f"{what}: {frac:.2e} of codes differ"
     if diff.any():
-        # same sign, adjacent magnitude codes (or +-0)
         gs, rs = g[diff], r[diff]
         mag_g, mag_r = gs & 0x7F, rs & 0x7F
-        assert np.all(np.abs(mag_g - mag_r) <= 1), f"{what}: codes more than one step apart"
+        adjacent = np.abs(mag_g - mag_r) <= 1
+        vg, vr = oracle.e4m3_decode(gs.astype(np.uint8)), oracle.e4m3_decode(rs.astype(np.uint8))
+        near_zero = np.abs(vg - vr) <= E4M3_NEAR_ZERO_STEPS * 2.0 ** -9
+        assert np.all(adjacent | near_zero), f"{what}: codes more than one step apart"
 
 
 def assert_bf16_close(got, ref, max_frac=5e-3, atol=0.0, what="bf16"):
