@@ -139,3 +139,33 @@ def test_w8a16_ops_refuse_bad_arguments(m2):
     assert m2._lib.fp8_linear_workspace_size(64, 10304, 2688, ctypes.byref(n8)) == m2.M2_OK
     assert n.value % (64 * 10304 * 4) == 0 and n8.value % (64 * 10304 * 4) == 0
     assert m2._lib.bf16_linear_workspace_size(4096, 10304, 2688, ctypes.byref(n)) == m2.M2_OK and n.value == 0
+
+
+def _header_enum(prefix):
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    return {m.group(1): int(m.group(2)) for m in re.finditer(rf"\b({prefix}\w*)\s*=\s*(-?\d+)", src)}
+
+
+def test_binding_constants_match_the_header(m2):
+    """The binding's status codes, dtype and arm codes and stage names are the
+    header's, value for value (the binding is marshalling only)."""
+    for name, value in _header_enum("M2_E").items():
+        assert getattr(m2, name) == value, name
+    for prefix in ("M2_DTYPE_", "M2_ARM_", "M2_LAYOUT_"):
+        for name, value in _header_enum(prefix).items():
+            assert getattr(m2, name) == value, name
+    assert _header_enum("M2_OK") == {"M2_OK": m2.M2_OK}
+    stages = {k: v for k, v in _header_enum("M2_STAGE_").items()}
+    assert len(stages) == len(m2.STAGES)
+    for name, value in stages.items():
+        assert m2.STAGES[value] == name[len("M2_STAGE_"):].lower(), name
+    assert _header_enum("M2_NSTAGES")["M2_NSTAGES"] == m2.NSTAGES
+
+
+def test_config_struct_layout_matches_the_header(m2):
+    """m2_config's fields in header order, all 4-byte, no padding."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct m2_config \{(.*?)\} m2_config;", src, flags=re.S).group(1)
+    fields = re.findall(r"\b(int|float)\s+(\w+)\s*;", body)
+    assert [n for _, n in fields] == [n for n, _ in m2.m2_config._fields_]
+    assert ctypes.sizeof(m2.m2_config) == 4 * len(fields)
