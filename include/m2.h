@@ -145,7 +145,9 @@ enum {
 
 /* Optional device buffers that receive intermediates of the next calls
  * (debugging and parity tests).  Any member may be NULL.  Sizes are for a
- * call over T tokens (prefill) or Bt rows (decode). */
+ * call over T tokens (prefill) or Bt rows (decode).  In the W8A16 arm q is
+ * not written (the input is not quantised) and q2 holds codes no stage
+ * reads; o is what out_proj consumes. */
 typedef struct m2_taps {
   uint8_t* q;      /* e4m3 [T, 2688]  quantised block input            */
   uint16_t* zx;    /* bf16 [T, 10304] in_proj output (z | xBC | dt)    */

@@ -169,3 +169,11 @@ def test_config_struct_layout_matches_the_header(m2):
     fields = re.findall(r"\b(int|float)\s+(\w+)\s*;", body)
     assert [n for _, n in fields] == [n for n, _ in m2.m2_config._fields_]
     assert ctypes.sizeof(m2.m2_config) == 4 * len(fields)
+
+
+@pytest.mark.parametrize("struct", ["m2_weights", "m2_stats", "m2_taps"])
+def test_struct_fields_match_the_header(m2, struct):
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(rf"typedef struct {struct} \{{(.*?)\}} {struct};", src, flags=re.S).group(1)
+    names = re.findall(r"(\w+)\s*;", body)
+    assert names == [n for n, _ in getattr(m2, struct)._fields_]
