@@ -706,3 +706,45 @@ def test_dequant_rounds_through_float32_many_scales():
     ref = t.to(torch.bfloat16).to(torch.float64).numpy()
     got = np.stack([oracle.dequant_e4m3_bf16(codes, float(s)) for s in scales])
     assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- the stack
+
+def _tiny_stack(L=3):
+    layers = [synth.make_weights(97, l, TINY) for l in range(L)]
+    norms = [synth.make_stack_norm_w(97, l, TINY) for l in range(L)]
+    return layers, norms
+
+
+def test_stack_with_silent_blocks_is_the_identity():
+    """Blocks whose out_proj weights are all zero add nothing: the residual
+    stream passes through unchanged while every layer's states still advance."""
+    layers, norms = _tiny_stack()
+    for W in layers:
+        W["out_proj"] = np.zeros_like(W["out_proj"])
+    h = synth.make_hidden(97, 9, TINY)
+    out, convs, ssms = oracle.stack_prefill(layers, norms, h, [9], 1e-5)
+    assert np.array_equal(out, h)
+    assert all(np.abs(s).max() > 0 for s in ssms)
+
+
+def test_stack_decode_after_prefill_equals_longer_prefill():
+    """The carry case through the whole stack: prefill t0 tokens, then decode
+    the rest token by token from every layer's returned states."""
+    layers, norms = _tiny_stack()
+    T, t0 = 9, 5
+    h = synth.make_hidden(98, T, TINY)
+    full, fconv, fssm = oracle.stack_prefill(layers, norms, h, [T], 1e-5)
+    part, convs, ssms = oracle.stack_prefill(layers, norms, h[:t0], [t0], 1e-5)
+    convs = [c.copy() for c in convs]
+    ssms = [s.copy() for s in ssms]
+    outs = [part]
+    for t in range(t0, T):
+        o, crow, srow = oracle.stack_decode(layers, norms, h[t:t + 1], convs, ssms, np.array([0]), 1e-5)
+        for l in range(len(layers)):
+            convs[l][0], ssms[l][0] = crow[l][0], srow[l][0]
+        outs.append(o)
+    np.testing.assert_allclose(np.concatenate(outs), full, rtol=1e-12, atol=1e-12)
+    for l in range(len(layers)):
+        np.testing.assert_allclose(ssms[l][0], fssm[l][0], rtol=1e-10, atol=1e-13)
+        np.testing.assert_array_equal(convs[l][0], fconv[l][0])
