@@ -748,3 +748,38 @@ def test_stack_decode_after_prefill_equals_longer_prefill():
     for l in range(len(layers)):
         np.testing.assert_allclose(ssms[l][0], fssm[l][0], rtol=1e-10, atol=1e-13)
         np.testing.assert_array_equal(convs[l][0], fconv[l][0])
+
+
+# ---------------------------------------------------------------- static quant
+
+def test_f32_rounds_to_nearest_even():
+    assert oracle.f32(np.array([1 + 2.0 ** -24]))[0] == 1.0                    # tie: even
+    assert oracle.f32(np.array([1 + 3 * 2.0 ** -24]))[0] == 1 + 2.0 ** -22     # tie: even (up)
+    assert oracle.f32(np.array([1 + 2.0 ** -24 + 2.0 ** -40]))[0] == 1 + 2.0 ** -23
+
+
+def test_static_quant_matches_torch_in_range():
+    """In range, the static quant equals torch's float32 division followed by
+    its e4m3 cast (torch maps out-of-range values to NaN instead of
+    saturating, so those are compared with the saturation pin)."""
+    rng = np.random.default_rng(31)
+    for s in (1 / 64, 1 / 32, 1 / 3, 0.0123):
+        x = (rng.standard_normal(100000) * 2).astype(np.float32).astype(np.float64)
+        q = oracle.quant_static_e4m3(x, s)
+        t = (torch.from_numpy(x.astype(np.float32)) / torch.tensor(s, dtype=torch.float32)).to(
+            torch.float8_e4m3fn).view(torch.uint8).numpy()
+        inr = np.abs(x / s) < 448
+        assert inr.mean() > 0.99
+        assert np.array_equal(q[inr], t[inr])
+    big = np.array([1000.0, -1e30])
+    assert np.array_equal(oracle.quant_static_e4m3(big, 1.0), np.array([0x7E, 0xFE], np.uint8))
+
+
+def test_static_quant_decides_on_the_float32_quotient():
+    """x / s rounded to float32 lands exactly on the e4m3 tie 1.0625 (which
+    goes to the even code, 1.0) although the exact quotient lies just above
+    it: the decision is taken on the float32 quotient."""
+    s = float(np.float32(1 / 3))
+    x = float(np.float32(1.0625 * s))
+    assert x / s > 1.0625 and np.float32(x) / np.float32(s) == np.float32(1.0625)
+    assert oracle.quant_static_e4m3(np.array([x]), s)[0] == oracle.e4m3_encode(np.array([1.0]))[0]
