@@ -551,7 +551,8 @@ def measure_fp8_peak():
     rec = dict(fp8_tflops=flop / (best * 1e-3) / 1e12, fp8_tflops_sustained=flop * iters / (t_total * 1e-3) / 1e12,
                how="torch._scaled_mm e4m3 x e4m3 -> bf16, 8192^3, 2 n^3 flops: best of 10 (burst) and "
                    "back to back for 3 s (sustained), CUDA events", clocks=clocks,
-               gpu=torch.cuda.get_device_name(0), torch=torch.__version__)
+               gpu=torch.cuda.get_device_name(0), torch=torch.__version__,
+               command="python bench.py --measure-fp8-peak")
     out = os.path.join(ROOT, "profiles", "fp8_gemm_peak.json")
     json.dump(rec, open(out, "w"), indent=1)
     print(json.dumps(rec))
