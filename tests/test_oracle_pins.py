@@ -783,3 +783,97 @@ def test_static_quant_decides_on_the_float32_quotient():
     x = float(np.float32(1.0625 * s))
     assert x / s > 1.0625 and np.float32(x) / np.float32(s) == np.float32(1.0625)
     assert oracle.quant_static_e4m3(np.array([x]), s)[0] == oracle.e4m3_encode(np.array([1.0]))[0]
+
+
+# ---------------------------------------------------------------- block glue: A and dt
+#
+# The block turns its per-head parameters into the recurrence's inputs
+# (vllm.cpp PR #1288, "What it does": the Mamba2 op chain; the reading of
+# the standard Mamba-2 parameterisation): A = -exp(A_log) and
+# dt = softplus(dt_raw + dt_bias), dt_raw being the in_proj output's tail.
+# A block is built whose answers are exact powers of two: in_proj maps the
+# first hidden column to dt_raw = 1 in every head and nothing else, so with
+# x = B = C = 0 the state only decays, by exp(-a dt) per token.  Choosing
+# a = exp(A_log) in {1, 2, 3} and dt_raw + dt_bias in {0, ln 3, ln 7} makes
+# dt in {ln 2, ln 4, ln 8} (log(1 + e^v) with e^v in {1, 3, 7}) and the
+# per-token decay 2^-(a log2(1 + e^v)); the expected values below are those
+# fractions, worked by hand.
+
+GLUE = synth.Geometry(hidden=32, d_inner=32, nheads=8, headdim=4, n_groups=2, d_state=8, conv_width=4)
+_LN2, _LN3, _LN7 = math.log(2.0), math.log(3.0), math.log(7.0)
+# per head: (A_log, dt_bias, dt = softplus(1 + dt_bias), per-token decay)
+GLUE_HEADS = [
+    (0.0, -1.0, _LN2, 1 / 2),
+    (_LN2, -1.0, _LN2, 1 / 4),
+    (0.0, _LN3 - 1.0, 2 * _LN2, 1 / 4),
+    (_LN2, _LN3 - 1.0, 2 * _LN2, 1 / 16),
+    (_LN3, -1.0, _LN2, 1 / 8),
+    (0.0, _LN7 - 1.0, 3 * _LN2, 1 / 8),
+    (_LN3, _LN7 - 1.0, 3 * _LN2, 1 / 512),
+    (_LN2, _LN7 - 1.0, 3 * _LN2, 1 / 64),
+]
+
+
+def _glue_block(xbc_inputs: bool):
+    """Weights of the glue block: in_proj rows of the dt tail read hidden
+    column 0 with weight 1 (code 0x38); with xbc_inputs the xBC rows also read
+    hidden columns 1.. with random small-integer weights."""
+    g = GLUE
+    Wt = dict(synth.make_weights(88, 0, g))
+    conv_dim = g.d_inner + 2 * g.n_groups * g.d_state
+    w = np.zeros((g.zx_width, g.hidden), np.uint8)
+    one = oracle.e4m3_encode(np.array([1.0]))[0]
+    w[g.d_inner + conv_dim:, 0] = one
+    if xbc_inputs:
+        rng = np.random.default_rng(88)
+        ints = rng.integers(-3, 4, (conv_dim, g.hidden - 1))
+        w[g.d_inner:g.d_inner + conv_dim, 1:] = oracle.e4m3_encode(ints.astype(np.float64))
+    Wt["in_proj"] = w
+    Wt["s_w1"] = 1.0
+    Wt["A_log"] = np.array([r[0] for r in GLUE_HEADS], np.float32)
+    Wt["dt_bias"] = np.array([r[1] for r in GLUE_HEADS], np.float32)
+    Wt["conv_w"] = np.ones_like(Wt["conv_w"])
+    return Wt
+
+
+def test_block_glue_zero_input_decays_by_powers_of_two():
+    """x = B = C = 0: the state decays by exp(T dt A); the dt the scan sees and
+    the final state are the hand-worked values.  Catches A = -A_log (no decay
+    where A_log = 0), a dropped, sign-flipped or misplaced dt_bias, and dt_raw
+    dropped or sign-flipped."""
+    g = GLUE
+    Wt = _glue_block(xbc_inputs=False)
+    T = 3
+    h = np.zeros((T, g.hidden), np.float32)
+    h[:, 0] = 1.0                      # e4m3(1 / s_x) = 64 exactly: dt_raw = s_x * 64 * 1 = 1
+    conv_dim = g.d_inner + 2 * g.n_groups * g.d_state
+    S0 = np.random.default_rng(89).standard_normal((1, g.nheads, g.headdim, g.d_state)) * 0.1
+    r = oracle.block_prefill(Wt, h, [T], np.zeros((1, conv_dim, g.conv_width - 1)), S0, keep=True)
+    assert np.all(r["zx"][:, g.d_inner + conv_dim:] == 1.0) and np.all(r["zx"][:, :g.d_inner + conv_dim] == 0)
+    dt_ref = np.array([row[2] for row in GLUE_HEADS])
+    np.testing.assert_allclose(r["dt"], np.broadcast_to(dt_ref, (T, g.nheads)), rtol=1e-7)
+    assert np.all(r["y"] == 0)          # C = 0 and x = 0
+    for h_i, row in enumerate(GLUE_HEADS):
+        np.testing.assert_allclose(r["ssm_state"][0, h_i], row[3] ** T * S0[0, h_i], rtol=1e-6)
+
+
+def test_block_glue_first_token_input_carries_the_same_dt():
+    """From zero state one token leaves S = dt x (outer) B, with dt the
+    hand-worked value of its head (the input term takes the same dt as the
+    decay).  x and B are read from the conv output."""
+    g = GLUE
+    Wt = _glue_block(xbc_inputs=True)
+    rng = np.random.default_rng(90)
+    h = synth.as_bf16_values(rng.integers(-2, 3, (1, g.hidden)).astype(np.float32) / 8)
+    h[0, 0] = 1.0
+    conv_dim = g.d_inner + 2 * g.n_groups * g.d_state
+    r = oracle.block_prefill(Wt, h, [1], np.zeros((1, conv_dim, g.conv_width - 1)),
+                             np.zeros((1, g.nheads, g.headdim, g.d_state)), keep=True)
+    x, B, _ = oracle.split_xbc(r["u"][0], g.d_inner, g.n_groups, g.d_state)
+    x = x.reshape(g.nheads, g.headdim)
+    B = B.reshape(g.n_groups, g.d_state)
+    assert np.abs(x).max() > 0.1 and np.abs(B).max() > 0.1
+    hpg = g.nheads // g.n_groups
+    for h_i, row in enumerate(GLUE_HEADS):
+        np.testing.assert_allclose(r["ssm_state"][0, h_i], row[2] * np.outer(x[h_i], B[h_i // hpg]), rtol=1e-7,
+                                   atol=1e-12)
