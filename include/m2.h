@@ -194,10 +194,35 @@ m2_status m2_set_taps(m2_handle* h, const m2_taps* taps);
 
 /*
  * Read and clear the handle's device error word (synchronises the device).
- * M2_EINVAL: a decode row named a slot outside [0, n_slots) (that row was
- * skipped, its output zeroed); M2_ETIMEOUT: a bounded wait ran out.
+ * M2_EINVAL: a decode row named a slot outside [0, n_slots), or a slot an
+ * earlier row of the same call already named (that row was skipped, its
+ * output zeroed); M2_ETIMEOUT: a bounded wait ran out (the kernel returned
+ * early: outputs of that call are incomplete).
  */
 m2_status m2_check(m2_handle* h);
+
+/*
+ * The same for the standalone entry points (fp8_linear, fp8_linear_bf16,
+ * bf16_linear, fp8_linear_noalloc), which have no handle: they share one
+ * library-owned error word per device (a file-scope device variable, looked
+ * up once per device on the first such call, which should therefore come
+ * before any stream capture).  Synchronises the current device, reads and
+ * clears its word.  M2_ETIMEOUT: a bounded wait of one of those calls ran
+ * out and its y is incomplete.
+ */
+m2_status m2_check_standalone(void);
+
+/*
+ * Self-test of the failure detection (no counterpart on the pages): one
+ * kernel allocates tensor memory, waits with the kernels' bounded mbarrier
+ * wait on a barrier that nothing ever completes, gives up after limit_us
+ * microseconds (1 to 100000), takes the kernels' abort path (sets the error
+ * word, drains, frees tensor memory) and returns, leaving the context usable.
+ * The error word is the handle's (then m2_check(h) reports M2_ETIMEOUT) or,
+ * with h == NULL, the standalone one (m2_check_standalone).  Asynchronous on
+ * `stream`.  Errors: M2_EINVAL (limit out of range), M2_EDEVICE, M2_ECUDA.
+ */
+m2_status m2_selftest_timeout(m2_handle* h, unsigned limit_us, void* stream);
 
 /* Workspace bytes m2_prefill needs for these sequence lengths. */
 m2_status m2_prefill_workspace_size(const m2_handle* h, const int32_t* seqlens_host, int nseq,
@@ -241,9 +266,12 @@ m2_status m2_decode_workspace_size(const m2_handle* h, int Bt, size_t* bytes);
  * Paged decode: one token per row.  Row b advances pool slot slot_idx[b] in
  * place (PR #1288, "What it does": the paged arm advances the gathered rows
  * IN PLACE).  slot_idx[b] == -1 is a padding row: output zeroed, no state
- * touched.  Slot ids must be unique (duplicates race; not checked).  An id
- * outside [-1, n_slots) is detected on the device: that row is skipped, its
- * output zeroed, and m2_check() reports M2_EINVAL.
+ * touched.  Slot ids must be unique within a call: a row naming a slot that
+ * an earlier row of the call already named is detected on the device, skipped
+ * (output zeroed, no state touched; the first row naming the slot advances
+ * it) and m2_check() reports M2_EINVAL.  An id outside [-1, n_slots) is
+ * detected the same way: that row is skipped, its output zeroed, and
+ * m2_check() reports M2_EINVAL.
  *   hidden     bf16 [Bt, 2688] device
  *   conv_pool  bf16 [n_slots, 6144, 3] device
  *   ssm_pool   [n_slots, 64, 64, 128] device, f32 or bf16 (ssm_dtype)
@@ -273,8 +301,9 @@ m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* c
  * The input quant and both projections run once over all rows; the decode
  * rows advance their pool rows in place, the prefill rows run the chunked
  * scan.  Bt = 0 or nseq = 0 is allowed (not both); the decode arguments may
- * be NULL when Bt = 0, the prefill ones when nseq = 0.  Intermediate taps are
- * not written by this call.  Errors as m2_decode and m2_prefill.
+ * be NULL when Bt = 0, the prefill ones when nseq = 0.  Of the intermediate
+ * taps this call writes q, zx and q2 (Bt + sum(T) rows, in batch order); the
+ * others are not written.  Errors as m2_decode and m2_prefill.
  */
 m2_status m2_mixed_workspace_size(const m2_handle* h, int Bt, const int32_t* seqlens_host, int nseq,
                                   size_t* bytes);
@@ -317,8 +346,14 @@ m2_status fp8_linear(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_
  * workspace for its split-K partial sums; this variant instead uses one
  * library-owned scratch array in device memory (a file-scope __device__
  * array of M2_NOALLOC_SCRATCH_BYTES = 16 MiB), so it calls no cudaMalloc,
- * cudaFree or allocating library routine.  Every GPU on which this entry point
- * has run holds that array until the process exits.
+ * cudaFree or allocating library routine.  The array is part of the library's
+ * device code: every GPU on which that code is loaded holds it until the
+ * process exits (with the default lazy module loading, the GPUs on which a
+ * call of this library has run; with CUDA_MODULE_LOADING=EAGER, every GPU the
+ * process initialises, whether or not it calls this entry point).  The
+ * device address of the array is cached per device on first use; a
+ * cudaDeviceReset() of a device invalidates it, so this entry point must not
+ * be called on a device after that device was reset.
  *
  * Same arguments and result as fp8_linear without the workspace.  Only the
  * few-row (decode) form is offered: 1 <= M <= 256, and the split-K partials
@@ -334,6 +369,8 @@ m2_status fp8_linear(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_
 #define M2_NOALLOC_SCRATCH_BYTES (16u << 20)
 m2_status fp8_linear_noalloc(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_w, uint16_t* y, int M,
                              int N, int K, void* stream);
+/* (A bounded wait that runs out inside fp8_linear_noalloc, fp8_linear,
+ * fp8_linear_bf16 or bf16_linear is reported by m2_check_standalone().) */
 
 /*
  * The quantise-inside form (MatmulFp8CutlassD of PR #972): x bf16 [M, K] is

@@ -35,7 +35,8 @@ EXPORTED = ["m2_last_error", "m2_create", "m2_destroy", "m2_get_stats", "m2_set_
             "fp8_quant", "fp8_linear_workspace_size", "fp8_linear", "fp8_linear_bf16",
             "m2_rmsnorm_residual", "m2_profile_enable", "m2_profile_read", "fp8_linear_noalloc",
             "m2_prefill_q", "m2_decode_q", "m2_rmsnorm_residual_quant", "m2_mixed_workspace_size", "m2_mixed",
-            "fp8_dequant", "bf16_linear_workspace_size", "bf16_linear"]
+            "fp8_dequant", "bf16_linear_workspace_size", "bf16_linear", "m2_check_standalone",
+            "m2_selftest_timeout"]
 
 STAGES = ["quant_in", "in_proj", "conv", "conv_state", "ssd_cumsum", "ssd_chunk_state", "ssd_state_pass",
           "ssd_chunk_scan", "norm_quant", "out_proj", "decode_fused", "dec_quant_in", "dec_in_proj",
@@ -102,6 +103,8 @@ _sigs = {
     "fp8_dequant": ([_vp, _sz, _f, _vp, _vp], _i),
     "bf16_linear_workspace_size": ([_i, _i, _i, ctypes.POINTER(_sz)], _i),
     "bf16_linear": ([_vp, _vp, _f, _vp, _i, _i, _i, _vp, _sz, _vp], _i),
+    "m2_check_standalone": ([], _i),
+    "m2_selftest_timeout": ([_vp, ctypes.c_uint, _vp], _i),
 }
 for _name, (_args, _ret) in _sigs.items():
     _fn = getattr(_lib, _name)
@@ -219,6 +222,12 @@ class Mamba2Mixer:
     def check(self):
         _check(_lib.m2_check(self._h))
 
+    def selftest_timeout(self, limit_us: int = 1000, stream=None):
+        """Run the failure-detection self-test on this handle's error word:
+        a bounded wait that nothing completes runs out after limit_us; the
+        next check() raises M2Error(M2_ETIMEOUT)."""
+        _check(_lib.m2_selftest_timeout(self._h, int(limit_us), _stream(stream)))
+
     def profile(self, on: bool):
         _check(_lib.m2_profile_enable(self._h, int(bool(on))))
 
@@ -322,6 +331,17 @@ def _mixed_ws_size(blk, Bt, seqlens):
     arr = (ctypes.c_int32 * max(len(seqlens), 1))(*seqlens)
     _check(_lib.m2_mixed_workspace_size(blk._h, Bt, arr, len(seqlens), ctypes.byref(n)))
     return n.value
+
+
+def check_standalone():
+    """Read and clear the standalone entry points' device error word
+    (synchronises); raises M2Error(M2_ETIMEOUT) if a bounded wait ran out."""
+    _check(_lib.m2_check_standalone())
+
+
+def selftest_timeout_standalone(limit_us: int = 1000, stream=None):
+    """The failure-detection self-test on the standalone error word."""
+    _check(_lib.m2_selftest_timeout(None, int(limit_us), _stream(stream)))
 
 
 def fp8_quant(x: torch.Tensor, scale: float, q: torch.Tensor | None = None, stream=None) -> torch.Tensor:

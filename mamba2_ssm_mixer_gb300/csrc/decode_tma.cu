@@ -14,7 +14,11 @@
 //  - conv, gate and norm for an item run on the consumer warps while the ring
 //    keeps streaming.
 // The pool rows are advanced in place through slot_idx: the gather and
-// scatter of vllm.cpp PR #1288 ("What it does") are addressing.  A bf16 pool
+// scatter of vllm.cpp PR #1288 ("What it does") are addressing.  Slot ids
+// must be unique within a call (two rows advancing one slot would race): a row
+// whose slot an earlier row of the call already names is skipped like a bad
+// id (output zeroed, nothing touched) and flagged in the error word, so the
+// first row naming a slot is the one that advances it.  A bf16 pool
 // (the non-f32 state cache of the same section's ssm_dtype term) is widened
 // to f32 as it is read, updated and reduced to y in f32, and rounded to bf16
 // (nearest even) as it is written back.  Every wait is
@@ -49,6 +53,15 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory"); }
+
+// True when a row before b names `slot` too (whole warp; every lane gets the
+// answer).  Rows are read in strides of 32, so a batch of Bt rows costs each
+// lane Bt / 32 cached loads per item.
+__device__ __forceinline__ bool slot_named_earlier(const int32_t* __restrict__ slot_idx, int b, int slot, int lane) {
+  bool hit = false;
+  for (int j = lane; j < b; j += 32) hit |= (slot_idx[j] == slot);
+  return __any_sync(0xffffffffu, hit);
+}
 
 // Pool element types: 4 consecutive d_state entries as f32.
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
@@ -108,17 +121,19 @@ __global__ void __launch_bounds__(kThreadsT, 2)
 
   if (warp == kConsumers / 32) {
     // ------------------------------------------------ producer warp
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      bool issued[kStages];
-      uint32_t issued_phase[kStages];
-      for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
-      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const int b = it / kG, g = it % kG;
-        const int slot = slot_idx[b];
-        if (slot < 0 || slot >= n_slots) continue;
+    // (all lanes walk the items to share the duplicate scan; lane 0 issues)
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    bool issued[kStages];
+    uint32_t issued_phase[kStages];
+    for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
+    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+      const int b = it / kG, g = it % kG;
+      const int slot = slot_idx[b];
+      if (slot < 0 || slot >= n_slots) continue;
+      if (slot_named_earlier(slot_idx, b, slot, lane)) continue;
+      if (lane == 0) {
         const S* src = ssm_pool + ((size_t)slot * kNH + g * kHPG) * (kP * kN);
         for (int hh = 0; hh < kHPG; ++hh) {
           if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
@@ -134,10 +149,11 @@ __global__ void __launch_bounds__(kThreadsT, 2)
           if (++stage == kStages) stage = 0, phase ^= 1u;
         }
       }
-      if (*abort)   // let loads already in flight land before the CTA can exit
-        for (int s = 0; s < kStages; ++s)
-          if (issued[s]) mbar_wait(&sm.full[s], issued_phase[s], nullptr, 100000000ull);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
     }
+    if (lane == 0 && *abort)   // let loads already in flight land before the CTA can exit
+      for (int s = 0; s < kStages; ++s)
+        if (issued[s]) mbar_wait(&sm.full[s], issued_phase[s], nullptr, 100000000ull);
     return;
   }
 
@@ -151,8 +167,12 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     const int b = it / kG, g = it % kG;
     const int slot = slot_idx[b];
     uint8_t* q2row = q2 + (size_t)b * kI + g * kGroupCh;
-    if (slot < 0 || slot >= n_slots) {
-      if (slot != -1 && tid == 0) atomicOr(err, kErrSlot);
+    const bool bad = slot < 0 || slot >= n_slots;
+    // every consumer warp takes the same decision from the same reads
+    const bool dup = !bad && slot_named_earlier(slot_idx, b, slot, lane);
+    if (bad || dup) {
+      if (tid == 0 && dup) atomicOr(err, kErrDupSlot);
+      if (tid == 0 && bad && slot != -1) atomicOr(err, kErrSlot);
       for (int i = tid; i < kGroupCh; i += kConsumers) q2row[i] = 0;
       continue;
     }

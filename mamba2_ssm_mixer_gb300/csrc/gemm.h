@@ -28,6 +28,11 @@ cudaError_t gemm_tc_big_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, 
                              int* err, cudaStream_t st);
 constexpr int kSkinnyMaxRows = 256;
 
+// Failure-detection self-test: one CTA allocates TMEM, waits with the GEMMs'
+// bounded mbarrier wait (limit_ns) on a barrier nothing arrives at, takes
+// their abort path (error word, drain, TMEM freed) and returns.
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* err, cudaStream_t st);
+
 // W8A16 weight preparation (dequant.cu): out[i] = bf16(dec(q[i]) * scale),
 // the product formed in f32 and rounded to nearest even.
 cudaError_t launch_dequant_e4m3_bf16(const uint8_t* q, size_t n, float scale, uint16_t* out, cudaStream_t st);

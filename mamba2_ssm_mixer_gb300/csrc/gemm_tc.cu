@@ -410,6 +410,48 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(const float* __restrict__
 }
 
 // ---------------------------------------------------------------------------
+// Failure-detection self-test: the abort path of the kernels above, reached
+// without breaking anything.  Warp 1's lane 0 (the MMA issuer's role) waits
+// on a barrier that no copy or thread ever completes; the wait runs out after
+// limit_ns, raises the abort flag and the error word, drains (a commit with
+// no MMA outstanding arrives at once) and the CTA frees its TMEM and returns.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(64, 1) k_wait_selftest(uint64_t limit_ns, int* err) {
+  __shared__ Ctl ctl;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(&ctl.full[0], 1);
+    mbar_init(&ctl.drain, 1);
+    ctl.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&ctl.tmem_base, 32);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();
+  if (warp == 1 && lane == 0) {
+    if (!mbar_wait(&ctl.full[0], 0, &ctl.abort, limit_ns)) raise_abort(&ctl, err);
+    if (ctl.abort) {
+      mma_commit(&ctl.drain);
+      mbar_wait(&ctl.drain, 0, nullptr, 100000000ull);
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(ctl.tmem_base, 32);
+  }
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, int* err, cudaStream_t st) {
+  return launch_pdl(k_wait_selftest, dim3(1), dim3(64), 0, st, limit_ns, err);
+}
+
+// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 namespace {

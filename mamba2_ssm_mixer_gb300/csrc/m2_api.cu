@@ -78,6 +78,11 @@ struct Carve {
   }
 };
 
+// The error word of the standalone entry points (fp8_linear, fp8_linear_bf16,
+// bf16_linear, fp8_linear_noalloc): one file-scope device int per device,
+// found once per device; m2_check_standalone reads and clears it.
+m2_status standalone_error_word(int** out);
+
 }  // namespace
 
 struct m2_handle {
@@ -296,14 +301,39 @@ m2_status m2_profile_read(m2_handle* h, double* ms, uint64_t* launches) {
   return M2_OK;
 }
 
+// Status of a device error word's bits (timeouts first: they leave outputs
+// incomplete).
+static m2_status error_word_status(int v, const char* who) {
+  if (v & kErrTimeout) return fail(M2_ETIMEOUT, "%s: a bounded device wait ran out", who);
+  if (v & kErrSlot) return fail(M2_EINVAL, "%s: a decode row named a slot outside [0, n_slots)", who);
+  if (v & kErrDupSlot)
+    return fail(M2_EINVAL, "%s: two decode rows named the same slot (the later rows were skipped)", who);
+  return M2_OK;
+}
+
 m2_status m2_check(m2_handle* h) {
   if (!h) return fail(M2_EINVAL, "m2_check: null handle");
   int v = 0;
   M2_CUDA(cudaDeviceSynchronize());
   M2_CUDA(cudaMemcpy(&v, h->err, sizeof v, cudaMemcpyDeviceToHost));
   M2_CUDA(cudaMemset(h->err, 0, sizeof(int)));
-  if (v & kErrTimeout) return fail(M2_ETIMEOUT, "m2_check: a bounded device wait ran out");
-  if (v & kErrSlot) return fail(M2_EINVAL, "m2_check: a decode row named a slot outside [0, n_slots)");
+  return error_word_status(v, "m2_check");
+}
+
+m2_status m2_selftest_timeout(m2_handle* h, unsigned limit_us, void* stream) {
+  g_err.clear();
+  if (limit_us < 1 || limit_us > 100000)
+    return fail(M2_EINVAL, "m2_selftest_timeout: limit_us %u not in [1, 100000]", limit_us);
+  int* err = nullptr;
+  if (h) {
+    err = h->err;
+  } else {
+    m2_status s = check_device();
+    if (s) return s;
+    if ((s = standalone_error_word(&err))) return s;
+  }
+  M2_CUDA(launch_wait_selftest((uint64_t)limit_us * 1000ull, err, static_cast<cudaStream_t>(stream)));
+  if (h) h->stats.kernel_launches += 1;
   return M2_OK;
 }
 
@@ -741,6 +771,12 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
   }
   M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl,
            gemm_fp8(w.q2, h->out_proj, out, R, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+  if (h->taps_on) {   // the row-aligned intermediates, in batch order
+    m2_status s;
+    if ((s = copy_tap(h->taps.q, w.q, (size_t)R * kH, st))) return s;
+    if ((s = copy_tap(h->taps.zx, w.zx, (size_t)R * kZ * 2, st))) return s;
+    if ((s = copy_tap(h->taps.q2, w.q2, (size_t)R * kI, st))) return s;
+  }
   if (T > 0) {
     h->stats.prefill_calls += 1;
     h->stats.conv_fwd_calls += 1;
@@ -793,8 +829,10 @@ m2_status fp8_linear(const uint8_t* a_q, float s_a, const uint8_t* w_q, float s_
   size_t need = gemm_workspace_bytes(M, N, K);
   if (ws_bytes < need || (need && !workspace))
     return fail(M2_ENOMEM, "fp8_linear: workspace %zu bytes < %zu needed", ws_bytes, need);
+  int* err = nullptr;
+  if ((s = standalone_error_word(&err))) return s;
   int nl = 0;
-  M2_CUDA(gemm_fp8(a_q, w_q, y, M, N, K, s_a * s_w, workspace, ws_bytes, nullptr, static_cast<cudaStream_t>(stream), &nl));
+  M2_CUDA(gemm_fp8(a_q, w_q, y, M, N, K, s_a * s_w, workspace, ws_bytes, err, static_cast<cudaStream_t>(stream), &nl));
   return M2_OK;
 }
 
@@ -807,11 +845,13 @@ m2_status fp8_linear_bf16(const uint16_t* x, float s_a, const uint8_t* w_q, floa
   size_t qbytes = align256((size_t)M * K);
   size_t need = qbytes + gemm_workspace_bytes(M, N, K);
   if (ws_bytes < need) return fail(M2_ENOMEM, "fp8_linear_bf16: workspace %zu bytes < %zu needed", ws_bytes, need);
+  int* err = nullptr;
+  if ((s = standalone_error_word(&err))) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* q = static_cast<uint8_t*>(workspace);
   M2_CUDA(launch_quant_e4m3(x, (size_t)M * K, s_a, q, st));
   int nl = 0;
-  M2_CUDA(gemm_fp8(q, w_q, y, M, N, K, s_a * s_w, static_cast<char*>(workspace) + qbytes, ws_bytes - qbytes, nullptr, st, &nl));
+  M2_CUDA(gemm_fp8(q, w_q, y, M, N, K, s_a * s_w, static_cast<char*>(workspace) + qbytes, ws_bytes - qbytes, err, st, &nl));
   return M2_OK;
 }
 
@@ -848,8 +888,10 @@ m2_status bf16_linear(const uint16_t* x, const uint16_t* w, float scale, uint16_
   const size_t need = gemm_workspace_bytes_bf16(M, N, K);
   if (ws_bytes < need || (need && !workspace))
     return fail(M2_ENOMEM, "bf16_linear: workspace %zu bytes < %zu needed", ws_bytes, need);
+  int* err = nullptr;
+  if ((s = standalone_error_word(&err))) return s;
   int nl = 0;
-  M2_CUDA(gemm_bf16(x, w, y, M, N, K, scale, workspace, ws_bytes, nullptr, static_cast<cudaStream_t>(stream), &nl));
+  M2_CUDA(gemm_bf16(x, w, y, M, N, K, scale, workspace, ws_bytes, err, static_cast<cudaStream_t>(stream), &nl));
   return M2_OK;
 }
 
@@ -894,6 +936,29 @@ namespace {
 // up once per device (noalloc_scratch below).
 __device__ __align__(256) float g_noalloc_scratch[M2_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
+// The standalone entry points' device error word (bounded-wait timeouts).
+__device__ int g_standalone_err;
+
+m2_status standalone_error_word(int** out) {
+  static std::mutex mu;
+  static std::map<int, int*> by_device;
+  int dev = 0;
+  M2_CUDA(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = by_device.find(dev);
+  if (it != by_device.end()) {
+    *out = it->second;
+    return M2_OK;
+  }
+  int* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_standalone_err);
+  if (e != cudaSuccess || !p)
+    return fail(M2_ECUDA, "cudaGetSymbolAddress of the standalone error word failed: %s", cudaGetErrorString(e));
+  by_device[dev] = p;
+  *out = p;
+  return M2_OK;
+}
+
 m2_status noalloc_scratch(float** out) {
   static std::mutex mu;
   static std::map<int, float*> by_device;
@@ -929,9 +994,24 @@ extern "C" m2_status fp8_linear_noalloc(const uint8_t* a_q, float s_a, const uin
                 N, K, need, (unsigned)M2_NOALLOC_SCRATCH_BYTES);
   float* scratch = nullptr;
   if ((s = noalloc_scratch(&scratch))) return s;
+  int* err = nullptr;
+  if ((s = standalone_error_word(&err))) return s;
   int nl = 0;
-  M2_CUDA(gemm_tc_skinny(a_q, w_q, y, M, N, K, s_a * s_w, scratch, (size_t)M2_NOALLOC_SCRATCH_BYTES, nullptr,
+  M2_CUDA(gemm_tc_skinny(a_q, w_q, y, M, N, K, s_a * s_w, scratch, (size_t)M2_NOALLOC_SCRATCH_BYTES, err,
                          static_cast<cudaStream_t>(stream), &nl));
   return M2_OK;
+}
+
+extern "C" m2_status m2_check_standalone(void) {
+  g_err.clear();
+  m2_status s = check_device();
+  if (s) return s;
+  int* err = nullptr;
+  if ((s = standalone_error_word(&err))) return s;
+  int v = 0;
+  M2_CUDA(cudaDeviceSynchronize());
+  M2_CUDA(cudaMemcpy(&v, err, sizeof v, cudaMemcpyDeviceToHost));
+  M2_CUDA(cudaMemset(err, 0, sizeof(int)));
+  return error_word_status(v, "m2_check_standalone");
 }
 

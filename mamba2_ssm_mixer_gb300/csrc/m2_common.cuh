@@ -30,8 +30,9 @@ constexpr int kOffB = kI;                // 4096
 constexpr int kOffC = kI + kG * kN;      // 5120
 
 // Device error word bits.
-constexpr int kErrSlot = 1;
-constexpr int kErrTimeout = 2;
+constexpr int kErrSlot = 1;      // a decode row named a slot outside [0, n_slots)
+constexpr int kErrTimeout = 2;   // a bounded wait ran out
+constexpr int kErrDupSlot = 4;   // two decode rows of one call named the same slot
 
 __device__ __forceinline__ float bf2f(__nv_bfloat16 v) { return __bfloat162float(v); }
 __device__ __forceinline__ float bfbits2f(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }

@@ -2,6 +2,8 @@
 device results with the oracle.  Holds none of the block's arithmetic."""
 from __future__ import annotations
 
+import contextlib
+
 import numpy as np
 import torch
 
@@ -64,32 +66,84 @@ def bf16_ulp(v):
     return np.exp2(np.floor(np.log2(a)) - 7)
 
 
-# One e4m3 code step of out_proj's input at the top of the e4m3 range is 32
-# codes = 1.0 in units of the normed activation (s_y = 1/32); times the largest
-# out_proj weight (|W2| <= ~0.11 for N(0, 0.02) over 11M entries) it moves an
-# output element by up to ~0.11.  Two W8A8 implementations whose unrounded
-# activations differ in the last bf16 bit take different e4m3 decisions for a
-# small fraction of elements (both decisions are correct roundings of their own
-# inputs), so a per-element bound must admit one flip.
-FLIP_BOUND = 0.15
-MAX_FRAC_OVER_2E2 = 1e-2
+def assert_block_out(got, ref, what="out", q2=None, ref_q2=None, Wt=None, o=None, ref_o=None):
+    """Block output (bf16) against the oracle's: relative L2 <= 1e-2, and every
+    element within 2e-2 + one bf16 ulp of the larger value (the ulp is the
+    output's own storage rounding: outputs reach |8| where one bf16 step is
+    0.03).
 
-
-def assert_block_out(got, ref, what="out"):
-    """Block output (bf16): relative L2 <= 1e-2; every element within
-    FLIP_BOUND; and at most 1% of elements beyond 2e-2 + one bf16 ulp of the
-    larger value (the ulp term is the output's own storage rounding: outputs
-    reach |8| where one bf16 step is 0.03)."""
+    Two W8A8 implementations whose unrounded out_proj inputs differ in the last
+    bf16 bit take different e4m3 decisions for a small fraction of codes (both
+    correct roundings of their own inputs), and one code step near the top of
+    the e4m3 range is 1.0 in units of the normed activation.  Given q2 (the
+    device's out_proj input codes, its q2 tap), ref_q2 (the oracle's) and Wt
+    (out_proj's weights and scales), each element may in addition differ by
+    exactly what the differing codes of its row move it,
+        s_y s_w2 sum_k |dec(q2[m, k]) - dec(ref_q2[m, k])| |dec(W2[n, k])|,
+    which is zero on rows whose codes all agree: those rows meet the stated
+    bound as it is.  This presumes the device output is out_proj applied to
+    its own codes, which assert_out_is_gemm checks (bit for bit against the
+    library's standalone GEMM, itself pinned against the oracle); the codes
+    are checked by assert_e4m3_close.  For the W8A16 arm, whose out_proj takes
+    the bf16 gated-norm output, o / ref_o play the part of the codes against
+    the dequantised weights."""
+    import oracle
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     ma, rl = max_abs(got, ref), rel_l2(got, ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
-    bound = OUT_MAX_ABS + bf16_ulp(np.maximum(np.abs(got), np.abs(ref)))
-    frac = float(np.mean(np.abs(got - ref) > bound))
-    msg = f"{what}: max abs {ma:.3e}, rel L2 {rl:.3e}, {frac:.2e} of elements over 2e-2 + 1 ulp"
+    err = np.abs(got - ref)
+    base = OUT_MAX_ABS + bf16_ulp(np.maximum(np.abs(got), np.abs(ref)))
+    allowed = base
+    note = "no out_proj inputs given: the stated bound on every element"
+    if q2 is not None or o is not None:
+        if q2 is not None:    # W8A8: e4m3 codes against e4m3 weights
+            a, ref_a = oracle.e4m3_decode(np.asarray(q2)), oracle.e4m3_decode(np.asarray(ref_q2))
+            w = oracle.e4m3_decode(Wt["out_proj"])
+            s = float(Wt["s_y"]) * float(Wt["s_w2"])
+        else:                 # W8A16: bf16 activations against dequantised bf16 weights
+            a, ref_a = np.asarray(o, np.float64), np.asarray(ref_o, np.float64)
+            w = oracle.dequant_e4m3_bf16(Wt["out_proj"], Wt["s_w2"])
+            s = 1.0
+        assert a.shape == ref_a.shape == (got.shape[0], Wt["out_proj"].shape[1])
+        rows = np.nonzero(np.any(a != ref_a, axis=1))[0]
+        flip = np.zeros_like(got)
+        if len(rows):
+            flip[rows] = s * (np.abs(a[rows] - ref_a[rows]) @ np.abs(w).T)
+        allowed = base + flip
+        over_rows = np.unique(np.nonzero(err > base)[0])
+        note = (f"{len(rows)} of {got.shape[0]} rows have differing out_proj inputs; "
+                f"elements over 2e-2 + 1 ulp lie in {len(over_rows)} rows, all among them: "
+                f"{bool(np.isin(over_rows, rows).all())}")
+    bad = err > allowed
+    msg = (f"{what}: max abs {ma:.3e}, rel L2 {rl:.3e}, {float(np.mean(err > base)):.2e} of elements over "
+           f"2e-2 + 1 ulp; {note}")
     print(msg)
-    assert rl <= OUT_REL_L2 and ma <= FLIP_BOUND and frac <= MAX_FRAC_OVER_2E2, msg
+    assert rl <= OUT_REL_L2 and not bad.any(), msg + f"; {int(bad.sum())} elements beyond the bound"
     return ma, rl
+
+
+def gpu_out_proj(Wt, arm="w8a8"):
+    """out_proj as the library's standalone entry point computes it on the
+    device: fp8_linear(q2, s_y, W2, s_w2) (W8A8), or bf16_linear(o, W2 dequantised
+    by fp8_dequant) (W8A16).  Takes and returns numpy arrays."""
+    import mamba2_ssm_mixer_gb300 as m2
+    w = u8_dev(Wt["out_proj"])
+    if arm == "w8a16":
+        wb = m2.fp8_dequant(w, Wt["s_w2"])
+        return lambda a: to_np(m2.bf16_linear(bf16_dev(a), wb, 1.0))
+    return lambda a: to_np(m2.fp8_linear(u8_dev(a), Wt["s_y"], w, Wt["s_w2"]))
+
+
+def assert_out_is_gemm(got, a, gemm, what="out"):
+    """The block's output rows are out_proj applied to the block's own out_proj
+    input a (its q2 or o tap) by the library's standalone GEMM, bit for bit
+    (same kernel and summation order for the same number of rows)."""
+    g = gemm(np.asarray(a))
+    got = np.asarray(got, np.float64)
+    assert g.shape == got.shape
+    bad = int(np.sum(g != got))
+    assert bad == 0, f"{what}: {bad} elements differ from out_proj of the block's own input"
 
 
 def assert_state(got, ref, what="ssm_state"):
@@ -123,10 +177,16 @@ def assert_e4m3_close(got_codes, ref_codes, max_frac=2e-3, what="q2"):
     if diff.any():
         gs, rs = g[diff], r[diff]
         mag_g, mag_r = gs & 0x7F, rs & 0x7F
-        adjacent = np.abs(mag_g - mag_r) <= 1
+        same_sign = (gs & 0x80) == (rs & 0x80)
+        adjacent = (same_sign & (np.abs(mag_g - mag_r) <= 1)) | ((mag_g == 0) & (mag_r == 0))
         vg, vr = oracle.e4m3_decode(gs.astype(np.uint8)), oracle.e4m3_decode(rs.astype(np.uint8))
         near_zero = np.abs(vg - vr) <= E4M3_NEAR_ZERO_STEPS * 2.0 ** -9
-        assert np.all(adjacent | near_zero), f"{what}: codes more than one step apart"
+        far = ~adjacent
+        pairs = ", ".join(f"{a:#04x}/{b:#04x} ({x:+.5f}/{y:+.5f})"
+                          for a, b, x, y in zip(gs[far][:20], rs[far][:20], vg[far][:20], vr[far][:20]))
+        print(f"{what}: {int(diff.sum())} of {g.size} codes differ, {int(adjacent.sum())} by one step; "
+              f"not adjacent (device/reference): {pairs if far.any() else 'none'}")
+        assert np.all(adjacent | near_zero), f"{what}: codes more than one step apart: {pairs}"
 
 
 def assert_bf16_close(got, ref, max_frac=5e-3, atol=0.0, what="bf16"):
@@ -151,6 +211,18 @@ def gemm_atol(a_codes, w_codes, scale):
     generous 256 for the accumulation depth and order)."""
     import oracle
     return 2.0 ** -16 * scale * (np.abs(oracle.e4m3_decode(a_codes)) @ np.abs(oracle.e4m3_decode(w_codes)).T)
+
+
+@contextlib.contextmanager
+def q2_tap(blk, rows: int):
+    """Install a q2 tap (the e4m3 codes out_proj consumes) on a block for the
+    calls inside the with-block; yields the device buffer."""
+    t = torch.zeros((rows, 4096), dtype=torch.uint8, device="cuda")
+    blk.set_taps(q2=t)
+    try:
+        yield t
+    finally:
+        blk.set_taps()
 
 
 def make_block(config: int, layer: int = 0):

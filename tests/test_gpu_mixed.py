@@ -8,7 +8,8 @@ import torch
 
 import oracle
 import synth
-from helpers import assert_bf16_close, assert_block_out, assert_state, bf16_dev, device_weights, f32_dev, to_np
+from helpers import (assert_bf16_close, assert_block_out, assert_e4m3_close, assert_state, bf16_dev, device_weights,
+                     assert_out_is_gemm, f32_dev, gpu_out_proj, q2_tap, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -39,15 +40,19 @@ def test_mixed_small_batch_vs_oracle(block0):
     h = np.concatenate([synth.make_hidden(2, Bt), synth.make_hidden(5, sum(lens))])
     cp, sp = bf16_dev(conv_pool0), f32_dev(ssm_pool0)
     cs, ss = bf16_dev(conv_st0), f32_dev(ssm_st0)
-    out = blk.mixed(bf16_dev(h), Bt, cp, sp, torch.from_numpy(slots).cuda(), lens, cs, ss, has_initial=[1, 0])
+    with q2_tap(blk, Bt + sum(lens)) as q2t:
+        out = blk.mixed(bf16_dev(h), Bt, cp, sp, torch.from_numpy(slots).cuda(), lens, cs, ss, has_initial=[1, 0])
     torch.cuda.synchronize()
     blk.check()
-    rd = oracle.block_decode(Wt, h[:Bt], conv_pool0, ssm_pool0, slots)
+    rd = oracle.block_decode(Wt, h[:Bt], conv_pool0, ssm_pool0, slots, keep=True)
     mask = np.array([1.0, 0.0])
-    rp = oracle.block_prefill(Wt, h[Bt:], lens, conv_st0 * mask[:, None, None], ssm_st0 * mask[:, None, None, None])
-    o = to_np(out)
-    assert_block_out(o[:Bt], rd["out"])
-    assert_block_out(o[Bt:], rp["out"])
+    rp = oracle.block_prefill(Wt, h[Bt:], lens, conv_st0 * mask[:, None, None], ssm_st0 * mask[:, None, None, None],
+                              keep=True)
+    o, q2 = to_np(out), to_np(q2t)
+    assert_e4m3_close(q2, np.concatenate([rd["q2"], rp["q2"]]))
+    assert_out_is_gemm(o, q2, gpu_out_proj(Wt))
+    assert_block_out(o[:Bt], rd["out"], q2=q2[:Bt], ref_q2=rd["q2"], Wt=Wt)
+    assert_block_out(o[Bt:], rp["out"], q2=q2[Bt:], ref_q2=rp["q2"], Wt=Wt)
     assert_state(to_np(sp)[slots], rd["ssm_rows"])
     assert_state(to_np(ss), rp["ssm_state"])
     untouched = np.setdiff1d(np.arange(n_slots), slots)
@@ -66,13 +71,21 @@ def test_mixed_bench_shape_vs_separate_calls(block0):
     zs = lambda: torch.zeros((4, 64, 64, 128), dtype=torch.float32, device="cuda")
     cp1, sp1, cs1, ss1 = conv_pool0.clone(), ssm_pool0.clone(), zc(), zs()
     cp2, sp2, cs2, ss2 = conv_pool0.clone(), ssm_pool0.clone(), zc(), zs()
-    od = blk.decode(hd, cp1, sp1, slots)
-    op = blk.prefill(hp, lens, cs1, ss1)
-    om = blk.mixed(torch.cat([hd, hp]), Bt, cp2, sp2, slots, lens, cs2, ss2)
+    with q2_tap(blk, Bt) as qd:
+        od = blk.decode(hd, cp1, sp1, slots)
+    with q2_tap(blk, sum(lens)) as qp:
+        op = blk.prefill(hp, lens, cs1, ss1)
+    with q2_tap(blk, Bt + sum(lens)) as qm:
+        om = blk.mixed(torch.cat([hd, hp]), Bt, cp2, sp2, slots, lens, cs2, ss2)
     torch.cuda.synchronize()
     blk.check()
-    assert_block_out(to_np(om[:Bt]), to_np(od))
-    assert_block_out(to_np(om[Bt:]), to_np(op))
+    qm = to_np(qm)
+    gemm = gpu_out_proj(Wt)
+    assert_out_is_gemm(to_np(om), qm, gemm, what="mixed")
+    assert_out_is_gemm(to_np(od), to_np(qd), gemm, what="decode")
+    assert_out_is_gemm(to_np(op), to_np(qp), gemm, what="prefill")
+    assert_block_out(to_np(om[:Bt]), to_np(od), q2=qm[:Bt], ref_q2=to_np(qd), Wt=Wt, what="mixed vs decode")
+    assert_block_out(to_np(om[Bt:]), to_np(op), q2=qm[Bt:], ref_q2=to_np(qp), Wt=Wt, what="mixed vs prefill")
     rows = slots.cpu().numpy()
     assert_state(to_np(sp2)[rows], to_np(sp1)[rows])
     assert_state(to_np(ss2), to_np(ss1))

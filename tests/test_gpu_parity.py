@@ -13,7 +13,8 @@ import torch
 import oracle
 import synth
 from helpers import (assert_bf16_close, assert_block_out, assert_e4m3_close, assert_state, bf16_dev,
-                     device_weights, f32_dev, gemm_atol, max_abs, rel_l2, to_np, u8_dev)
+                     assert_out_is_gemm, device_weights, f32_dev, gemm_atol, gpu_out_proj, max_abs, q2_tap, rel_l2,
+                     to_np, u8_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -140,7 +141,8 @@ def test_config0_prefill_32_tokens_all_stages(block0):
     assert rel_l2(to_np(tp["y"]), ref["y"]) < 1e-2
     assert rel_l2(to_np(tp["o"]), ref["o"]) < 1e-2
     assert_e4m3_close(to_np(tp["q2"]), ref["q2"])
-    assert_block_out(to_np(out), ref["out"])
+    assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
+    assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])
     assert_bf16_close(to_np(conv), ref["conv_state"], atol=1e-3, what="conv_state")
 
@@ -166,7 +168,8 @@ def test_prefill_integer_exact_split_and_conv_state():
     assert np.array_equal(to_np(tp["zx"]), ref["zx"])
     assert np.array_equal(to_np(conv), ref["conv_state"])
     assert_bf16_close(to_np(tp["u"]), ref["u"], atol=1e-5, what="u")
-    assert_block_out(to_np(out), ref["out"])
+    assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
+    assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     blk.close()
 
 
@@ -187,7 +190,9 @@ def test_config1_decode_batch1(block0):
     assert_bf16_close(to_np(tp["zx"]), ref["zx"], atol=gemm_atol(ref["q"], Wt["in_proj"], Wt["s_x"] * Wt["s_w1"]),
                       what="zx")
     assert rel_l2(to_np(tp["u"]), ref["u"]) < 1e-3
-    assert_block_out(to_np(out), ref["out"])
+    assert_e4m3_close(to_np(tp["q2"]), ref["q2"], max_frac=1e-3)
+    assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
+    assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm)[0], ref["ssm_rows"][0])
     c = to_np(conv)[0]
     assert np.array_equal(c[:, :2], conv0[0][:, 1:])                      # shifted taps: exact copies
@@ -202,11 +207,14 @@ def test_config2_paged_decode_batch64(block0):
     slots = synth.make_slot_idx(2, n_slots, Bt)
     h = synth.make_hidden(2, Bt)
     conv, ssm = bf16_dev(conv0), f32_dev(ssm0)
-    out = blk.decode(bf16_dev(h), conv, ssm, torch.from_numpy(slots).cuda())
+    with q2_tap(blk, Bt) as q2:
+        out = blk.decode(bf16_dev(h), conv, ssm, torch.from_numpy(slots).cuda())
     torch.cuda.synchronize()
     blk.check()
-    ref = oracle.block_decode(Wt, h, conv0, ssm0, slots)
-    assert_block_out(to_np(out), ref["out"])
+    ref = oracle.block_decode(Wt, h, conv0, ssm0, slots, keep=True)
+    assert_e4m3_close(to_np(q2), ref["q2"])
+    assert_out_is_gemm(to_np(out), to_np(q2), gpu_out_proj(Wt))
+    assert_block_out(to_np(out), ref["out"], q2=to_np(q2), ref_q2=ref["q2"], Wt=Wt)
     ssm_np = ssm.cpu().numpy()
     conv_np = conv.cpu().to(torch.float32).numpy()
     assert_state(ssm_np[slots], ref["ssm_rows"])
@@ -226,13 +234,16 @@ def test_decode_padding_row_and_bad_slot_flag(block0):
     ssm0 = synth.make_ssm_state(3, n_slots)
     h = synth.make_hidden(3, 3)
     conv, ssm = bf16_dev(conv0), f32_dev(ssm0)
-    out = blk.decode(bf16_dev(h), conv, ssm, torch.tensor([2, -1, 0], dtype=torch.int32, device="cuda"))
+    with q2_tap(blk, 3) as q2:
+        out = blk.decode(bf16_dev(h), conv, ssm, torch.tensor([2, -1, 0], dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
     blk.check()
-    ref = oracle.block_decode(Wt, h, conv0, ssm0, np.array([2, -1, 0]))
+    ref = oracle.block_decode(Wt, h, conv0, ssm0, np.array([2, -1, 0]), keep=True)
     o = to_np(out)
-    assert np.all(o[1] == 0)
-    assert_block_out(o, ref["out"])
+    assert np.all(o[1] == 0) and np.all(to_np(q2)[1] == 0)
+    live = ref["live"]
+    assert_out_is_gemm(o, to_np(q2), gpu_out_proj(Wt))
+    assert_block_out(o[live], ref["out"][live], q2=to_np(q2)[live], ref_q2=ref["q2"], Wt=Wt)
     assert np.array_equal(ssm.cpu().numpy()[[1, 3]], ssm0[[1, 3]])
     # an id outside the pool is skipped on the device and reported by m2_check
     before = ssm.clone()
@@ -253,10 +264,13 @@ def test_varlen_prefill_ragged_with_initial_states(block0):
     rng_ssm = synth.make_ssm_state(11, len(lens))
     has = [1, 0, 1, 1, 0, 1]
     h = synth.make_hidden(11, sum(lens))
-    out, conv, ssm, _ = _run_prefill(blk, h, lens, rng_conv, rng_ssm, has_initial=has)
+    out, conv, ssm, tp = _run_prefill(blk, h, lens, rng_conv, rng_ssm, has_initial=has, taps=True)
     mask = np.array(has, np.float64)
-    ref = oracle.block_prefill(Wt, h, lens, rng_conv * mask[:, None, None], rng_ssm * mask[:, None, None, None])
-    assert_block_out(to_np(out), ref["out"])
+    ref = oracle.block_prefill(Wt, h, lens, rng_conv * mask[:, None, None], rng_ssm * mask[:, None, None, None],
+                               keep=True)
+    assert_e4m3_close(to_np(tp["q2"]), ref["q2"])
+    assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
+    assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])
     assert_bf16_close(to_np(conv), ref["conv_state"], atol=1e-3, what="conv_state")
 
@@ -267,13 +281,18 @@ def test_decode_after_prefill_carry(block0):
     Wt, blk = block0
     T, t0 = 40, 33
     h = synth.make_hidden(12, T)
-    out, conv, ssm, _ = _run_prefill(blk, h[:t0], [t0])
-    outs = [to_np(out)]
+    out, conv, ssm, tp = _run_prefill(blk, h[:t0], [t0], taps=True)
+    outs, q2s = [to_np(out)], [to_np(tp["q2"])]
     slot = torch.zeros(1, dtype=torch.int32, device="cuda")
     for t in range(t0, T):
-        outs.append(to_np(blk.decode(bf16_dev(h[t:t + 1]), conv, ssm, slot)))
-    ref = oracle.block_prefill(Wt, h, [T])
-    assert_block_out(np.concatenate(outs), ref["out"])
+        with q2_tap(blk, 1) as q2:
+            outs.append(to_np(blk.decode(bf16_dev(h[t:t + 1]), conv, ssm, slot)))
+        q2s.append(to_np(q2))
+    ref = oracle.block_prefill(Wt, h, [T], keep=True)
+    gemm = gpu_out_proj(Wt)
+    for o_, q_ in zip(outs, q2s):                 # each call's out_proj on its own codes
+        assert_out_is_gemm(o_, q_, gemm)
+    assert_block_out(np.concatenate(outs), ref["out"], q2=np.concatenate(q2s), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])
 
 
@@ -281,9 +300,11 @@ def test_config3_prefill_4x2048(block0):
     Wt, blk = block0
     lens = [2048] * 4
     h = synth.make_hidden(3, sum(lens))
-    out, conv, ssm, _ = _run_prefill(blk, h, lens)
-    ref = oracle.block_prefill(Wt, h, lens)
-    assert_block_out(to_np(out), ref["out"])
+    out, conv, ssm, tp = _run_prefill(blk, h, lens, taps=True)
+    ref = oracle.block_prefill(Wt, h, lens, keep=True)
+    assert_e4m3_close(to_np(tp["q2"]), ref["q2"])
+    assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
+    assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])
     assert_bf16_close(to_np(conv), ref["conv_state"], atol=1e-3, what="conv_state")
 

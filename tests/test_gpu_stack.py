@@ -2,20 +2,24 @@
 512-slot pool per layer, then varlen prefill {4096, 1024, 512, 37}, against the
 oracle's stack (h <- h + block(rmsnorm(h) * w), bf16 residual stream).
 
-Two checks per direction:
+Three checks per direction:
   * per layer, at the block tolerances: the GPU block l is run on the oracle's
-    own input to layer l (oracle -> GPU, never the other way), with that
-    layer's weights, pools and slot routing, and its output and states are
-    compared with the oracle's;
-  * end to end, the composition: the whole stack runs on the GPU from the
-    first input.  The e4m3 quantisation of each layer's input and of out_proj's
-    input turns last-bit differences into whole-code flips (FLIP_BOUND), and 23
-    layers compound them (measured in decode: layer-0 states agree to 3.5e-6,
-    layer-22 states to 2.5e-2, final output rel L2 4.9e-2; in prefill the
-    final states integrate every token's input: layer 1 1.05e-2, layer 6
-    1.15e-1), so the end-to-end check is a composition check: relative L2
-    <= 0.5 on the output and on every layer's states (a routing, residual or
-    per-layer-state error is O(1)).
+    own input to layer l (oracle -> GPU; no GPU value enters the oracle), with
+    that layer's weights, pools and slot routing; its output is out_proj of
+    its own codes (bit for bit against the standalone GEMM) and within the
+    stated bound plus what its differing out_proj codes move (helpers), its
+    states within the state bound;
+  * the composition: the whole-stack call equals, bit for bit, a layer-by-layer
+    replay of the same calls written out here (residual add, RMSNorm with layer
+    l's weight, block l on layer l's pools), in the output and every layer's
+    states, so the end-to-end run is exactly the per-layer blocks composed;
+  * end to end against the oracle, as a coarse guard: the e4m3 quantisation of
+    each layer's input and of out_proj's input turns last-bit differences into
+    whole-code flips, and 23 layers compound them (measured in decode: layer-0
+    states agree to 3.5e-6, layer-22 states to 2.5e-2, final output rel L2
+    4.9e-2; in prefill the final states integrate every token's input: layer 1
+    1.05e-2, layer 6 1.15e-1), so this one is rel L2 <= 0.5 on the output and
+    on every layer's states (a routing, residual or state error is O(1)).
 """
 import concurrent.futures as cf
 import multiprocessing as mp
@@ -27,7 +31,8 @@ import torch
 
 import oracle
 import synth
-from helpers import assert_block_out, assert_state, bf16_dev, device_weights, rel_l2, to_np
+from helpers import (assert_block_out, assert_out_is_gemm, assert_state, bf16_dev, device_weights, gpu_out_proj, q2_tap,
+                     rel_l2, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -72,26 +77,44 @@ def test_config4_stack_decode_b128_512_slots(stack):
     sel_conv = [p[sl].clone() for p in conv_pools]
     sel_ssm = [p[sl].clone() for p in ssm_pools]
     keep_ssm = [p[untouched].clone() for p in ssm_pools]
+    # the replay's copies of the selected rows, as compact pools of Bt slots
+    rep_conv = [c.clone() for c in sel_conv]
+    rep_ssm = [c.clone() for c in sel_ssm]
     h = synth.make_hidden(CFG, Bt)
     out = stk.decode(bf16_dev(h), conv_pools, ssm_pools, torch.from_numpy(slots).to(dev))
     torch.cuda.synchronize()
     for b in stk.blocks:
         b.check()
+    # composition: the same calls, layer by layer (rows renumbered 0..Bt-1)
+    ident_dev = torch.arange(Bt, dtype=torch.int32, device=dev)
+    hr = bf16_dev(h)
+    prev = None
+    for l in range(LAYERS):
+        x = m2.m2_rmsnorm_residual(hr, prev, stk.norm_ws[l], EPS)
+        prev = stk.blocks[l].decode(x, rep_conv[l], rep_ssm[l], ident_dev)
+    m2.m2_rmsnorm_residual(hr, prev, None, EPS, norm=False)
+    torch.cuda.synchronize()
+    assert torch.equal(hr, out)
+    for l in range(LAYERS):
+        assert torch.equal(rep_ssm[l], ssm_pools[l][sl]) and torch.equal(rep_conv[l], conv_pools[l][sl])
+    del rep_conv, rep_ssm
     e2e_rows = [p[sl].cpu().numpy() for p in ssm_pools]
     ident = np.arange(Bt)
-    ident_dev = torch.arange(Bt, dtype=torch.int32, device=dev)
     hh = h.astype(np.float64)
     for l in range(LAYERS):
         assert torch.equal(ssm_pools[l][untouched], keep_ssm[l])            # untouched slots byte-identical
         conv_rows = to_np(sel_conv[l])
         ssm_rows = sel_ssm[l].cpu().numpy()
         x = oracle.rmsnorm(hh, norm_ws_np[l], EPS)
-        r = oracle.block_decode(weights[l], x, conv_rows, ssm_rows, ident)
+        r = oracle.block_decode(weights[l], x, conv_rows, ssm_rows, ident, keep=True)
         # per layer, on the oracle's input to this layer
         c_pool, s_pool = sel_conv[l].clone(), sel_ssm[l].clone()
-        got = stk.blocks[l].decode(bf16_dev(x), c_pool, s_pool, ident_dev)
+        with q2_tap(stk.blocks[l], Bt) as q2:
+            got = stk.blocks[l].decode(bf16_dev(x), c_pool, s_pool, ident_dev)
         torch.cuda.synchronize()
-        assert_block_out(to_np(got), r["out"], what=f"decode layer {l} out")
+        assert_out_is_gemm(to_np(got), to_np(q2), gpu_out_proj(weights[l]), what=f"decode layer {l} out")
+        assert_block_out(to_np(got), r["out"], what=f"decode layer {l} out", q2=to_np(q2), ref_q2=r["q2"],
+                         Wt=weights[l])
         assert_state(s_pool.cpu().numpy(), r["ssm_rows"], what=f"decode layer {l} ssm rows")
         # end to end, on the GPU stack's own input
         e = rel_l2(e2e_rows[l], r["ssm_rows"])
@@ -115,23 +138,40 @@ def test_config4_stack_varlen_prefill(stack):
     for b in stk.blocks:
         b.check()
     ws = torch.empty(stk.blocks[0].prefill_workspace_size(lens), dtype=torch.uint8, device=dev)
+    # composition: the same calls, layer by layer
+    hr = bf16_dev(h)
+    prev = None
+    for l in range(LAYERS):
+        x = m2.m2_rmsnorm_residual(hr, prev, stk.norm_ws[l], EPS)
+        c1 = torch.zeros((4, 6144, 3), dtype=torch.bfloat16, device=dev)
+        s1 = torch.zeros((4, 64, 64, 128), dtype=torch.float32, device=dev)
+        prev = stk.blocks[l].prefill(x, lens, c1, s1, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(c1, conv[l]) and torch.equal(s1, ssm[l]), f"layer {l} states"
+    m2.m2_rmsnorm_residual(hr, prev, None, EPS, norm=False)
+    torch.cuda.synchronize()
+    assert torch.equal(hr, out)
     hh = h.astype(np.float64)
     # the oracle's recurrence runs group by group on a spawn pool (groups are
     # independent; each group's recurrence is still token by token)
     with cf.ProcessPoolExecutor(max_workers=min(8, os.cpu_count() or 1), mp_context=mp.get_context("spawn")) as ex:
         for l in range(LAYERS):
             x = oracle.rmsnorm(hh, norm_ws_np[l], EPS)
-            r = oracle.block_prefill(weights[l], x, lens, map_fn=ex.map)
+            r = oracle.block_prefill(weights[l], x, lens, map_fn=ex.map, keep=True)
             c1 = torch.zeros((4, 6144, 3), dtype=torch.bfloat16, device=dev)
             s1 = torch.zeros((4, 64, 64, 128), dtype=torch.float32, device=dev)
-            got = stk.blocks[l].prefill(bf16_dev(x), lens, c1, s1, workspace=ws)
+            with q2_tap(stk.blocks[l], sum(lens)) as q2:
+                got = stk.blocks[l].prefill(bf16_dev(x), lens, c1, s1, workspace=ws)
             torch.cuda.synchronize()
-            assert_block_out(to_np(got), r["out"], what=f"prefill layer {l} out")
+            assert_out_is_gemm(to_np(got), to_np(q2), gpu_out_proj(weights[l]), what=f"prefill layer {l} out")
+            assert_block_out(to_np(got), r["out"], what=f"prefill layer {l} out", q2=to_np(q2), ref_q2=r["q2"],
+                             Wt=weights[l])
             assert_state(to_np(s1), r["ssm_state"], what=f"prefill layer {l} final ssm state")
             e = rel_l2(to_np(ssm[l]), r["ssm_state"])
             print(f"prefill layer {l}: end-to-end final ssm state rel L2 {e:.3e}")
             assert e <= _e2e_state_bound(l), f"layer {l} end-to-end final state: rel L2 {e:.3e}"
             hh = oracle.bf16_round(hh + r["out"])
+            del r                      # the intermediates of 5669 tokens (float64) are large
     rl = rel_l2(to_np(out), hh)
     print(f"prefill stack output: end-to-end rel L2 {rl:.3e}")
     assert np.all(np.isfinite(to_np(out))) and rl <= 0.5

@@ -10,8 +10,8 @@ import torch
 
 import oracle
 import synth
-from helpers import (assert_bf16_close, assert_block_out, assert_state, bf16_dev, device_weights, f32_dev, rel_l2,
-                     to_np, u8_dev)
+from helpers import (assert_bf16_close, assert_block_out, assert_out_is_gemm, assert_state, bf16_dev, device_weights,
+                     f32_dev, gpu_out_proj, rel_l2, to_np, u8_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -107,7 +107,8 @@ def test_w8a16_prefill_varlen_and_separation(block_w8a16):
     assert_bf16_close(to_np(taps["zx"]), ref["zx"], atol=2.0 ** -16 * (np.abs(h) @ np.abs(wd).T), what="zx")
     assert rel_l2(to_np(taps["o"]), ref["o"]) < 1e-2
     got = to_np(out)
-    _, floor = assert_block_out(got, ref["out"])
+    assert_out_is_gemm(got, to_np(taps["o"]), gpu_out_proj(Wt, "w8a16"))
+    _, floor = assert_block_out(got, ref["out"], o=to_np(taps["o"]), ref_o=ref["o"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])
     assert_bf16_close(to_np(conv), ref["conv_state"], atol=1e-3, what="conv_state")
     # the W8A8 arm on the same inputs differs by the e4m3 activation quant:
@@ -126,13 +127,18 @@ def test_w8a16_paged_decode_with_padding_row(block_w8a16):
     slots = np.array([4, 11, -1, 0, 7, 15], np.int32)
     h = synth.make_hidden(3, len(slots))
     conv, ssm = bf16_dev(conv0), f32_dev(ssm0)
+    o_tap = torch.zeros((len(slots), 4096), dtype=torch.bfloat16, device="cuda")
+    blk.set_taps(o=o_tap)
     out = blk.decode(bf16_dev(h), conv, ssm, torch.from_numpy(slots).cuda())
+    blk.set_taps()
     torch.cuda.synchronize()
     blk.check()
-    ref = oracle.block_decode(Wt, h, conv0, ssm0, slots, arm="w8a16")
+    ref = oracle.block_decode(Wt, h, conv0, ssm0, slots, arm="w8a16", keep=True)
     got = to_np(out)
     assert np.all(got[2] == 0)                                  # padding row: output zero
-    assert_block_out(got, ref["out"])
+    lv = ref["live"]
+    assert_out_is_gemm(got, to_np(o_tap), gpu_out_proj(Wt, "w8a16"))
+    assert_block_out(got[lv], ref["out"][lv], o=to_np(o_tap)[lv], ref_o=ref["o"], Wt=Wt)
     live = slots[slots >= 0]
     ssm_np, conv_np = to_np(ssm), to_np(conv)
     assert_state(ssm_np[live], ref["ssm_rows"])
@@ -167,19 +173,28 @@ def test_w8a16_with_bf16_state_cache_carry():
     h = synth.make_hidden(6, T)
     conv = torch.zeros((1, 6144, 3), dtype=torch.bfloat16, device="cuda")
     ssm = torch.zeros((1, 64, 64, 128), dtype=torch.bfloat16, device="cuda")
+    o_tap = torch.zeros((T, 4096), dtype=torch.bfloat16, device="cuda")
+    blk.set_taps(o=o_tap[:t0])
     outs = [to_np(blk.prefill(bf16_dev(h[:t0]), [t0], conv, ssm))]
     slot = torch.zeros(1, dtype=torch.int32, device="cuda")
     for t in range(t0, T):
+        blk.set_taps(o=o_tap[t:t + 1])
         outs.append(to_np(blk.decode(bf16_dev(h[t:t + 1]), conv, ssm, slot)))
+    blk.set_taps()
     torch.cuda.synchronize()
     blk.check()
-    r = oracle.block_prefill(Wt, h[:t0], [t0], state_cache="bf16", arm="w8a16")
-    rc, rs, ro = r["conv_state"], r["ssm_state"], [r["out"]]
+    r = oracle.block_prefill(Wt, h[:t0], [t0], state_cache="bf16", arm="w8a16", keep=True)
+    rc, rs, ro, rso = r["conv_state"], r["ssm_state"], [r["out"]], [r["o"]]
     for t in range(t0, T):
-        d = oracle.block_decode(Wt, h[t:t + 1], rc, rs, np.array([0]), state_cache="bf16", arm="w8a16")
+        d = oracle.block_decode(Wt, h[t:t + 1], rc, rs, np.array([0]), state_cache="bf16", arm="w8a16", keep=True)
         rc, rs = d["conv_rows"], d["ssm_rows"]
         ro.append(d["out"])
-    assert_block_out(np.concatenate(outs), np.concatenate(ro))
+        rso.append(d["o"])
+    gemm, ot = gpu_out_proj(Wt, "w8a16"), to_np(o_tap)
+    assert_out_is_gemm(outs[0], ot[:t0], gemm)
+    for i, o_ in enumerate(outs[1:]):
+        assert_out_is_gemm(o_, ot[t0 + i:t0 + i + 1], gemm)
+    assert_block_out(np.concatenate(outs), np.concatenate(ro), o=to_np(o_tap), ref_o=np.concatenate(rso), Wt=Wt)
     assert_state(ssm.to(torch.float32).cpu().numpy()[0], rs[0])
     blk.close()
 
@@ -193,7 +208,8 @@ def test_w8a16_short_prefill_takes_the_few_row_gemm(block_w8a16):
     h = synth.make_hidden(8, T)
     conv = torch.zeros((2, 6144, 3), dtype=torch.bfloat16, device="cuda")
     ssm = torch.zeros((2, 64, 64, 128), dtype=torch.float32, device="cuda")
-    taps = dict(zx=torch.empty((T, 10304), dtype=torch.bfloat16, device="cuda"))
+    taps = dict(zx=torch.empty((T, 10304), dtype=torch.bfloat16, device="cuda"),
+                o=torch.empty((T, 4096), dtype=torch.bfloat16, device="cuda"))
     blk.set_taps(**taps)
     out = blk.prefill(bf16_dev(h), lens, conv, ssm)
     blk.set_taps()
@@ -202,5 +218,6 @@ def test_w8a16_short_prefill_takes_the_few_row_gemm(block_w8a16):
     ref = oracle.block_prefill(Wt, h, lens, keep=True, arm="w8a16")
     wd = oracle.dequant_e4m3_bf16(Wt["in_proj"], Wt["s_w1"])
     assert_bf16_close(to_np(taps["zx"]), ref["zx"], atol=2.0 ** -16 * (np.abs(h) @ np.abs(wd).T), what="zx")
-    assert_block_out(to_np(out), ref["out"])
+    assert_out_is_gemm(to_np(out), to_np(taps["o"]), gpu_out_proj(Wt, "w8a16"))
+    assert_block_out(to_np(out), ref["out"], o=to_np(taps["o"]), ref_o=ref["o"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])
