@@ -302,8 +302,8 @@ m2_status m2_decode_q(m2_handle* h, const uint8_t* hidden_q, int Bt, uint16_t* c
  * rows advance their pool rows in place, the prefill rows run the chunked
  * scan.  Bt = 0 or nseq = 0 is allowed (not both); the decode arguments may
  * be NULL when Bt = 0, the prefill ones when nseq = 0.  Of the intermediate
- * taps this call writes q, zx and q2 (Bt + sum(T) rows, in batch order); the
- * others are not written.  Errors as m2_decode and m2_prefill.
+ * taps this call writes q, zx, y, o and q2 (Bt + sum(T) rows, in batch
+ * order); u and dt are not written.  Errors as m2_decode and m2_prefill.
  */
 m2_status m2_mixed_workspace_size(const m2_handle* h, int Bt, const int32_t* seqlens_host, int nseq,
                                   size_t* bytes);

@@ -739,6 +739,7 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
     h->stats.kernel_launches += 1;
     if (fork_decode) {
       DecodeTaps dt{};
+      if (h->taps_on) dt.o = h->taps.o, dt.y = h->taps.y;
       M2_CUDA(launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err,
                                    dt, h->side));
       h->stats.kernel_launches += 1;
@@ -759,12 +760,14 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
                                    conv_state, st));
     M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
              launch_ssd_chunk_scan_tc(w.pf.u, w.pf.cumdt, w.pf.sin_img, bp, local, w.pf.y, h->err, st));
-    M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.pf.y, zx_pf, bp, T, q2_pf, nullptr, st));
+    uint16_t* o_tap = (h->taps_on && h->taps.o) ? h->taps.o + (size_t)Bt * kI : nullptr;
+    M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.pf.y, zx_pf, bp, T, q2_pf, o_tap, st));
   }
   if (fork_decode) {
     M2_CUDA(cudaStreamWaitEvent(st, h->join_ev, 0));
   } else if (Bt > 0) {
     DecodeTaps dt{};
+    if (h->taps_on) dt.o = h->taps.o, dt.y = h->taps.y;
     M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
              launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err,
                                   dt, st));
@@ -776,6 +779,7 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
     if ((s = copy_tap(h->taps.q, w.q, (size_t)R * kH, st))) return s;
     if ((s = copy_tap(h->taps.zx, w.zx, (size_t)R * kZ * 2, st))) return s;
     if ((s = copy_tap(h->taps.q2, w.q2, (size_t)R * kI, st))) return s;
+    if (h->taps.y && T > 0 && (s = copy_tap(h->taps.y + (size_t)Bt * kI, w.pf.y, (size_t)T * kI * 2, st))) return s;
   }
   if (T > 0) {
     h->stats.prefill_calls += 1;

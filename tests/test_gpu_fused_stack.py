@@ -46,8 +46,9 @@ def test_rmsnorm_residual_quant_equals_norm_then_quant(T):
     # against the oracle: RMSNorm in f64 then the e4m3 encoder (the bf16 normed
     # value may differ in its last bit, so a code may differ by one step)
     hs = oracle.bf16_round(h.astype(np.float64) + a)
-    ref = oracle.quant_static_e4m3(oracle.rmsnorm(hs, to_np(w), 1e-5), s_x)
-    assert_e4m3_close(to_np(q2), ref)
+    ref_normed = oracle.rmsnorm(hs, to_np(w), 1e-5)
+    ref = oracle.quant_static_e4m3(ref_normed, s_x)
+    assert_e4m3_close(to_np(q2), ref, to_np(normed2), ref_normed, s_x)
 
 
 def test_rmsnorm_residual_quant_without_add_and_normed():

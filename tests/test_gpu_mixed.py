@@ -9,7 +9,7 @@ import torch
 import oracle
 import synth
 from helpers import (assert_bf16_close, assert_block_out, assert_e4m3_close, assert_state, bf16_dev, device_weights,
-                     assert_out_is_gemm, f32_dev, gpu_out_proj, q2_tap, to_np)
+                     assert_out_is_gemm, f32_dev, gpu_out_proj, q2_tap, rel_l2, to_np)
 
 pytestmark = pytest.mark.gpu
 
@@ -40,8 +40,13 @@ def test_mixed_small_batch_vs_oracle(block0):
     h = np.concatenate([synth.make_hidden(2, Bt), synth.make_hidden(5, sum(lens))])
     cp, sp = bf16_dev(conv_pool0), f32_dev(ssm_pool0)
     cs, ss = bf16_dev(conv_st0), f32_dev(ssm_st0)
-    with q2_tap(blk, Bt + sum(lens)) as q2t:
-        out = blk.mixed(bf16_dev(h), Bt, cp, sp, torch.from_numpy(slots).cuda(), lens, cs, ss, has_initial=[1, 0])
+    R = Bt + sum(lens)
+    q2t = torch.zeros((R, 4096), dtype=torch.uint8, device="cuda")
+    o_t = torch.zeros((R, 4096), dtype=torch.bfloat16, device="cuda")
+    y_t = torch.zeros((R, 4096), dtype=torch.bfloat16, device="cuda")
+    blk.set_taps(q2=q2t, o=o_t, y=y_t)
+    out = blk.mixed(bf16_dev(h), Bt, cp, sp, torch.from_numpy(slots).cuda(), lens, cs, ss, has_initial=[1, 0])
+    blk.set_taps()
     torch.cuda.synchronize()
     blk.check()
     rd = oracle.block_decode(Wt, h[:Bt], conv_pool0, ssm_pool0, slots, keep=True)
@@ -49,7 +54,9 @@ def test_mixed_small_batch_vs_oracle(block0):
     rp = oracle.block_prefill(Wt, h[Bt:], lens, conv_st0 * mask[:, None, None], ssm_st0 * mask[:, None, None, None],
                               keep=True)
     o, q2 = to_np(out), to_np(q2t)
-    assert_e4m3_close(q2, np.concatenate([rd["q2"], rp["q2"]]))
+    assert rel_l2(to_np(y_t), np.concatenate([rd["y"], rp["y"]])) < 1e-3
+    assert_e4m3_close(q2, np.concatenate([rd["q2"], rp["q2"]]), to_np(o_t), np.concatenate([rd["o"], rp["o"]]),
+                      Wt["s_y"])
     assert_out_is_gemm(o, q2, gpu_out_proj(Wt))
     assert_block_out(o[:Bt], rd["out"], q2=q2[:Bt], ref_q2=rd["q2"], Wt=Wt)
     assert_block_out(o[Bt:], rp["out"], q2=q2[Bt:], ref_q2=rp["q2"], Wt=Wt)

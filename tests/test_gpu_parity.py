@@ -140,7 +140,7 @@ def test_config0_prefill_32_tokens_all_stages(block0):
     assert rel_l2(to_np(tp["dt"]), ref["dt"]) < 1e-4
     assert rel_l2(to_np(tp["y"]), ref["y"]) < 1e-2
     assert rel_l2(to_np(tp["o"]), ref["o"]) < 1e-2
-    assert_e4m3_close(to_np(tp["q2"]), ref["q2"])
+    assert_e4m3_close(to_np(tp["q2"]), ref["q2"], to_np(tp["o"]), ref["o"], Wt["s_y"])
     assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
     assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])
@@ -190,7 +190,7 @@ def test_config1_decode_batch1(block0):
     assert_bf16_close(to_np(tp["zx"]), ref["zx"], atol=gemm_atol(ref["q"], Wt["in_proj"], Wt["s_x"] * Wt["s_w1"]),
                       what="zx")
     assert rel_l2(to_np(tp["u"]), ref["u"]) < 1e-3
-    assert_e4m3_close(to_np(tp["q2"]), ref["q2"], max_frac=1e-3)
+    assert_e4m3_close(to_np(tp["q2"]), ref["q2"], to_np(tp["o"]), ref["o"], Wt["s_y"], max_frac=1e-3)
     assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
     assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm)[0], ref["ssm_rows"][0])
@@ -207,12 +207,15 @@ def test_config2_paged_decode_batch64(block0):
     slots = synth.make_slot_idx(2, n_slots, Bt)
     h = synth.make_hidden(2, Bt)
     conv, ssm = bf16_dev(conv0), f32_dev(ssm0)
-    with q2_tap(blk, Bt) as q2:
-        out = blk.decode(bf16_dev(h), conv, ssm, torch.from_numpy(slots).cuda())
+    o_tap = torch.zeros((Bt, 4096), dtype=torch.bfloat16, device="cuda")
+    q2 = torch.zeros((Bt, 4096), dtype=torch.uint8, device="cuda")
+    blk.set_taps(q2=q2, o=o_tap)
+    out = blk.decode(bf16_dev(h), conv, ssm, torch.from_numpy(slots).cuda())
+    blk.set_taps()
     torch.cuda.synchronize()
     blk.check()
     ref = oracle.block_decode(Wt, h, conv0, ssm0, slots, keep=True)
-    assert_e4m3_close(to_np(q2), ref["q2"])
+    assert_e4m3_close(to_np(q2), ref["q2"], to_np(o_tap), ref["o"], Wt["s_y"])
     assert_out_is_gemm(to_np(out), to_np(q2), gpu_out_proj(Wt))
     assert_block_out(to_np(out), ref["out"], q2=to_np(q2), ref_q2=ref["q2"], Wt=Wt)
     ssm_np = ssm.cpu().numpy()
@@ -268,7 +271,7 @@ def test_varlen_prefill_ragged_with_initial_states(block0):
     mask = np.array(has, np.float64)
     ref = oracle.block_prefill(Wt, h, lens, rng_conv * mask[:, None, None], rng_ssm * mask[:, None, None, None],
                                keep=True)
-    assert_e4m3_close(to_np(tp["q2"]), ref["q2"])
+    assert_e4m3_close(to_np(tp["q2"]), ref["q2"], to_np(tp["o"]), ref["o"], Wt["s_y"])
     assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
     assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])
@@ -302,7 +305,7 @@ def test_config3_prefill_4x2048(block0):
     h = synth.make_hidden(3, sum(lens))
     out, conv, ssm, tp = _run_prefill(blk, h, lens, taps=True)
     ref = oracle.block_prefill(Wt, h, lens, keep=True)
-    assert_e4m3_close(to_np(tp["q2"]), ref["q2"])
+    assert_e4m3_close(to_np(tp["q2"]), ref["q2"], to_np(tp["o"]), ref["o"], Wt["s_y"])
     assert_out_is_gemm(to_np(out), to_np(tp["q2"]), gpu_out_proj(Wt))
     assert_block_out(to_np(out), ref["out"], q2=to_np(tp["q2"]), ref_q2=ref["q2"], Wt=Wt)
     assert_state(to_np(ssm), ref["ssm_state"])

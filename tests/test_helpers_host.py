@@ -10,28 +10,37 @@ def _codes(vals):
     return oracle.e4m3_encode(np.asarray(vals, np.float64))
 
 
-def test_e4m3_close_accepts_adjacent_and_near_zero_codes():
-    ref = _codes(np.linspace(-3, 3, 4000))
-    got = ref.copy()
-    got[10] = ref[10] + 1                                                    # the next magnitude code
-    i = int(np.argmin(np.abs(oracle.e4m3_decode(ref))))                      # the code nearest zero
-    got[i] = _codes([oracle.e4m3_decode(ref[i:i + 1])[0] + 3 * 2.0 ** -9])[0]  # three uniform steps away
-    assert_e4m3_close(got, ref, max_frac=1e-3)
+
+def _quant(o, s):
+    return oracle.quant_static_e4m3(o, s)
 
 
-def test_e4m3_close_rejects_two_steps_away_from_zero():
-    ref = _codes(np.full(2000, 1.0))
-    got = ref.copy()
-    got[5] = _codes([1.25])[0]                  # two codes above 1.0 (steps of 0.125)
-    with pytest.raises(AssertionError, match="more than one step"):
-        assert_e4m3_close(got, ref, max_frac=1e-3)
+def test_e4m3_close_accepts_codes_their_inputs_explain():
+    rng = np.random.default_rng(0)
+    s = 1.0 / 32
+    ref_o = oracle.bf16_round(rng.standard_normal(4000))
+    got_o = ref_o.copy()
+    got_o[10] = oracle.bf16_round(ref_o[10] * (1 + 2.0 ** -7))      # one bf16 step: at most one code
+    got_o[20] = ref_o[20] + 0.01                                     # a small value moved by an upstream step
+    assert_e4m3_close(_quant(got_o, s), _quant(ref_o, s), got_o, ref_o, s, max_frac=1e-3, o_rel_l2=1e-2)
+
+
+def test_e4m3_close_rejects_codes_their_inputs_do_not_explain():
+    rng = np.random.default_rng(1)
+    s = 1.0 / 32
+    o = oracle.bf16_round(rng.standard_normal(2000))
+    g = _quant(o, s)
+    g[5] = g[5] + 2 if (g[5] & 0x7F) < 0x70 else g[5] - 2         # two codes off, same input
+    with pytest.raises(AssertionError, match="not the e4m3 rounding"):
+        assert_e4m3_close(g, _quant(o, s), o, o, s)
 
 
 def test_e4m3_close_rejects_too_many_differences():
-    ref = _codes(np.full(100, 1.0))
-    got = _codes(np.full(100, 1.125))
-    with pytest.raises(AssertionError, match="of codes differ"):
-        assert_e4m3_close(got, ref)
+    s = 1.0
+    ref_o = np.full(100, 1.0)
+    got_o = np.full(100, 1.125)
+    with pytest.raises(AssertionError):
+        assert_e4m3_close(_quant(got_o, s), _quant(ref_o, s), got_o, ref_o, s, o_rel_l2=1.0)
 
 
 def _out_case(seed=0, T=40, H=48, K=256):
