@@ -852,12 +852,8 @@ def run_configs(args):
              s_x=Wt["s_x"], s_y=Wt["s_y"], eps=Wt["eps"])
     blk = m2.Mamba2Mixer(w, device=dev)
     pk = peaks() or {}
-    hbm = pk.get("hbm_gbs")
-    fp8_peak = None
-    try:
-        fp8_peak = float(json.load(open(os.path.join(ROOT, "profiles", "fp8_gemm_peak.json")))["fp8_tflops_sustained"])
-    except Exception:
-        pass
+    hbm = pk.get("hbm_gbs") or 6800.0
+    fp8_peak = 2.0 * (pk.get("bf16_tflops") or 1900.0)   # e4m3 = 2 x the measured bf16 burst
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     W_BYTES = Z * H + H * I
     STATE_ROW = 64 * 64 * 128 * 4
@@ -904,7 +900,7 @@ def run_configs(args):
         if cfg == 0:
             byts = W_BYTES + T * H * 2 * 2 + len(lens) * (STATE_ROW + CONV_ROW)
             r.update(algorithmic_bytes=byts, gbs=byts / (ms * 1e-3) / 1e9,
-                     frac_of_hbm=(byts / (ms * 1e-3) / 1e9 / hbm) if hbm else None)
+                     frac_of_hbm=byts / (ms * 1e-3) / 1e9 / hbm, frac_of_8tbs=byts / (ms * 1e-3) / 1e9 / 8000.0)
         else:
             flop = 2.0 * T * (Z * H + H * I)
             blk.profile(True)
@@ -917,7 +913,8 @@ def run_configs(args):
             gemm_ms = (st["in_proj"][0] + st["out_proj"][0]) / args.steps
             tf = flop / (gemm_ms * 1e-3) / 1e12
             r.update(projection_flop=flop, projections_ms=gemm_ms, projections_tflops=tf,
-                     frac_of_fp8=(tf / fp8_peak) if fp8_peak else None)
+                     frac_of_fp8=tf / fp8_peak, frac_of_fp8_nominal=tf / 4500.0,
+                     stages_us={k: 1e3 * v[0] / args.steps for k, v in st.items()})
         res[str(cfg)] = r
     # 1 and 2: decode
     for cfg, n_slots, Bt in ((1, 1, 1), (2, N_SLOTS, DEC_B)):
@@ -929,12 +926,25 @@ def run_configs(args):
         ws = torch.empty(blk.decode_workspace_size(Bt), dtype=torch.uint8, device=dev)
         ms, nl = timed(lambda: blk.decode(h, conv_pool, ssm_pool, slots, out=out, workspace=ws))
         byts = W_BYTES + Bt * (2 * STATE_ROW + 2 * CONV_ROW + 2 * H * 2)
+        # per-stage times (a separate, event-bracketed pass)
+        blk.profile(True)
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            blk.decode(h, conv_pool, ssm_pool, slots, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        st = blk.profile_read()
+        blk.profile(False)
         res[str(cfg)] = dict(workload=f"decode {Bt} row(s) from a {n_slots}-slot pool", ms=ms,
                              tokens_per_s=Bt / (ms * 1e-3), launches=nl, algorithmic_bytes=byts,
-                             gbs=byts / (ms * 1e-3) / 1e9, frac_of_hbm=(byts / (ms * 1e-3) / 1e9 / hbm) if hbm else None)
+                             gbs=byts / (ms * 1e-3) / 1e9, frac_of_hbm=byts / (ms * 1e-3) / 1e9 / hbm,
+                             frac_of_8tbs=byts / (ms * 1e-3) / 1e9 / 8000.0,
+                             stages_us={k: 1e3 * v[0] / args.steps for k, v in st.items()})
     blk.close()
     print(json.dumps(dict(case="configs", launch="cuda_graph", l2="flushed before each step",
-                          peaks=dict(hbm_gbs=hbm, fp8_tflops=fp8_peak), results=res)))
+                          peaks=dict(hbm_gbs=hbm, fp8_tflops=fp8_peak,
+                                     note="MEASURED_PEAKS hbm_gbs and 2 x bf16_tflops; frac_of_8tbs and "
+                                          "frac_of_fp8_nominal against 8000 GB/s and 4500 TFLOP/s"),
+                          results=res)))
 
 
 def run_case(args):
@@ -955,6 +965,23 @@ def run_case(args):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         for _ in range(args.steps):
             m2.fp8_linear(a, 1.0 / 64, w, 0.01, y=y)
+    elif args.case == "decode1":
+        # one decode row from its own state (the single-row decode workload)
+        import synth
+        Wt = synth.make_weights(0)
+        blk = m2.Mamba2Mixer({k: (v.to(dev) if isinstance(v, torch.Tensor) else v)
+                              for k, v in _weights_torch(Wt).items()}, device=dev)
+        conv = torch.from_numpy(synth.make_conv_state(1, 1)).to(torch.bfloat16).to(dev)
+        ssm = torch.from_numpy(synth.make_ssm_state(1, 1)).to(dev)
+        h = torch.from_numpy(synth.make_hidden(1, 1)).to(torch.bfloat16).to(dev)
+        slot = torch.zeros(1, dtype=torch.int32, device=dev)
+        out = torch.empty((1, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(max(blk.decode_workspace_size(1), 256), dtype=torch.uint8, device=dev)
+        for _ in range(args.steps):
+            blk.decode(h, conv, ssm, slot, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        blk.check()
+        blk.close()
     else:
         ctx = build_workload(dev)
         for _ in range(args.steps):
@@ -965,6 +992,17 @@ def run_case(args):
     torch.cuda.synchronize()
 
 
+def _weights_torch(Wt):
+    """The block's weights as host torch tensors in their device dtypes."""
+    import numpy as np
+    import torch
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16)
+    return dict(in_proj=torch.from_numpy(Wt["in_proj"]), s_w1=Wt["s_w1"], out_proj=torch.from_numpy(Wt["out_proj"]),
+                s_w2=Wt["s_w2"], conv_w=bf(Wt["conv_w"]), conv_b=None, A_log=torch.from_numpy(Wt["A_log"]),
+                D=torch.from_numpy(Wt["D"]), dt_bias=torch.from_numpy(Wt["dt_bias"]), norm_w=bf(Wt["norm_w"]),
+                s_x=Wt["s_x"], s_y=Wt["s_y"], eps=Wt["eps"])
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -972,7 +1010,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "prefill", "stack", "decode_bf16", "arms",
+    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "decode1", "prefill", "stack", "decode_bf16", "arms",
                                        "configs"],
                     default=None,
                     help="run one kernel family at the workload shape (for profiler captures); prints nothing")

@@ -11,10 +11,11 @@ size_t gemm_workspace_bytes(int M, int N, int K);
 size_t gemm_workspace_bytes_bf16(int M, int N, int K);
 // *launches receives the number of kernels launched.
 // err: device error word for bounded-wait timeouts (may be null).
+// w_static: B (the weights) is never written by a kernel of the stream.
 cudaError_t gemm_fp8(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale,
-                     void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches);
+                     void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches, bool w_static = false);
 cudaError_t gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, int N, int K, float scale,
-                      void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches);
+                      void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches, bool w_static = false);
 
 // tensor-core kernels (gemm_tc.cu); Kbytes = K x operand size
 size_t gemm_tc_skinny_workspace(int Mtok, int N, int Kbytes);
@@ -22,6 +23,14 @@ cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int 
                            void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches);
 cudaError_t gemm_tc_skinny_bf16(const uint16_t* X, const uint16_t* W, uint16_t* y, int Mtok, int N, int K,
                                 float scale, void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches);
+// Up to kFewRowMax rows: K split across a cluster, partials added in
+// distributed shared memory (no scratch).  w_static: no kernel of the stream
+// writes W (so its first tiles may be fetched before the previous kernel ends).
+constexpr int kFewRowMax = 128;
+cudaError_t gemm_tc_fewrow(const uint8_t* X, const uint8_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
+                           bool w_static, int* err, cudaStream_t st);
+cudaError_t gemm_tc_fewrow_bf16(const uint16_t* X, const uint16_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
+                                bool w_static, int* err, cudaStream_t st);
 cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
                         cudaStream_t st);
 cudaError_t gemm_tc_big_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, int N, int K, float scale,

@@ -11,10 +11,14 @@
 //   two TMEM accumulators, warps 2-5 drain the other accumulator
 //   (tcgen05.ld), scale, round to bf16 and store, so the epilogue of tile i
 //   overlaps the MMAs of tile i+1.
-// k_gemm_tc_skinny (decode, few rows): the weight matrix is the MMA's
+// k_gemm_fewrow (decode, up to 128 rows): the weight matrix is the MMA's
 //   128-row A operand and the few activation rows are its N operand
-//   (D^T = W . X^T), with the K dimension split across CTAs so every SM
-//   streams weights; f32 partials are summed by k_splitk_reduce.
+//   (D^T = W . X^T); the K dimension is split across the CTAs of a cluster so
+//   every SM streams weights, and the partial sums are added in distributed
+//   shared memory.
+// k_gemm_tc_skinny (129 to 256 rows, and the allocation-free entry point):
+//   the same swap-AB tiles with K split across independent CTAs; f32 partials
+//   in global scratch are summed by k_splitk_reduce.
 // Every mbarrier wait is bounded: a wait that runs out raises the CTA's abort
 // flag and the device error word, the roles leave their loops, outstanding
 // copies and MMAs are drained with bounded waits, and TMEM is freed.
@@ -380,6 +384,193 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Few-row GEMM with K split across a thread-block cluster (decode
+// projections, Mtok <= 128).  CTA rank r of a cluster of S CTAs (the cluster
+// spans grid x; grid y walks the 128-row weight blocks) computes, swap-AB as
+// k_gemm_tc_skinny, D^T[n, m] = sum over k-blocks [r K/S, (r+1) K/S) of
+// W[n, k] X[m, k].  The partial sums meet in distributed shared memory: each
+// CTA copies its accumulator into its own pipeline memory (idle by then),
+// the cluster synchronises, and CTA r sums rows [128 r / S, 128 (r+1) / S) of
+// the block over the S ranks in rank order (the same order every call),
+// scales, rounds to bf16 and stores y.  No global scratch, no second kernel.
+// w_static: no kernel of the stream writes the weights (the handle's own
+// copies), so the first ring stages of weights are requested before waiting
+// on the previous kernel and stream while it finishes.
+// Every thread of every CTA reaches both cluster barriers, after an abort
+// too (the sums of an aborted call are then wrong and the error word says so).
+// ---------------------------------------------------------------------------
+template <int BNT, int STAGES, bool kBf16>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_fewrow(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                  uint16_t* __restrict__ y, int Mtok, int N, int K, float scale, int w_static, int* err) {
+  static_assert(BNT % 16 == 0 && BNT >= 16 && BNT <= 128, "BNT");
+  constexpr uint32_t A_BYTES = kBM * kBK;
+  constexpr uint32_t B_BYTES = BNT * kBK;
+  constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  constexpr uint32_t TMEM_COLS = BNT <= 32 ? 32 : (BNT <= 64 ? 64 : 128);
+  constexpr uint32_t IDESC = idesc_f32acc(kBM, BNT, kBf16 ? 1u : 0u);
+  constexpr int ES = kBf16 ? 2 : 1;
+  constexpr int RED_LD = BNT + 4;   // floats per exchange row (padding spreads the rows over the banks)
+  static_assert(kBM * RED_LD * 4 <= (int)(STAGES * STAGE_BYTES), "the exchange buffer fits in the ring");
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_align<1024>(smem_raw);
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  float* red = reinterpret_cast<float*>(smem);   // [128 weight rows][RED_LD], over the ring once it is idle
+  volatile int* abort = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = (int)gridDim.x;
+  const int rank = (int)cluster_ctarank();
+  const int n0 = blockIdx.y * kBM;
+  const int kblocks = (K * ES + kBK - 1) / kBK;
+  const int kb0 = rank * kblocks / S;
+  const int nk = (rank + 1) * kblocks / S - kb0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&ctl->full[s], 1);
+      mbar_init(&ctl->empty[s], 1);
+    }
+    mbar_init(&ctl->tfull[0], 1);
+    mbar_init(&ctl->drain, 1);
+    ctl->abort = 0;
+    fence_mbar_init();
+    tma_prefetch(&tmW);
+    tma_prefetch(&tmX);
+  }
+  if (warp == 1) {
+    tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer: ring slot i holds k-block kb0 + i
+      const int npre = nk < STAGES ? nk : STAGES;
+      if (w_static)
+        for (int i = 0; i < npre; ++i) {
+          mbar_expect_tx(&ctl->full[i], STAGE_BYTES);
+          tma_load_2d(smem + i * STAGE_BYTES, &tmW, &ctl->full[i], (kb0 + i) * (kBK / ES), n0);
+        }
+      pdl_wait();      // the activations are produced by the previous kernel
+      pdl_trigger();
+      for (int i = 0; i < npre; ++i) {
+        if (!w_static) {
+          mbar_expect_tx(&ctl->full[i], STAGE_BYTES);
+          tma_load_2d(smem + i * STAGE_BYTES, &tmW, &ctl->full[i], (kb0 + i) * (kBK / ES), n0);
+        }
+        tma_load_2d(smem + i * STAGE_BYTES + A_BYTES, &tmX, &ctl->full[i], (kb0 + i) * (kBK / ES), 0);
+      }
+      int issued = npre;
+      for (int i = npre; i < nk; ++i) {
+        const int stg = i % STAGES;
+        const uint32_t use = (uint32_t)(i / STAGES);
+        if (!mbar_wait(&ctl->empty[stg], (use & 1u) ^ 1u, abort)) {
+          raise_abort(ctl, err);
+          break;
+        }
+        uint8_t* sA = smem + stg * STAGE_BYTES;
+        mbar_expect_tx(&ctl->full[stg], STAGE_BYTES);
+        tma_load_2d(sA, &tmW, &ctl->full[stg], (kb0 + i) * (kBK / ES), n0);
+        tma_load_2d(sA + A_BYTES, &tmX, &ctl->full[stg], (kb0 + i) * (kBK / ES), 0);
+        issued = i + 1;
+      }
+      if (*abort)   // let the copies in flight land before the CTA can exit
+        for (int j = issued > STAGES ? issued - STAGES : 0; j < issued; ++j)
+          mbar_wait(&ctl->full[j % STAGES], (uint32_t)(j / STAGES) & 1u, nullptr, 100000000ull);
+    }
+  } else {
+    pdl_wait();
+    pdl_trigger();
+    if (warp == 1) {
+      if (lane == 0) {
+        // ---------------- MMA issuer
+        bool ok = true;
+        for (int i = 0; i < nk; ++i) {
+          const int stg = i % STAGES;
+          if (!mbar_wait(&ctl->full[stg], (uint32_t)(i / STAGES) & 1u, abort)) {
+            raise_abort(ctl, err);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stg * STAGE_BYTES);
+          const uint64_t adesc = desc_kmajor_sw128(a_addr);
+          const uint64_t bdesc = desc_kmajor_sw128(a_addr + A_BYTES);
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k)
+            mma_k32b<kBf16>(tmem_base, adesc + 2 * k, bdesc + 2 * k, IDESC, (i | k) != 0);
+          mma_commit(&ctl->empty[stg]);
+        }
+        if (ok && nk > 0) {
+          mma_commit(&ctl->tfull[0]);
+        } else {
+          mma_commit(&ctl->drain);
+          mbar_wait(&ctl->drain, 0, nullptr, 100000000ull);
+        }
+      }
+    } else {
+      // ---------------- epilogue warps 2..5: accumulator rows -> own exchange buffer
+      const int quarter = warp & 3;
+      float* dst = red + (quarter * 32 + lane) * RED_LD;
+      if (nk > 0 && mbar_wait(&ctl->tfull[0], 0, abort)) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < BNT; c += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(dst + c + 4 * q) =
+                make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]), __uint_as_float(r[4 * q + 2]),
+                            __uint_as_float(r[4 * q + 3]));
+        }
+        tc_fence_before();
+      } else {
+        if (nk > 0) raise_abort(ctl, err);
+        for (int c = 0; c < BNT; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  }
+  __syncwarp();
+  cluster_sync();   // every CTA's partial sits in its exchange buffer
+  {
+    // this CTA's rows of the block, summed over the ranks in rank order;
+    // consecutive threads take consecutive weight rows (coalesced stores)
+    const int r0 = rank * kBM / S, rows = (rank + 1) * kBM / S - r0;
+    const int quads = (Mtok + 3) >> 2;
+    const uint32_t red_s = smem_u32(red);
+    for (int idx = threadIdx.x; idx < rows * quads; idx += kThreads) {
+      const int nl = r0 + idx % rows, m = 4 * (idx / rows);
+      const uint32_t off = red_s + (uint32_t)((nl * RED_LD + m) * 4);
+      float4 acc = ld_dsmem_f32x4(cluster_map(off, 0));
+      for (int r = 1; r < S; ++r) {
+        const float4 v = ld_dsmem_f32x4(cluster_map(off, (uint32_t)r));
+        acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
+      }
+      const int n = n0 + nl;
+      if (n < N) {
+        uint16_t* yc = y + (size_t)m * N + n;
+        yc[0] = f2bfbits(acc.x * scale);
+        if (m + 1 < Mtok) yc[N] = f2bfbits(acc.y * scale);
+        if (m + 2 < Mtok) yc[2 * (size_t)N] = f2bfbits(acc.z * scale);
+        if (m + 3 < Mtok) yc[3 * (size_t)N] = f2bfbits(acc.w * scale);
+      }
+    }
+  }
+  cluster_sync();   // no CTA leaves while another still reads its buffer
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
 // y[m, n] = bf16(scale * sum_s partial[s][m][n]); 4 columns per thread, or
 // one when the sizes or y's alignment do not allow vectors.
 __global__ void __launch_bounds__(256) k_splitk_reduce(const float* __restrict__ partial, int splits, int Mtok, int N,
@@ -524,6 +715,61 @@ cudaError_t launch_skinny(const void* X, const void* W, uint16_t* y, float* part
                     scale, err);
 }
 
+// Cluster size of the few-row GEMM: as many K splits as keep every CTA
+// resident in one wave (CTAs per SM from the shared-memory footprint, with a
+// margin for cluster placement), at most 8 (the portable cluster size), and
+// at least two k-blocks per CTA.
+int fewrow_splits(int N, int kblocks, size_t smem) {
+  const int nb = (N + kBM - 1) / kBM;
+  int per_sm = (int)((228 * 1024) / (smem + 1024));
+  if (per_sm < 1) per_sm = 1;
+  int s = (int)(0.9 * per_sm * num_sms() / nb);
+  if (s > 8) s = 8;
+  if (s > kblocks / 2) s = kblocks / 2;
+  return s < 1 ? 1 : s;
+}
+
+template <int BNT, int STAGES, bool kBf16>
+cudaError_t launch_fewrow(const void* X, const void* W, uint16_t* y, int Mtok, int N, int K, float scale,
+                          bool w_static, int* err, cudaStream_t st) {
+  CUtensorMap tw, tx;
+  cudaError_t e;
+  constexpr int es = kBf16 ? 2 : 1;
+  if ((e = make_map(&tw, W, N, K, kBM, es)) != cudaSuccess) return e;
+  if ((e = make_map(&tx, X, Mtok, K, BNT, es)) != cudaSuccess) return e;
+  const size_t smem = 1024 + (size_t)STAGES * (kBM + BNT) * kBK + sizeof(Ctl);
+  auto k = k_gemm_fewrow<BNT, STAGES, kBf16>;
+  if ((e = set_smem(k, smem)) != cudaSuccess) return e;
+  const int kblocks = (K * es + kBK - 1) / kBK;
+  const int S = fewrow_splits(N, kblocks, smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(S, (N + kBM - 1) / kBM);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = S;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k, tw, tx, y, Mtok, N, K, scale, (int)w_static, err);
+}
+
+template <bool kBf16>
+cudaError_t fewrow_t(const void* X, const void* W, uint16_t* y, int Mtok, int N, int K, float scale, bool w_static,
+                     int* err, cudaStream_t st) {
+  const int bnt = (Mtok + 15) / 16 * 16;
+  if (bnt <= 16) return launch_fewrow<16, 4, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
+  if (bnt <= 32) return launch_fewrow<32, 4, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
+  if (bnt <= 64) return launch_fewrow<64, 4, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
+  if (bnt <= 128) return launch_fewrow<128, 3, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 // Split plan of the skinny GEMM for (Mtok, N, Kbytes = K x operand size):
@@ -604,6 +850,16 @@ cudaError_t gemm_tc_skinny(const uint8_t* X, const uint8_t* W, uint16_t* y, int 
 cudaError_t gemm_tc_skinny_bf16(const uint16_t* X, const uint16_t* W, uint16_t* y, int Mtok, int N, int K,
                                 float scale, void* ws, size_t ws_bytes, int* err, cudaStream_t st, int* launches) {
   return skinny_t<true>(X, W, y, Mtok, N, K, scale, ws, ws_bytes, err, st, launches);
+}
+
+cudaError_t gemm_tc_fewrow(const uint8_t* X, const uint8_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
+                           bool w_static, int* err, cudaStream_t st) {
+  return fewrow_t<false>(X, W, y, Mtok, N, K, scale, w_static, err, st);
+}
+
+cudaError_t gemm_tc_fewrow_bf16(const uint16_t* X, const uint16_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
+                                bool w_static, int* err, cudaStream_t st) {
+  return fewrow_t<true>(X, W, y, Mtok, N, K, scale, w_static, err, st);
 }
 
 cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,

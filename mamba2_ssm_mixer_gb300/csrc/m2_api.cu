@@ -441,12 +441,12 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
   const uint8_t* q = hidden_q ? hidden_q : w.q;
   if (w8a16) {
     M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
-             gemm_bf16(hidden, h->in_proj_bf16, w.zx, T, kZ, kH, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+             gemm_bf16(hidden, h->in_proj_bf16, w.zx, T, kZ, kH, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   } else {
     if (!hidden_q)
       M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)T * kH, h->cfg.s_x, w.q, st));
     M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
-             gemm_fp8(q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+             gemm_fp8(q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   }
   // the cumsum reads only the in_proj output: it runs on the second stream
   // beside the conv (serially while stage profiling)
@@ -475,12 +475,12 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
     // the bf16 normed output feeds out_proj (the e4m3 codes are written too, unused)
     M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, w.o, st));
     M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl,
-             gemm_bf16(w.o, h->out_proj_bf16, out, T, kH, kI, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+             gemm_bf16(w.o, h->out_proj_bf16, out, T, kH, kI, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   } else {
     M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1,
              launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, h->taps_on ? h->taps.o : nullptr, st));
     M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl,
-             gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+             gemm_fp8(w.q2, h->out_proj, out, T, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   }
   if (h->taps_on) {
     if (w8a16) {
@@ -579,7 +579,7 @@ static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t
   const uint8_t* q = hidden_q ? hidden_q : w.q;
   if (w8a16) {
     M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl,
-             gemm_bf16(hidden, h->in_proj_bf16, w.zx, Bt, kZ, kH, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+             gemm_bf16(hidden, h->in_proj_bf16, w.zx, Bt, kZ, kH, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
     // the kernel writes the bf16 normed rows through its o output, which
     // skips padding rows: those stay zero, so their output rows are zero
     M2_CUDA(cudaMemsetAsync(w.o, 0, (size_t)Bt * kI * 2, st));
@@ -588,17 +588,17 @@ static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t
     if (!hidden_q)
       M2_STAGE(h, st, M2_STAGE_DEC_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)Bt * kH, h->cfg.s_x, w.q, st));
     M2_STAGE(h, st, M2_STAGE_DEC_IN_PROJ, nl,
-             gemm_fp8(q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+             gemm_fp8(q, h->in_proj, w.zx, Bt, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   }
   M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, 1,
            launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, h->cfg.ssm_dtype == M2_DTYPE_BF16, n_slots, slot_idx,
                                 Bt, w.q2, h->err, dt, st));
   if (w8a16) {
     M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl,
-             gemm_bf16(w.o, h->out_proj_bf16, out, Bt, kH, kI, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+             gemm_bf16(w.o, h->out_proj_bf16, out, Bt, kH, kI, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   } else {
     M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl,
-             gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+             gemm_fp8(w.q2, h->out_proj, out, Bt, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   }
   if (h->taps_on) {
     m2_status s;
@@ -722,7 +722,7 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
   int nl = 0;
   M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)R * kH, h->cfg.s_x, w.q, st));
   M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
-           gemm_fp8(w.q, h->in_proj, w.zx, R, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+           gemm_fp8(w.q, h->in_proj, w.zx, R, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   // A second stream runs, beside the prefill rows' conv and scan, the
   // prefill cumsum (it reads only the in_proj output) and then the decode
   // rows' state stream (HBM-bound; the scan is latency-bound and its last
@@ -773,7 +773,7 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
                                   dt, st));
   }
   M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl,
-           gemm_fp8(w.q2, h->out_proj, out, R, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl));
+           gemm_fp8(w.q2, h->out_proj, out, R, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   if (h->taps_on) {   // the row-aligned intermediates, in batch order
     m2_status s;
     if ((s = copy_tap(h->taps.q, w.q, (size_t)R * kH, st))) return s;
