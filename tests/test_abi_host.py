@@ -134,10 +134,14 @@ def test_w8a16_ops_refuse_bad_arguments(m2):
     assert m2._lib.bf16_linear(16, 16, 0.0, 16, 4, 4, 32, None, 0, None) == m2.M2_EINVAL
     n, n8 = ctypes.c_size_t(), ctypes.c_size_t()
     assert m2._lib.bf16_linear_workspace_size(8, 8, 20, ctypes.byref(n)) == m2.M2_ESHAPE
-    # split-K partials of a decode-sized problem: f32 [splits, M, N]
-    assert m2._lib.bf16_linear_workspace_size(64, 10304, 2688, ctypes.byref(n)) == m2.M2_OK
-    assert m2._lib.fp8_linear_workspace_size(64, 10304, 2688, ctypes.byref(n8)) == m2.M2_OK
-    assert n.value % (64 * 10304 * 4) == 0 and n8.value % (64 * 10304 * 4) == 0
+    # up to 128 rows the partial sums meet in distributed shared memory: no workspace
+    assert m2._lib.bf16_linear_workspace_size(64, 10304, 2688, ctypes.byref(n)) == m2.M2_OK and n.value == 0
+    assert m2._lib.fp8_linear_workspace_size(128, 10304, 2688, ctypes.byref(n8)) == m2.M2_OK and n8.value == 0
+    # 129-256 rows: split-K partials in the workspace, f32 [splits, M, N]
+    assert m2._lib.bf16_linear_workspace_size(200, 10304, 2688, ctypes.byref(n)) == m2.M2_OK
+    assert m2._lib.fp8_linear_workspace_size(200, 10304, 2688, ctypes.byref(n8)) == m2.M2_OK
+    assert n.value > 0 and n8.value > 0
+    assert n.value % (200 * 10304 * 4) == 0 and n8.value % (200 * 10304 * 4) == 0
     assert m2._lib.bf16_linear_workspace_size(4096, 10304, 2688, ctypes.byref(n)) == m2.M2_OK and n.value == 0
 
 

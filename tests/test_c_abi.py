@@ -42,8 +42,10 @@ int main(void) {
   CHECK(fp8_quant(NULL, 16, 1.0f, NULL, NULL) == M2_EINVAL);
   CHECK(fp8_dequant(NULL, 16, 1.0f, NULL, NULL) == M2_EINVAL);
   CHECK(fp8_linear_workspace_size(8, 8, 20, &n) == M2_ESHAPE);
-  CHECK(fp8_linear_workspace_size(64, 10304, 2688, &n) == M2_OK && n > 0);
-  CHECK(bf16_linear_workspace_size(64, 10304, 2688, &n) == M2_OK && n > 0);
+  CHECK(fp8_linear_workspace_size(64, 10304, 2688, &n) == M2_OK && n == 0);
+  CHECK(fp8_linear_workspace_size(200, 10304, 2688, &n) == M2_OK && n > 0);
+  CHECK(bf16_linear_workspace_size(64, 10304, 2688, &n) == M2_OK && n == 0);
+  CHECK(bf16_linear_workspace_size(200, 10304, 2688, &n) == M2_OK && n > 0);
   CHECK(bf16_linear(NULL, NULL, 1.0f, NULL, 4, 4, 24, NULL, 0, NULL) == M2_ESHAPE);
   CHECK(m2_rmsnorm_residual(NULL, NULL, NULL, 1e-5f, NULL, 4, 12, NULL) == M2_ESHAPE);
   CHECK(m2_check(NULL) == M2_EINVAL);
