@@ -1,29 +1,45 @@
-// Paged decode of the mixer block (conv
-// window update + SiLU, dt, the single-step state update of each head read
-// from and written back to pool[slot] in place, y = S C + D x, gated group
-// RMSNorm and e4m3 quant), organised for HBM bandwidth:
+// Paged decode of the mixer block, in two kernels organised for HBM bandwidth.
 //
-//  - persistent CTAs (two per SM, so one streams while the other is in its
-//    conv or norm phase) walk the (row, group) work items;
-//  - a producer thread streams every head's state (64 x 128, contiguous in the
-//    pool: 32 KB in f32, 16 KB in bf16) into a shared-memory ring with
-//    cp.async.bulk (TMA, 1-D) several heads ahead, so loads are always in
-//    flight;
-//  - 8 consumer warps update the state in shared memory, reduce y, and one
-//    thread writes the updated 32 KB back with a bulk store;
-//  - conv, gate and norm for an item run on the consumer warps while the ring
-//    keeps streaming.
+// k_decode_conv: per decode row, the conv window update + SiLU of all 6144
+//   xBC channels (bf16 u into the workspace) and, per head, dt and exp(dt A);
+//   the row's conv window in the pool shifts by one in place.
+// k_decode_stream: the single-step state update of each head, read from and
+//   written back to pool[slot] in place, y = S C + D x, gated group RMSNorm
+//   and e4m3 quant of out_proj's input:
+//  - a work item is one (row, group); its 8 heads go to one CTA (HPC = 8,
+//    from a few rows up) or, for the smallest batches, to the 8 CTAs of a
+//    thread-block cluster, one head each (HPC = 1), so a single row spreads
+//    its state traffic over 64 SMs; CTAs (clusters) are persistent (as many
+//    as can be resident) and walk the items;
+//  - in each CTA a producer thread streams its heads' states (64 x 128,
+//    contiguous in the pool: 32 KB in f32, 16 KB in bf16) into a
+//    shared-memory ring with cp.async.bulk (TMA, 1-D), items ahead, with an
+//    evict-first L2 policy (the rows pass through once), and each item's u,
+//    gate and dt slices into a small staging ring; the first state loads are
+//    issued before waiting on the previous kernel (no earlier kernel of the
+//    call writes the pool); 8 consumer warps update the state in shared
+//    memory and one thread writes it back with a bulk store;
+//  - the group's RMSNorm needs the sum of squares over all 8 heads: with a
+//    cluster, each CTA stores its partial into every CTA of the cluster
+//    (distributed shared memory) and arrives on their barriers; each then
+//    adds the partials in rank order (the same total everywhere) and
+//    normalises and quantises its own channels.
 // The pool rows are advanced in place through slot_idx: the gather and
 // scatter of vllm.cpp PR #1288 ("What it does") are addressing.  Slot ids
 // must be unique within a call (two rows advancing one slot would race): a row
 // whose slot an earlier row of the call already names is skipped like a bad
 // id (output zeroed, nothing touched) and flagged in the error word, so the
-// first row naming a slot is the one that advances it.  A bf16 pool
-// (the non-f32 state cache of the same section's ssm_dtype term) is widened
-// to f32 as it is read, updated and reduced to y in f32, and rounded to bf16
-// (nearest even) as it is written back.  Every wait is
-// bounded; a wait that runs out sets the device error word and the CTA stops
-// issuing work, drains its copies and returns.
+// first row naming a slot is the one that advances it.  A bf16 pool (the
+// non-f32 state cache of the same section's ssm_dtype term) is widened to f32
+// as it is read, updated and reduced to y in f32, and rounded to bf16
+// (nearest even) as it is written back.  Optionally the state kernel also
+// brings a buffer (the out_proj weights) into L2 with an evict-last policy, so
+// the next kernel reads it from L2.  Every wait is bounded; a wait that runs
+// out sets the device error word and the CTA stops issuing work, drains its
+// copies and returns.
+#include <map>
+#include <mutex>
+
 #include "m2_kernels.h"
 #include "launch_util.h"
 #include "tc_ptx.cuh"
@@ -34,19 +50,22 @@ using namespace tc;
 
 namespace {
 
-constexpr int kRingBytes = 3 * kP * kN * 4;   // 96 KB ring per CTA, 2 CTAs per SM
+constexpr int kRingBytes = 3 * kP * kN * 4;   // 96 KB state ring per CTA, 2 CTAs per SM
 constexpr int kConsumers = 256;             // 8 warps
 constexpr int kThreadsT = kConsumers + 32;  // + producer warp
+constexpr int kStg = 4;                     // staging ring depth (items)
 
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   smem_u32(dst)),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
 }
-__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(dst)),
-               "r"(smem_u32(src)), "r"(bytes)
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes, uint64_t pol) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(smem_u32(src)), "r"(bytes), "l"(pol)
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -75,250 +94,473 @@ __device__ __forceinline__ void st4(uint16_t* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 
-template <typename S>
+// One item's inputs as they sit in the workspace and zx (bulk-copied).
+template <int HPC>
+struct __align__(16) Staging {
+  uint16_t ux[kP * HPC];   // u, the x channels of this CTA's heads (bf16)
+  uint16_t ub[kN];         // u, the group's B
+  uint16_t uc[kN];         // u, the group's C
+  uint16_t z[kP * HPC];    // the gate (z of zx) of this CTA's channels
+  float4 dtA[HPC];         // (dt, exp(dt A), -, -) per head
+};
+
+template <typename S, int HPC>
 struct __align__(16) Smem {
   static constexpr int kStages = kRingBytes / (kP * kN * (int)sizeof(S));   // 3 (f32) or 6 (bf16)
+  static constexpr int kU = kHPG / HPC;                                      // CTAs per cluster
   S state[kStages][kP * kN];       // 96 KB ring
-  float ux[kGroupCh];
-  float4 ub[kN / 4];
-  float4 uc[kN / 4];
-  float ys[kGroupCh];
-  float dts[kHPG], dAs[kHPG];
+  Staging<HPC> stg[kStg];
+  float ys[kP * HPC];
   float red[kConsumers / 32];
+  float part[2][kU];               // the ranks' sums of squares, by item parity
   uint64_t full[kStages], empty[kStages];
+  uint64_t sfull[kStg], sempty[kStg];
+  uint64_t xb[2];                  // all ranks' partials have arrived, by item parity
   int abort;
 };
 
 }  // namespace
 
-template <typename S>
+// ---------------------------------------------------------------------------
+// conv window update + SiLU and dt of the decode rows: 128 threads x 2
+// channels per CTA, grid (6144 / 256, Bt).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) k_decode_conv(const uint16_t* __restrict__ zx, const uint16_t* __restrict__ conv_w,
+                                                     const uint16_t* __restrict__ conv_b,
+                                                     const float* __restrict__ A_log, const float* __restrict__ dt_bias,
+                                                     uint16_t* __restrict__ conv_pool, int n_slots,
+                                                     const int32_t* __restrict__ slot_idx, uint16_t* __restrict__ u,
+                                                     float4* __restrict__ dtA, uint16_t* __restrict__ taps_u,
+                                                     float* __restrict__ taps_dt) {
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.y, tid = threadIdx.x;
+  const int slot = slot_idx[b];
+  if (slot < 0 || slot >= n_slots) return;        // the state kernel flags and skips the row
+  bool hit = false;
+  for (int j = tid; j < b; j += blockDim.x) hit |= (slot_idx[j] == slot);
+  if (__syncthreads_or(hit)) return;              // a repeated slot: only its first row advances it
+  const uint16_t* zrow = zx + (size_t)b * kZ;
+  const int c = blockIdx.x * 256 + 2 * tid;
+  // the taps of channels c and c + 1: 6 bf16, [channel][tap], tap 0 oldest
+  uint32_t* tp = reinterpret_cast<uint32_t*>(conv_pool + ((size_t)slot * kConv + c) * (kW - 1));
+  const uint32_t w0 = tp[0], w1 = tp[1], w2 = tp[2];
+  const uint32_t xn = *reinterpret_cast<const uint32_t*>(zrow + kOffXBC + c);
+  const uint4 cw = *reinterpret_cast<const uint4*>(conv_w + (size_t)c * kW);
+  const uint16_t t0a = w0 & 0xFFFF, t1a = w0 >> 16, t2a = w1 & 0xFFFF;
+  const uint16_t t0b = w1 >> 16, t1b = w2 & 0xFFFF, t2b = w2 >> 16;
+  const uint16_t xa = xn & 0xFFFF, xb = xn >> 16;
+  float acc_a = conv_b ? bfbits2f(conv_b[c]) : 0.f;
+  float acc_b = conv_b ? bfbits2f(conv_b[c + 1]) : 0.f;
+  acc_a = fmaf(bfbits2f(cw.x & 0xFFFF), bfbits2f(t0a), acc_a);
+  acc_a = fmaf(bfbits2f(cw.x >> 16), bfbits2f(t1a), acc_a);
+  acc_a = fmaf(bfbits2f(cw.y & 0xFFFF), bfbits2f(t2a), acc_a);
+  acc_a = fmaf(bfbits2f(cw.y >> 16), bfbits2f(xa), acc_a);
+  acc_b = fmaf(bfbits2f(cw.z & 0xFFFF), bfbits2f(t0b), acc_b);
+  acc_b = fmaf(bfbits2f(cw.z >> 16), bfbits2f(t1b), acc_b);
+  acc_b = fmaf(bfbits2f(cw.w & 0xFFFF), bfbits2f(t2b), acc_b);
+  acc_b = fmaf(bfbits2f(cw.w >> 16), bfbits2f(xb), acc_b);
+  const uint32_t uu = (uint32_t)f2bfbits(silu_f(acc_a)) | ((uint32_t)f2bfbits(silu_f(acc_b)) << 16);
+  *reinterpret_cast<uint32_t*>(u + (size_t)b * kConv + c) = uu;
+  if (taps_u) *reinterpret_cast<uint32_t*>(taps_u + (size_t)b * kConv + c) = uu;
+  // the window shifts in: (t1, t2, x_new) per channel
+  tp[0] = (uint32_t)t1a | ((uint32_t)t2a << 16);
+  tp[1] = (uint32_t)xa | ((uint32_t)t1b << 16);
+  tp[2] = (uint32_t)t2b | ((uint32_t)xb << 16);
+  if (blockIdx.x == 0 && tid < kNH) {
+    const int h = tid;
+    const float dt = softplus_f(bfbits2f(zrow[kOffDt + h]) + dt_bias[h]);
+    dtA[(size_t)b * kNH + h] = make_float4(dt, expf(dt * -expf(A_log[h])), 0.f, 0.f);
+    if (taps_dt) taps_dt[(size_t)b * kNH + h] = dt;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// state update, y, gated norm and quant; cluster of 8 / HPC CTAs per item
+// ---------------------------------------------------------------------------
+template <typename S, int HPC>
 __global__ void __launch_bounds__(kThreadsT, 2)
-    k_decode_stream(const uint16_t* __restrict__ zx, const uint16_t* __restrict__ conv_w,
-                    const uint16_t* __restrict__ conv_b, const float* __restrict__ A_log, const float* __restrict__ Dp,
-                    const float* __restrict__ dt_bias, const uint16_t* __restrict__ norm_w, float eps, float s_y,
-                    uint16_t* __restrict__ conv_pool, S* __restrict__ ssm_pool, int n_slots,
-                    const int32_t* __restrict__ slot_idx, int Bt, uint8_t* __restrict__ q2, int* __restrict__ err,
-                    DecodeTaps taps) {
-  constexpr int kStages = Smem<S>::kStages;
+    k_decode_stream(const uint16_t* __restrict__ zx, const uint16_t* __restrict__ u, const float4* __restrict__ dtA,
+                    const float* __restrict__ Dp, const uint16_t* __restrict__ norm_w, float eps, float s_y,
+                    S* __restrict__ ssm_pool, int n_slots, const int32_t* __restrict__ slot_idx, int Bt,
+                    uint8_t* __restrict__ q2, int* __restrict__ err, DecodeTaps taps,
+                    const uint8_t* __restrict__ l2_prefetch, uint32_t l2_prefetch_bytes) {
+  using Sm = Smem<S, HPC>;
+  constexpr int kStages = Sm::kStages;
+  constexpr int kU = Sm::kU;
   constexpr uint32_t kHeadBytes = kP * kN * sizeof(S);
+  constexpr uint32_t kStgBytes = sizeof(Staging<HPC>);
+  constexpr int kCh = kP * HPC;                                  // channels of this CTA
+  constexpr int kPer = (kCh + kConsumers - 1) / kConsumers;      // of them per consumer thread
   extern __shared__ uint8_t smem_raw[];
-  Smem<S>& sm = *reinterpret_cast<Smem<S>*>(smem_align<128>(smem_raw));
+  Sm& sm = *reinterpret_cast<Sm*>(smem_align<128>(smem_raw));
   volatile int* abort = &sm.abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int items = Bt * kG;
+  const int rank = kU > 1 ? (int)cluster_ctarank() : 0;   // the CTA's heads: rank * HPC .. of the group
+  const int cluster = blockIdx.x / kU, nclusters = gridDim.x / kU;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
+    for (int s = 0; s < kStg; ++s) {
+      mbar_init(&sm.sfull[s], 1);
+      mbar_init(&sm.sempty[s], 1);
+    }
+    mbar_init(&sm.xb[0], kU);
+    mbar_init(&sm.xb[1], kU);
     sm.abort = 0;
     fence_mbar_init();
   }
-  __syncthreads();
-  pdl_wait();
-  pdl_trigger();
+  __syncwarp();
+  if (kU > 1) cluster_sync();   // every CTA's barriers exist before any remote arrive
+  else __syncthreads();
+  const uint64_t pol_stream = policy_evict_first();
 
   if (warp == kConsumers / 32) {
     // ------------------------------------------------ producer warp
     // (all lanes walk the items to share the duplicate scan; lane 0 issues)
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, ss = 0, heads = 0;
+    uint32_t phase = 0, sphase = 0;
     bool ok = true;
-    bool issued[kStages];
-    uint32_t issued_phase[kStages];
+    bool issued[kStages], sissued[kStg];
+    uint32_t issued_phase[kStages], sissued_phase[kStg];
     for (int s = 0; s < kStages; ++s) issued[s] = false, issued_phase[s] = 0;
-    for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+    for (int s = 0; s < kStg; ++s) sissued[s] = false, sissued_phase[s] = 0;
+    // the first ring fill of state rows, before waiting on the previous kernel
+    // (it writes none of the pool): heads [0, npre) in item order
+    int npre = 0;
+    for (int it = cluster; it < items && npre < kStages; it += nclusters) {
+      const int b = it / kG, g = it % kG;
+      const int slot = slot_idx[b];
+      if (slot < 0 || slot >= n_slots) continue;
+      if (slot_named_earlier(slot_idx, b, slot, lane)) continue;
+      for (int hh = 0; hh < HPC && npre < kStages; ++hh, ++npre) {
+        if (lane == 0) {
+          mbar_expect_tx(&sm.full[npre], kHeadBytes);
+          bulk_load(sm.state[npre], ssm_pool + ((size_t)slot * kNH + g * kHPG + rank * HPC + hh) * (kP * kN),
+                    kHeadBytes, &sm.full[npre], pol_stream);
+          issued[npre] = true;
+        }
+      }
+    }
+    pdl_wait();      // u, dt and zx come from the previous kernels
+    pdl_trigger();
+    for (int it = cluster; it < items && ok; it += nclusters) {
       const int b = it / kG, g = it % kG;
       const int slot = slot_idx[b];
       if (slot < 0 || slot >= n_slots) continue;
       if (slot_named_earlier(slot_idx, b, slot, lane)) continue;
       if (lane == 0) {
-        const S* src = ssm_pool + ((size_t)slot * kNH + g * kHPG) * (kP * kN);
-        for (int hh = 0; hh < kHPG; ++hh) {
-          if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
-            *abort = 1;
-            atomicOr(err, kErrTimeout);
-            ok = false;
-            break;
+        const int h0 = g * kHPG + rank * HPC;
+        // the item's inputs
+        if (mbar_wait(&sm.sempty[ss], sphase ^ 1u, abort)) {
+          Staging<HPC>& st = sm.stg[ss];
+          mbar_expect_tx(&sm.sfull[ss], kStgBytes);
+          const uint16_t* ur = u + (size_t)b * kConv;
+          bulk_load(st.ux, ur + h0 * kP, kP * HPC * 2, &sm.sfull[ss], pol_stream);
+          bulk_load(st.ub, ur + kOffB + g * kN, kN * 2, &sm.sfull[ss], pol_stream);
+          bulk_load(st.uc, ur + kOffC + g * kN, kN * 2, &sm.sfull[ss], pol_stream);
+          bulk_load(st.z, zx + (size_t)b * kZ + h0 * kP, kP * HPC * 2, &sm.sfull[ss], pol_stream);
+          bulk_load(st.dtA, dtA + (size_t)b * kNH + h0, 16 * HPC, &sm.sfull[ss], pol_stream);
+          sissued[ss] = true;
+          sissued_phase[ss] = sphase;
+          if (++ss == kStg) ss = 0, sphase ^= 1u;
+        } else {
+          ok = false;
+        }
+        // the item's state rows (the first npre heads are already on their way)
+        for (int hh = 0; hh < HPC && ok; ++hh, ++heads) {
+          if (heads >= npre) {
+            if (!mbar_wait(&sm.empty[stage], phase ^ 1u, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(&sm.full[stage], kHeadBytes);
+            bulk_load(sm.state[stage], ssm_pool + ((size_t)slot * kNH + h0 + hh) * (kP * kN), kHeadBytes,
+                      &sm.full[stage], pol_stream);
+            issued[stage] = true;
+            issued_phase[stage] = phase;
           }
-          mbar_expect_tx(&sm.full[stage], kHeadBytes);
-          bulk_load(sm.state[stage], src + (size_t)hh * (kP * kN), kHeadBytes, &sm.full[stage]);
-          issued[stage] = true;
-          issued_phase[stage] = phase;
           if (++stage == kStages) stage = 0, phase ^= 1u;
+        }
+        if (!ok) {
+          *abort = 1;
+          atomicOr(err, kErrTimeout);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
     }
-    if (lane == 0 && *abort)   // let loads already in flight land before the CTA can exit
+    if (lane == 0) {
+      // this CTA's share of the buffer the next kernel reads, into L2
+      if (l2_prefetch && l2_prefetch_bytes) {
+        const uint32_t per = ((l2_prefetch_bytes + gridDim.x - 1) / gridDim.x + 15) & ~15u;
+        const uint32_t off = per * blockIdx.x;
+        if (off < l2_prefetch_bytes)
+          prefetch_l2(l2_prefetch + off, min(per, l2_prefetch_bytes - off), policy_evict_last());
+      }
+      // let every load issued land before the CTA can exit (state and staging)
       for (int s = 0; s < kStages; ++s)
         if (issued[s]) mbar_wait(&sm.full[s], issued_phase[s], nullptr, 100000000ull);
-    return;
-  }
-
-  // ------------------------------------------------ consumer warps
-  int stage = 0;
-  uint32_t phase = 0;
-  int prev = -1;   // stage whose bulk store may still be reading shared memory (thread 0)
-  // (an abort does not break this loop: every consumer must reach every named
-  // barrier; after an abort the waits return at once and nothing is stored)
-  for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    const int b = it / kG, g = it % kG;
-    const int slot = slot_idx[b];
-    uint8_t* q2row = q2 + (size_t)b * kI + g * kGroupCh;
-    const bool bad = slot < 0 || slot >= n_slots;
-    // every consumer warp takes the same decision from the same reads
-    const bool dup = !bad && slot_named_earlier(slot_idx, b, slot, lane);
-    if (bad || dup) {
-      if (tid == 0 && dup) atomicOr(err, kErrDupSlot);
-      if (tid == 0 && bad && slot != -1) atomicOr(err, kErrSlot);
-      for (int i = tid; i < kGroupCh; i += kConsumers) q2row[i] = 0;
-      continue;
+      for (int s = 0; s < kStg; ++s)
+        if (sissued[s]) mbar_wait(&sm.sfull[s], sissued_phase[s], nullptr, 100000000ull);
     }
-    const uint16_t* zrow = zx + (size_t)b * kZ;
-    // conv window update of the group's 512 x + 128 B + 128 C channels
-    float* ubf = reinterpret_cast<float*>(sm.ub);
-    float* ucf = reinterpret_cast<float*>(sm.uc);
-    for (int k = tid; k < kGroupCh + 2 * kN; k += kConsumers) {
-      int c;
-      if (k < kGroupCh) c = g * kGroupCh + k;
-      else if (k < kGroupCh + kN) c = kOffB + g * kN + (k - kGroupCh);
-      else c = kOffC + g * kN + (k - kGroupCh - kN);
-      uint16_t* st = conv_pool + ((size_t)slot * kConv + c) * (kW - 1);
-      const uint16_t t0 = st[0], t1 = st[1], t2 = st[2];
-      const uint16_t xn = zrow[kOffXBC + c];
-      float acc = conv_b ? bfbits2f(conv_b[c]) : 0.f;
-      const uint16_t* w = conv_w + c * kW;
-      acc = fmaf(bfbits2f(w[0]), bfbits2f(t0), acc);
-      acc = fmaf(bfbits2f(w[1]), bfbits2f(t1), acc);
-      acc = fmaf(bfbits2f(w[2]), bfbits2f(t2), acc);
-      acc = fmaf(bfbits2f(w[3]), bfbits2f(xn), acc);
-      st[0] = t1;
-      st[1] = t2;
-      st[2] = xn;
-      const uint16_t u16 = f2bfbits(silu_f(acc));
-      const float uv = bfbits2f(u16);
-      if (k < kGroupCh) sm.ux[k] = uv;
-      else if (k < kGroupCh + kN) ubf[k - kGroupCh] = uv;
-      else ucf[k - kGroupCh - kN] = uv;
-      if (taps.u) taps.u[(size_t)b * kConv + c] = u16;
-    }
-    if (tid < kHPG) {
-      const int h = g * kHPG + tid;
-      const float dt = softplus_f(bfbits2f(zrow[kOffDt + h]) + dt_bias[h]);
-      sm.dts[tid] = dt;
-      sm.dAs[tid] = expf(dt * -expf(A_log[h]));
-      if (taps.dt) taps.dt[(size_t)b * kNH + h] = dt;
-    }
-    consumers_sync();
-    const float4 bv = sm.ub[lane];
-    const float4 cv = sm.uc[lane];
-    S* dst_base = ssm_pool + ((size_t)slot * kNH + g * kHPG) * (kP * kN);
-    for (int hh = 0; hh < kHPG; ++hh) {
-      const int h = g * kHPG + hh;
-      const bool ok = mbar_wait(&sm.full[stage], phase, abort);
-      if (!ok) {
+  } else {
+    // ------------------------------------------------ consumer warps
+    pdl_wait();
+    pdl_trigger();
+    int stage = 0, ss = 0;
+    uint32_t phase = 0, sphase = 0;
+    int prev = -1;   // stage whose bulk store may still be reading shared memory (thread 0)
+    int k = 0;       // items exchanged so far (the partials' parity)
+    // (an abort does not break this loop: every consumer must reach every named
+    // barrier; after an abort the waits return at once and nothing is stored)
+    for (int it = cluster; it < items; it += nclusters) {
+      const int b = it / kG, g = it % kG;
+      const int h0 = g * kHPG + rank * HPC;
+      const int slot = slot_idx[b];
+      uint8_t* q2c = q2 + (size_t)b * kI + h0 * kP;
+      const bool bad = slot < 0 || slot >= n_slots;
+      // every consumer warp takes the same decision from the same reads (and
+      // every CTA of the cluster too: they share the row)
+      const bool dup = !bad && slot_named_earlier(slot_idx, b, slot, lane);
+      if (bad || dup) {
+        if (tid == 0 && rank == 0 && dup) atomicOr(err, kErrDupSlot);
+        if (tid == 0 && rank == 0 && bad && slot != -1) atomicOr(err, kErrSlot);
+        for (int j = tid; j < kCh; j += kConsumers) q2c[j] = 0;
+        continue;
+      }
+      if (!mbar_wait(&sm.sfull[ss], sphase, abort)) {
         if (tid == 0) atomicOr(err, kErrTimeout);
         *abort = 1;
       }
-      S* St = sm.state[stage];
-      const float dt = sm.dts[hh], dA = sm.dAs[hh];
-      float part[kP / 8];
+      const Staging<HPC>& st = sm.stg[ss];
+      const uint2 bw = *reinterpret_cast<const uint2*>(st.ub + 4 * lane);
+      const uint2 cw = *reinterpret_cast<const uint2*>(st.uc + 4 * lane);
+      const float4 bv = make_float4(__uint_as_float(bw.x << 16), __uint_as_float(bw.x & 0xFFFF0000u),
+                                    __uint_as_float(bw.y << 16), __uint_as_float(bw.y & 0xFFFF0000u));
+      const float4 cv = make_float4(__uint_as_float(cw.x << 16), __uint_as_float(cw.x & 0xFFFF0000u),
+                                    __uint_as_float(cw.y << 16), __uint_as_float(cw.y & 0xFFFF0000u));
+      for (int hh = 0; hh < HPC; ++hh) {
+        const int h = h0 + hh;
+        const bool ok = mbar_wait(&sm.full[stage], phase, abort);
+        if (!ok) {
+          if (tid == 0) atomicOr(err, kErrTimeout);
+          *abort = 1;
+        }
+        S* St = sm.state[stage];
+        const float dt = st.dtA[hh].x, dA = st.dtA[hh].y;
+        float part[kP / 8];
 #pragma unroll
-      for (int i = 0; i < kP / 8; ++i) {
-        const int p = warp + 8 * i;
-        float4 s = ld4(St + p * kN + 4 * lane);
-        const float xd = dt * sm.ux[hh * kP + p];
-        s.x = fmaf(dA, s.x, xd * bv.x);
-        s.y = fmaf(dA, s.y, xd * bv.y);
-        s.z = fmaf(dA, s.z, xd * bv.z);
-        s.w = fmaf(dA, s.w, xd * bv.w);
-        st4(St + p * kN + 4 * lane, s);   // f32, or rounded to bf16 for a bf16 pool
-        part[i] = s.x * cv.x + s.y * cv.y + s.z * cv.z + s.w * cv.w;
-      }
-#pragma unroll
-      for (int i = 0; i < kP / 8; ++i) {
-        float v = part[i];
-#pragma unroll
-        for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) {
+        for (int i = 0; i < kP / 8; ++i) {
           const int p = warp + 8 * i;
-          sm.ys[hh * kP + p] = round_bf16(v + Dp[h] * sm.ux[hh * kP + p]);
+          float4 s4 = ld4(St + p * kN + 4 * lane);
+          const float xd = dt * bfbits2f(st.ux[hh * kP + p]);
+          s4.x = fmaf(dA, s4.x, xd * bv.x);
+          s4.y = fmaf(dA, s4.y, xd * bv.y);
+          s4.z = fmaf(dA, s4.z, xd * bv.z);
+          s4.w = fmaf(dA, s4.w, xd * bv.w);
+          st4(St + p * kN + 4 * lane, s4);   // f32, or rounded to bf16 for a bf16 pool
+          part[i] = s4.x * cv.x + s4.y * cv.y + s4.z * cv.z + s4.w * cv.w;
         }
+#pragma unroll
+        for (int i = 0; i < kP / 8; ++i) {
+          float v = part[i];
+#pragma unroll
+          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) {
+            const int p = warp + 8 * i;
+            sm.ys[hh * kP + p] = round_bf16(v + Dp[h] * bfbits2f(st.ux[hh * kP + p]));
+          }
+        }
+        fence_async_smem();
+        consumers_sync();
+        if (tid == 0) {
+          // write the head back; release the previous stage once its store has
+          // finished reading shared memory (one store stays in flight)
+          S* dst = ssm_pool + ((size_t)slot * kNH + h) * (kP * kN);
+          if (ok) bulk_store(dst, sm.state[stage], kHeadBytes, pol_stream);
+          else asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+          if (prev >= 0) {
+            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+            mbar_arrive(&sm.empty[prev]);
+          }
+          prev = stage;
+        }
+        if (++stage == kStages) stage = 0, phase ^= 1u;
       }
-      fence_async_smem();
+      // gated group RMSNorm + e4m3 quant: this CTA's 64 HPC channels; the sum
+      // of squares over the group's 512 comes from all CTAs of the cluster
+      float gv[kPer];
+      float ssq = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int j = tid + i * kConsumers;
+        gv[i] = j < kCh ? sm.ys[j] * silu_f(bfbits2f(st.z[j])) : 0.f;
+        ssq = fmaf(gv[i], gv[i], ssq);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, o);
+      if (lane == 0) sm.red[warp] = ssq;
       consumers_sync();
-      if (tid == 0) {
-        // write the head back; release the previous stage once its store has
-        // finished reading shared memory (one store stays in flight)
-        if (ok) bulk_store(dst_base + (size_t)hh * (kP * kN), sm.state[stage], kHeadBytes);
-        else asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-        if (prev >= 0) {
-          asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-          mbar_arrive(&sm.empty[prev]);
+      float tot = 0.f;
+      const int par = k & 1;
+      if (kU > 1) {
+        if (tid == 0) {
+          float mine = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumers / 32; ++w) mine += sm.red[w];
+          const uint32_t pa = smem_u32(&sm.part[par][rank]);
+          const uint32_t xa = smem_u32(&sm.xb[par]);
+          for (int r = 0; r < kU; ++r) st_dsmem_f32(cluster_map(pa, (uint32_t)r), mine);
+          for (int r = 0; r < kU; ++r) mbar_arrive_remote(cluster_map(xa, (uint32_t)r));
         }
-        prev = stage;
+        if (!mbar_wait_cluster(&sm.xb[par], (uint32_t)(k >> 1) & 1u, abort)) {
+          if (tid == 0) atomicOr(err, kErrTimeout);
+          *abort = 1;
+        }
+#pragma unroll
+        for (int r = 0; r < kU; ++r) tot += sm.part[par][r];
+      } else {
+#pragma unroll
+        for (int w = 0; w < kConsumers / 32; ++w) tot += sm.red[w];
       }
-      if (++stage == kStages) stage = 0, phase ^= 1u;
+      const float rn = 1.0f / sqrtf(tot / (float)kGroupCh + eps);
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int j = tid + i * kConsumers;
+        if (j < kCh) {
+          const int ch = h0 * kP + j;
+          const uint16_t o16 = f2bfbits(gv[i] * rn * bfbits2f(norm_w[ch]));
+          q2c[j] = quant_e4m3(bfbits2f(o16), s_y);
+          if (taps.o) taps.o[(size_t)b * kI + ch] = o16;
+          if (taps.y) taps.y[(size_t)b * kI + ch] = f2bfbits(sm.ys[j]);
+        }
+      }
+      ++k;
+      consumers_sync();   // ys, red and the staging slot are free for the next item
+      if (tid == 0) mbar_arrive(&sm.sempty[ss]);
+      if (++ss == kStg) ss = 0, sphase ^= 1u;
     }
-    consumers_sync();
-    // gated group RMSNorm + e4m3 quant over the 512 channels
-    float gv[kGroupCh / kConsumers];
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < kGroupCh / kConsumers; ++j) {
-      const int i = tid + j * kConsumers;
-      gv[j] = sm.ys[i] * silu_f(bfbits2f(zrow[g * kGroupCh + i]));
-      ss = fmaf(gv[j], gv[j], ss);
+    if (tid == 0) {
+      bulk_wait_all();
+      if (prev >= 0) mbar_arrive(&sm.empty[prev]);
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) sm.red[warp] = ss;
-    consumers_sync();
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumers / 32; ++w) tot += sm.red[w];
-    const float r = 1.0f / sqrtf(tot / (float)kGroupCh + eps);
-#pragma unroll
-    for (int j = 0; j < kGroupCh / kConsumers; ++j) {
-      const int i = tid + j * kConsumers;
-      const int ch = g * kGroupCh + i;
-      const uint16_t o16 = f2bfbits(gv[j] * r * bfbits2f(norm_w[ch]));
-      q2row[i] = quant_e4m3(bfbits2f(o16), s_y);
-      if (taps.o) taps.o[(size_t)b * kI + ch] = o16;
-      if (taps.y) taps.y[(size_t)b * kI + ch] = f2bfbits(sm.ys[i]);
-    }
-    consumers_sync();   // ys, red, ux reused by the next item
   }
-  if (tid == 0) {
-    bulk_wait_all();
-    if (prev >= 0) mbar_arrive(&sm.empty[prev]);
+  __syncwarp();
+  if (kU > 1) cluster_sync();   // no CTA leaves while another may still write to it
+}
+
+namespace {
+
+// Clusters that fit on the device at once for this kernel (cached per
+// device and instantiation).
+template <typename S, int HPC>
+int resident_clusters(size_t smem) {
+  constexpr int kU = kHPG / HPC;
+  static std::mutex mu;
+  static std::map<int, int> by_device;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = by_device.find(dev);
+  if (it != by_device.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kU * 64);
+  cfg.blockDim = dim3(kThreadsT);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kU;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_decode_stream<S, HPC>, &cfg) != cudaSuccess || n < 1)
+    n = 2 * device_sm_count() / kU;   // two CTAs per SM
+  by_device[dev] = n;
+  return n;
+}
+
+}  // namespace
+
+template <typename S, int HPC>
+static cudaError_t launch_state_t(const uint16_t* zx, const uint16_t* u, const float4* dtA, const BlockParams& bp,
+                                  S* ssm_pool, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
+                                  const DecodeTaps& taps, const void* l2_prefetch, size_t l2_prefetch_bytes,
+                                  cudaStream_t st) {
+  constexpr int kU = kHPG / HPC;
+  auto k = k_decode_stream<S, HPC>;
+  const size_t smem = sizeof(Smem<S, HPC>) + 128;
+  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k), (int)smem);
+  if (e != cudaSuccess) return e;
+  const int items = Bt * kG;
+  const int rc = resident_clusters<S, HPC>(smem);
+  const int clusters = items < rc ? items : rc;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * kU);
+  cfg.blockDim = dim3(kThreadsT);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kU;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = kU > 1 ? 2 : 1;
+  const uint32_t pf = (l2_prefetch && l2_prefetch_bytes < (1u << 31)) ? (uint32_t)(l2_prefetch_bytes & ~(size_t)15) : 0u;
+  return cudaLaunchKernelEx(&cfg, k, zx, u, dtA, bp.D, bp.norm_w, bp.eps, bp.s_y, ssm_pool, n_slots, slot_idx, Bt, q2,
+                            err, taps, static_cast<const uint8_t*>(pf ? l2_prefetch : nullptr), pf);
+}
+
+// Heads per CTA of the state kernel for a batch of Bt rows: one for the
+// smallest batches (their few items then use 8 CTAs each), all eight of the
+// group otherwise (no exchange: measured faster from a few rows up, where
+// the items alone fill the GPU; 2 and 4 heads per CTA were slower at 64 rows).
+int decode_heads_per_cta(int Bt) { return Bt <= 2 ? 1 : 8; }
+
+template <typename S>
+static cudaError_t launch_state_s(const uint16_t* zx, const uint16_t* u, const float4* dtA, const BlockParams& bp,
+                                  S* ssm_pool, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
+                                  const DecodeTaps& taps, const void* l2_prefetch, size_t l2_prefetch_bytes,
+                                  cudaStream_t st) {
+  switch (decode_heads_per_cta(Bt)) {
+    case 1:
+      return launch_state_t<S, 1>(zx, u, dtA, bp, ssm_pool, n_slots, slot_idx, Bt, q2, err, taps, l2_prefetch,
+                                  l2_prefetch_bytes, st);
+    default:
+      return launch_state_t<S, 8>(zx, u, dtA, bp, ssm_pool, n_slots, slot_idx, Bt, q2, err, taps, l2_prefetch,
+                                  l2_prefetch_bytes, st);
   }
 }
 
-template <typename S>
-static cudaError_t launch_decode_t(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, S* ssm_pool,
-                                   int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
-                                   const DecodeTaps& taps, cudaStream_t st) {
-  auto k = k_decode_stream<S>;
-  cudaError_t e = ensure_smem_optin(reinterpret_cast<const void*>(k), (int)(sizeof(Smem<S>) + 128));
-  if (e != cudaSuccess) return e;
-  const int sms = device_sm_count();
-  const int items = Bt * kG;
-  const int grid = items < 2 * sms ? items : 2 * sms;
-  return launch_pdl(k, dim3(grid), dim3(kThreadsT), sizeof(Smem<S>) + 128, st, zx, bp.conv_w, bp.conv_b, bp.A_log,
-                    bp.D, bp.dt_bias, bp.norm_w, bp.eps, bp.s_y, conv_pool, ssm_pool, n_slots, slot_idx, Bt, q2, err,
-                    taps);
-}
+size_t decode_scratch_bytes(int Bt) { return (size_t)Bt * (kConv * 2 + kNH * 16); }
 
 cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, void* ssm_pool,
                                  bool bf16_state, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
-                                 const DecodeTaps& taps, cudaStream_t st) {
+                                 const DecodeTaps& taps, void* scratch, cudaStream_t st, int* launches,
+                                 const void* l2_prefetch, size_t l2_prefetch_bytes) {
+  uint16_t* u = static_cast<uint16_t*>(scratch);
+  float4* dtA = reinterpret_cast<float4*>(static_cast<char*>(scratch) + (size_t)Bt * kConv * 2);
+  *launches = 0;
+  cudaError_t e = launch_pdl(k_decode_conv, dim3(kConv / 256, Bt), dim3(128), 0, st, zx, bp.conv_w, bp.conv_b,
+                             bp.A_log, bp.dt_bias, conv_pool, n_slots, slot_idx, u, (float4*)dtA, taps.u, taps.dt);
+  if (e != cudaSuccess) return e;
+  *launches = 1;
   if (bf16_state)
-    return launch_decode_t(zx, bp, conv_pool, static_cast<uint16_t*>(ssm_pool), n_slots, slot_idx, Bt, q2, err,
-                           taps, st);
-  return launch_decode_t(zx, bp, conv_pool, static_cast<float*>(ssm_pool), n_slots, slot_idx, Bt, q2, err, taps, st);
+    e = launch_state_s(zx, u, dtA, bp, static_cast<uint16_t*>(ssm_pool), n_slots, slot_idx, Bt, q2, err, taps,
+                       l2_prefetch, l2_prefetch_bytes, st);
+  else
+    e = launch_state_s(zx, u, dtA, bp, static_cast<float*>(ssm_pool), n_slots, slot_idx, Bt, q2, err, taps,
+                       l2_prefetch, l2_prefetch_bytes, st);
+  if (e == cudaSuccess) *launches = 2;
+  return e;
 }
 
 }  // namespace m2
