@@ -570,9 +570,33 @@ __global__ void __launch_bounds__(kScThr, 1)
             split2t(mul2(g01, mul2(rf2, pk2(f.x, f.y))), hi[2 * q], lo[2 * q]);
             split2t(mul2(g23, mul2(rf2, pk2(f.z, f.w))), hi[2 * q + 1], lo[2 * q + 1]);
           }
+        } else if (j == rblk && (cd->hi[s0] - cd->hi[min(s0 + 31, cp.n - 1)]) +
+                                        (cd->lo[s0] - cd->lo[min(s0 + 31, cp.n - 1)]) < 60.f) {
+          // On the diagonal, when the block's log-decay span is below 60: the
+          // same factorisation as below it, exp(cum_t - cum_s) dt_s =
+          // exp(cum_t - cum_e) colf_s, the first factor now >= 1 but at most
+          // e^60 (t <= e), the second at least dt_s e^-60; then the causal
+          // mask and D on s = t.  (The span is the same for the whole warp.)
+          const int e = min(s0 + 31, cp.n - 1);
+          const float rf = tt < cp.n ? __expf((ct_hi - cd->hi[e]) + (ct_lo - cd->lo[e])) : 0.f;
+          const float4* cf = reinterpret_cast<const float4*>(cd->colf + s0);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float4 f = cf[q];
+            const float fs[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int e4 = 0; e4 < 4; ++e4) {
+              const int s = s0 + 4 * q + e4;
+              const float val = __uint_as_float(r[4 * q + e4]) * (rf * fs[e4]);
+              v[4 * q + e4] = s <= tlim ? val + (s == tt ? Dh : 0.f) : 0.f;
+            }
+          }
+#pragma unroll
+          for (int e4 = 0; e4 < 16; ++e4) split2t(pk2(v[2 * e4], v[2 * e4 + 1]), hi[e4], lo[e4]);
         } else if (j == rblk) {
-          // s > t (or a row past the chunk) selects 0; the exponential there
-          // may overflow and is discarded by the select
+          // (a span of 60 or more) one exponential per element; s > t (or a
+          // row past the chunk) selects 0, the exponential there may overflow
+          // and is discarded by the select
           const float4* h4 = reinterpret_cast<const float4*>(cd->hi + s0);
           const float4* l4 = reinterpret_cast<const float4*>(cd->lo + s0);
           const float4* d4 = reinterpret_cast<const float4*>(cd->dt + s0);
