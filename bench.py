@@ -949,7 +949,8 @@ def run_configs(args):
 
 def run_case(args):
     """One kernel family at its bench-workload shape, for profiler captures
-    (ncu -k <kernel> -c <n>): --case in_proj | out_proj | decode | prefill."""
+    (ncu -k <kernel> -c <n>): --case in_proj | out_proj | decode | decode1 |
+    prefill | glue."""
     import torch
 
     import mamba2_ssm_mixer_gb300 as m2
@@ -965,6 +966,28 @@ def run_case(args):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         for _ in range(args.steps):
             m2.fp8_linear(a, 1.0 / 64, w, 0.01, y=y)
+    elif args.case == "glue":
+        # the block's input quantisation, the stack's residual RMSNorm (plain
+        # and with the fused e4m3 output) and the W8A16 weight dequantisation,
+        # on buffers larger than L2: 4 x 8192 rows of the hidden width, and
+        # four in_proj-sized weight matrices
+        rng = torch.Generator(device=dev)
+        rng.manual_seed(1)
+        T = 4 * 8192
+        h = (torch.randn((T, H), generator=rng, device=dev) * 0.5).to(torch.bfloat16)
+        add = (torch.randn((T, H), generator=rng, device=dev) * 0.5).to(torch.bfloat16)
+        w = (1.0 + 0.1 * torch.randn((H,), generator=rng, device=dev)).to(torch.bfloat16)
+        normed = torch.empty_like(h)
+        q = torch.empty((T, H), dtype=torch.uint8, device=dev)
+        wq = torch.randint(0, 0x7E, (4 * Z, H), generator=rng, device=dev, dtype=torch.int32).to(torch.uint8)
+        wd = torch.empty((4 * Z, H), dtype=torch.bfloat16, device=dev)
+        for _ in range(args.steps):
+            m2.fp8_quant(h, 0.05, q=q)
+            m2.m2_rmsnorm_residual(h, add, w, 1e-5, normed=normed)
+            m2.m2_rmsnorm_residual_quant(h, add, w, 1e-5, 0.05, q=q)
+            m2.fp8_dequant(wq, 0.01, out=wd)
+        torch.cuda.synchronize()
+        m2.check_standalone()
     elif args.case == "decode1":
         # one decode row from its own state (the single-row decode workload)
         import synth
@@ -1010,8 +1033,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "decode1", "prefill", "stack", "decode_bf16", "arms",
-                                       "configs"],
+    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "decode1", "prefill", "glue", "stack",
+                                       "decode_bf16", "arms", "configs"],
                     default=None,
                     help="run one kernel family at the workload shape (for profiler captures); prints nothing")
     ap.add_argument("--measure-fp8-peak", action="store_true",
