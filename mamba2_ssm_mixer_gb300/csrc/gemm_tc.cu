@@ -4,13 +4,14 @@
 // bf16 values (the W8A16 arm, kind::f16, 16 per MMA); either way one MMA
 // consumes 32 bytes of each 128-byte swizzled K-slice.
 //
-// k_gemm_tc  (prefill, many rows): persistent CTAs, one per SM, each
-//   walking 128 x BN output tiles.  Warp roles: warp 0 issues TMA loads of
-//   128-byte-swizzled K-slices into a STAGES-deep shared-memory ring, warp 1
-//   issues tcgen05.mma (128 x BN x 32 bytes of K per instruction) into one of
-//   two TMEM accumulators, warps 2-5 drain the other accumulator
-//   (tcgen05.ld), scale, round to bf16 and store, so the epilogue of tile i
-//   overlaps the MMAs of tile i+1.
+// k_gemm_pair (prefill, more than 256 rows): persistent two-CTA clusters,
+//   each walking 256 x 256 output tiles with tcgen05.mma.cta_group::2 (each
+//   SM stages 128 rows of A and half of B).  Warp roles: warp 0 issues TMA
+//   loads of 128-byte-swizzled K-slices into a STAGES-deep shared-memory
+//   ring, warp 1 of the even CTA issues the MMAs into one of two TMEM
+//   accumulators, warps 2-5 drain the other accumulator (tcgen05.ld), scale,
+//   round to bf16 and write 64-column slices through shared memory with TMA
+//   stores, so the epilogue of tile i overlaps the MMAs of tile i+1.
 // k_gemm_fewrow (decode, up to 128 rows): the weight matrix is the MMA's
 //   128-row A operand and the few activation rows are its N operand
 //   (D^T = W . X^T); the K dimension is split across the CTAs of a cluster so
@@ -23,6 +24,9 @@
 // flag and the device error word, the roles leave their loops, outstanding
 // copies and MMAs are drained with bounded waits, and TMEM is freed.
 #include <cudaTypedefs.h>
+
+#include <map>
+#include <mutex>
 
 #include "gemm.h"
 #include "launch_util.h"
@@ -63,32 +67,130 @@ __device__ __forceinline__ void raise_abort(Ctl* ctl, int* err) {
   if (err) atomicOr(err, kErrTimeout);
 }
 
+// Output staging of the persistent kernels' epilogue: two buffers per
+// epilogue warp, each 32 rows x 64 bf16 (128 bytes a row) in the 128-byte
+// swizzle the output tensor map's TMA store reads.
+constexpr uint32_t kEpiBuf = 32 * 128;
+constexpr uint32_t kEpiBytes = 4 * 2 * kEpiBuf;
+
+// One epilogue warp drains its 32 accumulator lanes (output rows row0 ..
+// row0 + 31, this thread row0 + lane) over the tile's BN columns starting
+// at TMEM column `tcol` and output column n0: y = bf16(scale * acc).
+// With a store map (row stride and base 16-byte aligned) each 64-column
+// slice is staged in shared memory and written by one TMA store, full
+// 128-byte lines, while the warp converts the next slice; otherwise every
+// thread stores its own row.  `buf` alternates the warp's two buffers; a
+// buffer is reused only after the store issued from it two slices earlier
+// has read it.
+template <int BN>
+__device__ __forceinline__ void epilogue_rows(uint32_t tcol, uint8_t* bufs, int& buf, const CUtensorMap* tmC,
+                                              bool tma_store, uint16_t* __restrict__ C, int M, int N, int row0,
+                                              int n0, float scale, int lane) {
+  static_assert(BN % 64 == 0, "BN");
+  if (tma_store) {
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 64) {
+      // a slice wholly outside the output (and every later one) is neither
+      // staged nor stored: each staged buffer is followed by its store, which
+      // is what the read wait below counts on (warp-uniform condition)
+      if (row0 >= M || n0 + c >= N) break;
+      uint32_t r0[32], r1[32];
+      tmem_ld_32x32b_x32(tcol + (uint32_t)c, r0);
+      tmem_ld_32x32b_x32(tcol + (uint32_t)(c + 32), r1);
+      tmem_ld_wait();
+      uint8_t* b = bufs + buf * kEpiBuf;
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+      const uint32_t row_addr = smem_u32(b) + (uint32_t)lane * 128u;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {        // 16-byte chunk j: columns c + 8j .. c + 8j + 7
+        const uint32_t* v = j < 4 ? &r0[8 * j] : &r1[8 * (j - 4)];
+        st_shared_v4(row_addr + (uint32_t)((j ^ (lane & 7)) << 4),
+                     pack_bf16x2(__uint_as_float(v[0]) * scale, __uint_as_float(v[1]) * scale),
+                     pack_bf16x2(__uint_as_float(v[2]) * scale, __uint_as_float(v[3]) * scale),
+                     pack_bf16x2(__uint_as_float(v[4]) * scale, __uint_as_float(v[5]) * scale),
+                     pack_bf16x2(__uint_as_float(v[6]) * scale, __uint_as_float(v[7]) * scale));
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmC, b, n0 + c, row0);
+        bulk_commit();
+      }
+      buf ^= 1;
+    }
+    return;
+  }
+  const int row = row0 + lane;
+  uint16_t* crow = C + (size_t)row * N;
+  const bool vec_ok = (N % 8) == 0;
+#pragma unroll 1
+  for (int c = 0; c < BN; c += 32) {
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(tcol + (uint32_t)c, r);
+    tmem_ld_wait();
+    const int n = n0 + c;
+    if (row < M && n < N) {
+      if (vec_ok && n + 32 <= N) {
+        uint4* dst = reinterpret_cast<uint4*>(crow + n);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 v;
+          v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * scale, __uint_as_float(r[8 * q + 1]) * scale);
+          v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * scale, __uint_as_float(r[8 * q + 3]) * scale);
+          v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * scale, __uint_as_float(r[8 * q + 5]) * scale);
+          v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * scale, __uint_as_float(r[8 * q + 7]) * scale);
+          dst[q] = v;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (n + j < N) crow[n + j] = f2bfbits(__uint_as_float(r[j]) * scale);
+      }
+    }
+  }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Persistent prefill GEMM.
+// Persistent prefill GEMM on CTA pairs: each cluster of two CTAs computes
+// 256 x BN output tiles with one tcgen05.mma.cta_group::2 per 32 bytes of K.
+// CTA r of the pair loads rows [128 r, 128 r + 128) of the tile's A block and
+// columns [r BN/2, (r+1) BN/2) of its B block into its own shared memory, so
+// each SM stages half of B instead of all of it; the even CTA issues the
+// MMAs, which read both CTAs' operands and write 128 accumulator lanes into
+// each CTA's TMEM.  Barriers: every load of a stage completes on the even
+// CTA's full[stage] (expecting both CTAs' bytes); the MMA commits arrive on
+// empty[stage] and tfull[acc] of both CTAs (multicast); both CTAs' epilogue
+// warps arrive on the even CTA's tempty[acc].
 // ---------------------------------------------------------------------------
 template <int BN, int STAGES, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-              uint16_t* __restrict__ C, int M, int N, int K, float scale, int* err) {
-  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "BN");
+    k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, int tma_store, uint16_t* __restrict__ C, int M, int N,
+                int K, float scale, int* err) {
+  static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(STAGES <= 8, "STAGES");
-  constexpr uint32_t A_BYTES = kBM * kBK;
-  constexpr uint32_t B_BYTES = BN * kBK;
+  constexpr int kPM = 2 * kBM;                        // rows of a pair tile
+  constexpr uint32_t A_BYTES = kBM * kBK;             // this CTA's 128 rows
+  constexpr uint32_t B_BYTES = (BN / 2) * kBK;        // this CTA's half of the columns
   constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-  constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
-                                 : (2 * BN <= 256) ? 256 : 512;
-  constexpr uint32_t IDESC = idesc_f32acc(kBM, BN, kBf16 ? 1u : 0u);   // operand format: e4m3 0, bf16 1
-  constexpr int ES = kBf16 ? 2 : 1;                                      // bytes per operand element
+  constexpr uint32_t TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+  constexpr uint32_t IDESC = idesc_f32acc(kPM, BN, kBf16 ? 1u : 0u);
+  constexpr int ES = kBf16 ? 2 : 1;
+  constexpr uint16_t kPair = 0x3;                     // both CTAs of the (two-CTA) cluster
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_align<1024>(smem_raw);
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* epi = smem + STAGES * STAGE_BYTES;                           // output staging (kEpiBytes)
+  Ctl* ctl = reinterpret_cast<Ctl*>(epi + kEpiBytes);
   volatile int* abort = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles_m = (M + kBM - 1) / kBM, tiles_n = (N + BN - 1) / BN;
+  const uint32_t rank = cluster_ctarank();            // 0 issues the MMAs
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int tiles_m = (M + kPM - 1) / kPM, tiles_n = (N + BN - 1) / BN;
   const int num_tiles = tiles_m * tiles_n;
   const int kblocks = (K * ES + kBK - 1) / kBK;
 
@@ -99,19 +201,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&ctl->tfull[i], 1);
-      mbar_init(&ctl->tempty[i], 4 * 32);
+      mbar_init(&ctl->tempty[i], 2 * 4);              // one arrival per epilogue warp of both CTAs
     }
     mbar_init(&ctl->drain, 1);
     ctl->abort = 0;
     fence_mbar_init();
     tma_prefetch(&tmA);
     tma_prefetch(&tmB);
+    if (tma_store) tma_prefetch(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+    tmem_alloc_pair(&ctl->tmem_base, TMEM_COLS);
     tc_fence_before();
   }
-  __syncthreads();
+  __syncwarp();
+  cluster_sync();                                     // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
   pdl_wait();      // operands are produced by the previous kernel
@@ -119,15 +223,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // ---------------- TMA producer
+      // ---------------- TMA producer (both CTAs)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued_phase[STAGES];
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * BN;
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+        const int m0 = (tile % tiles_m) * kPM + (int)rank * kBM;
+        const int n0 = (tile / tiles_m) * BN + (int)rank * (BN / 2);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort)) {
             raise_abort(ctl, err);
@@ -135,30 +240,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           uint8_t* sA = smem + stage * STAGE_BYTES;
-          mbar_expect_tx(&ctl->full[stage], STAGE_BYTES);
-          tma_load_2d(sA, &tmA, &ctl->full[stage], kb * (kBK / ES), m0);
-          tma_load_2d(sA + A_BYTES, &tmB, &ctl->full[stage], kb * (kBK / ES), n0);
+          const uint32_t full0 = cluster_map(smem_u32(&ctl->full[stage]), 0);
+          if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * STAGE_BYTES);
+          tma_load_2d_pair(sA, &tmA, full0, kb * (kBK / ES), m0);
+          tma_load_2d_pair(sA + A_BYTES, &tmB, full0, kb * (kBK / ES), n0);
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == STAGES) stage = 0, phase ^= 1u;
         }
       }
       if (*abort) {
-        // let copies already in flight land before the CTA exits
+        // the even CTA's full barriers count both CTAs' copies: let those in
+        // flight land before the pair exits
+        if (rank == 0)
+          for (int s = 0; s < STAGES; ++s)
+            if (issued[s]) mbar_wait(&ctl->full[s], issued_phase[s], nullptr, 100000000ull);
+      } else {
+        // every stage's last MMA commit has arrived on this CTA's empty
+        // barrier before the CTA may exit
         for (int s = 0; s < STAGES; ++s)
-          if (issued[s]) mbar_wait(&ctl->full[s], issued_phase[s], nullptr, 100000000ull);
+          if (issued[s] && !mbar_wait(&ctl->empty[s], issued_phase[s], abort)) {
+            raise_abort(ctl, err);
+            break;
+          }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (even CTA only)
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        if (!mbar_wait(&ctl->tempty[acc], acc_phase ^ 1u, abort)) {
+      for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
+        if (!mbar_wait_cluster(&ctl->tempty[acc], acc_phase ^ 1u, abort)) {
           raise_abort(ctl, err);
           break;
         }
@@ -175,70 +291,55 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t adesc = desc_kmajor_sw128(a_addr);
           const uint64_t bdesc = desc_kmajor_sw128(a_addr + A_BYTES);
 #pragma unroll
-          for (int k = 0; k < kBK / 32; ++k)   // 32 bytes of K per MMA: +2 in the address field
-            mma_k32b<kBf16>(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
-          mma_commit(&ctl->empty[stage]);
+          for (int k = 0; k < kBK / 32; ++k) {   // 32 bytes of K per MMA: +2 in the address field
+            if constexpr (kBf16)
+              mma_f16_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+            else
+              mma_f8f6f4_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, IDESC, (kb | k) != 0);
+          }
+          mma_commit_pair(&ctl->empty[stage], kPair);
           if (++stage == STAGES) stage = 0, phase ^= 1u;
         }
         if (!ok) break;
-        mma_commit(&ctl->tfull[acc]);
+        mma_commit_pair(&ctl->tfull[acc], kPair);
         if (++acc == 2) acc = 0, acc_phase ^= 1u;
       }
       if (*abort) {
-        mma_commit(&ctl->drain);
+        mma_commit_pair(&ctl->drain, kPair);
         mbar_wait(&ctl->drain, 0, nullptr, 100000000ull);
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5 own TMEM lane quarters (warp % 4)
+    // ---------------- epilogue (both CTAs): warps 2..5 own TMEM lane quarters (warp % 4)
     const int quarter = warp & 3;
+    const uint32_t tempty0[2] = {cluster_map(smem_u32(&ctl->tempty[0]), 0),
+                                 cluster_map(smem_u32(&ctl->tempty[1]), 0)};
+    uint8_t* bufs = epi + quarter * 2 * kEpiBuf;
+    int buf = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
-    const bool vec_ok = (N % 8) == 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      const int m0 = (tile % tiles_m) * kBM, n0 = (tile / tiles_m) * BN;
+    for (int tile = pair; tile < num_tiles; tile += npairs) {
+      const int m0 = (tile % tiles_m) * kPM + (int)rank * kBM, n0 = (tile / tiles_m) * BN;
       if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort)) {
         raise_abort(ctl, err);
         break;
       }
       tc_fence_after();
-      const int row = m0 + quarter * 32 + lane;
-      uint16_t* crow = C + (size_t)row * N;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += 32) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN + c), r);
-        tmem_ld_wait();
-        const int n = n0 + c;
-        if (row < M && n < N) {
-          if (vec_ok && n + 32 <= N) {
-            uint4* dst = reinterpret_cast<uint4*>(crow + n);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * q + 0]) * scale, __uint_as_float(r[8 * q + 1]) * scale);
-              v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * scale, __uint_as_float(r[8 * q + 3]) * scale);
-              v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * scale, __uint_as_float(r[8 * q + 5]) * scale);
-              v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * scale, __uint_as_float(r[8 * q + 7]) * scale);
-              dst[q] = v;
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (n + j < N) crow[n + j] = f2bfbits(__uint_as_float(r[j]) * scale);
-          }
-        }
-      }
+      epilogue_rows<BN>(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * BN), bufs, buf, &tmC,
+                        tma_store != 0, C, M, N, m0 + quarter * 32, n0, scale, lane);
       tc_fence_before();
-      mbar_arrive(&ctl->tempty[acc]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(tempty0[acc]);
       if (++acc == 2) acc = 0, acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait<0>();          // this warp's stores are written before the CTA exits
   }
   __syncwarp();
   __syncthreads();
+  cluster_sync();                                     // no MMA of the pair still writes either CTA's TMEM
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
 }
 
@@ -676,6 +777,23 @@ cudaError_t make_map(CUtensorMap* map, const void* base, int rows, int K, int bo
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Output map for the persistent kernels' TMA stores: bf16 [rows, N], box
+// 64 columns x 32 rows, 128-byte swizzle.  False when the row stride or the
+// base is not 16-byte aligned; the kernels then store per thread.
+bool make_store_map(CUtensorMap* map, void* base, int rows, int N) {
+  if ((N * 2) % 16 != 0 || (reinterpret_cast<uintptr_t>(base) & 15) != 0) return false;
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)N * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int num_sms() { return device_sm_count(); }
 
 template <class Kern>
@@ -683,20 +801,66 @@ cudaError_t set_smem(Kern k, size_t bytes) {
   return ensure_smem_optin(reinterpret_cast<const void*>(k), (int)bytes);
 }
 
+// Two-CTA clusters of k_gemm_pair that fit on the device at once (cached per
+// device and instantiation).
 template <int BN, int STAGES, bool kBf16>
-cudaError_t launch_big(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, int* err,
-                       cudaStream_t st) {
+int pair_clusters(size_t smem) {
+  static std::mutex mu;
+  static std::map<int, int> by_device;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = by_device.find(dev);
+  if (it != by_device.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * num_sms());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm_pair<BN, STAGES, kBf16>, &cfg) != cudaSuccess || n < 1)
+    n = num_sms() / 2;
+  by_device[dev] = n;
+  return n;
+}
+
+template <int BN, int STAGES, bool kBf16>
+cudaError_t launch_pair(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, int* err,
+                        cudaStream_t st) {
   CUtensorMap ta, tb;
   cudaError_t e;
   constexpr int es = kBf16 ? 2 : 1;
   if ((e = make_map(&ta, A, M, K, kBM, es)) != cudaSuccess) return e;
-  if ((e = make_map(&tb, B, N, K, BN, es)) != cudaSuccess) return e;
-  const size_t smem = 1024 + (size_t)STAGES * (kBM + BN) * kBK + sizeof(Ctl);
-  auto k = k_gemm_tc<BN, STAGES, kBf16>;
+  if ((e = make_map(&tb, B, N, K, BN / 2, es)) != cudaSuccess) return e;
+  CUtensorMap tcm = {};
+  const int tma_store = make_store_map(&tcm, y, M, N) ? 1 : 0;
+  const size_t smem = 1024 + (size_t)STAGES * (kBM + BN / 2) * kBK + kEpiBytes + sizeof(Ctl);
+  auto k = k_gemm_pair<BN, STAGES, kBf16>;
   if ((e = set_smem(k, smem)) != cudaSuccess) return e;
-  const int tiles = ((M + kBM - 1) / kBM) * ((N + BN - 1) / BN);
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, ta, tb, y, M, N, K, scale, err);
+  const int tiles = ((M + 2 * kBM - 1) / (2 * kBM)) * ((N + BN - 1) / BN);
+  const int cap = pair_clusters<BN, STAGES, kBf16>(smem);
+  const int pairs = tiles < cap ? tiles : cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k, ta, tb, tcm, tma_store, y, M, N, K, scale, err);
 }
 
 template <int BNT, int STAGES, bool kBf16>
@@ -834,10 +998,9 @@ cudaError_t skinny_t(const void* X, const void* W, uint16_t* y, int Mtok, int N,
 template <bool kBf16>
 cudaError_t big_t(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, int* err,
                   cudaStream_t st) {
-  // Tile width: full 256-column tiles unless a narrower tile fills the last
-  // wave better (N = 2688 = 14 x 192).
-  if (N % 192 == 0 && N % 256 != 0) return launch_big<192, 5, kBf16>(A, B, y, M, N, K, scale, err, st);
-  return launch_big<256, 4, kBf16>(A, B, y, M, N, K, scale, err, st);
+  // 256 x 256 tiles on CTA pairs (N = 2688 leaves its last tile half
+  // empty, which still beats narrower tiles' extra waves)
+  return launch_pair<256, 6, kBf16>(A, B, y, M, N, K, scale, err, st);
 }
 
 }  // namespace

@@ -68,18 +68,36 @@ def _int_codes(rng, shape, lo=-8, hi=8):
 
 @pytest.mark.parametrize("M,N,K", [(1, 10304, 2688), (64, 10304, 2688), (37, 2688, 4096), (300, 200, 160),
                                    (128, 2688, 4096), (256, 2688, 4096), (5, 7, 2688), (257, 300, 2688),
-                                   (1000, 2688, 4096), (8192, 10304, 2688)])
+                                   (300, 203, 160), (1000, 2688, 4096), (8192, 10304, 2688)])
 def test_fp8_linear_integer_exact(M, N, K):
     """Integer-valued e4m3 operands: every partial sum is an exact integer
     below 2^24, so any summation order gives the same f32 value and the bf16
-    result must be bit-exact.  Shapes cover the skinny split-K path (M <= 256),
-    the persistent path (256- and 192-wide tiles), ragged M, N and K tails."""
+    result must be bit-exact.  Shapes cover the few-row cluster kernel
+    (M <= 128), the split-K kernel (129-256), the CTA-pair kernel with TMA
+    stores (N % 8 == 0) and with per-thread stores (N = 203), ragged M, N
+    and K tails."""
     rng = np.random.default_rng(M * 7 + N)
     _, a = _int_codes(rng, (M, K))
     _, w = _int_codes(rng, (N, K))
     y = to_np(m2.fp8_linear(u8_dev(a), 1.0, u8_dev(w), 1.0))
     ref = oracle.fp8_linear(a, 1.0, w, 1.0)
     assert np.array_equal(y, ref)
+
+
+def test_fp8_linear_partial_last_tile_repeated():
+    """in_proj's width 10304 leaves one 64-column slice in the last 256-wide
+    tile and M = 594 a partial last row tile: the epilogue's staged TMA
+    stores must skip the empty slices without reusing a buffer a store still
+    reads.  Five calls in a row, each bit-exact (integer-valued operands)."""
+    M, N, K = 594, 10304, 2688
+    rng = np.random.default_rng(594)
+    _, a = _int_codes(rng, (M, K))
+    _, w = _int_codes(rng, (N, K))
+    ref = oracle.fp8_linear(a, 1.0, w, 1.0)
+    ad, wd = u8_dev(a), u8_dev(w)
+    for _ in range(5):
+        y = to_np(m2.fp8_linear(ad, 1.0, wd, 1.0))
+        assert np.array_equal(y, ref)
 
 
 @pytest.mark.parametrize("M", [1, 8, 64, 200])

@@ -59,12 +59,13 @@ def test_fp8_dequant_in_proj_weights_bit_exact():
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 10304, 2688), (64, 10304, 2688), (37, 2688, 4096), (300, 200, 160),
-                                   (257, 300, 2688), (513, 10304, 2688), (600, 2688, 4096)])
+                                   (257, 300, 2688), (300, 203, 160), (513, 10304, 2688), (594, 10304, 2688),
+                                   (600, 2688, 4096)])
 def test_bf16_linear_integer_exact(M, N, K):
     """Integer-valued bf16 operands: every partial sum is an exact integer below
     2^24, so the bf16 result is bit-exact in any summation order.  Covers the
-    skinny split-K path (M <= 256), both persistent tile widths (256, 192) and
-    ragged M, N and K."""
+    few-row and split-K kernels (M <= 256), the CTA-pair kernel with TMA
+    stores and with per-thread stores (N = 203), and ragged M, N and K."""
     rng = np.random.default_rng(M * 13 + N)
     x = rng.integers(-8, 9, (M, K)).astype(np.float64)
     w = rng.integers(-8, 9, (N, K)).astype(np.float64)
