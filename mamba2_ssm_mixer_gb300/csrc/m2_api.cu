@@ -1,6 +1,7 @@
 // The C ABI of libm2 (declared in include/m2.h): argument validation, the
 // handle that owns the block's device weights, workspace carving, and the
 // launch sequence of prefill and decode.  All compute runs in the kernels.
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -405,6 +406,14 @@ m2_status m2_prefill_workspace_size(const m2_handle* h, const int32_t* seqlens_h
   return M2_OK;
 }
 
+// Longest sequence of a call: at most kRecMaxT tokens takes the token-by-token
+// SSD kernel (one launch) instead of the chunked stages (four launches).
+static int max_seqlen(const SeqInfo& si) {
+  int m = 0;
+  for (int i = 0; i < si.nseq; ++i) m = std::max(m, si.cu_seqlens[i + 1] - si.cu_seqlens[i]);
+  return m;
+}
+
 static m2_status copy_tap(void* dst, const void* src, size_t bytes, cudaStream_t st) {
   if (!dst) return M2_OK;
   M2_CUDA(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st));
@@ -448,10 +457,12 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
     M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
              gemm_fp8(q, h->in_proj, w.zx, T, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
   }
+  const bool recur = max_seqlen(local) <= kRecMaxT;
+  const bool bf16_state = h->cfg.ssm_dtype == M2_DTYPE_BF16;
   // the cumsum reads only the in_proj output: it runs on the second stream
   // beside the conv (serially while stage profiling)
   float* dt_tap = h->taps_on ? h->taps.dt : nullptr;
-  if (!h->prof_on) {
+  if (!h->prof_on && !recur) {
     M2_CUDA(cudaEventRecord(h->fork_ev, st));
     M2_CUDA(cudaStreamWaitEvent(h->side, h->fork_ev, 0));
     M2_CUDA(launch_ssd_cumsum(w.zx, bp, local, w.cumdt, dt_tap, h->side));
@@ -459,18 +470,23 @@ static m2_status prefill_impl(m2_handle* h, const uint16_t* hidden, const uint8_
     M2_CUDA(cudaEventRecord(h->cum_ev, h->side));
   }
   M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(w.zx, bp, conv_state, local, w.u, st));
-  if (h->prof_on) {
-    M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(w.zx, bp, local, w.cumdt, dt_tap, st));
+  if (recur) {
+    // short sequences: the recurrence token by token (profiled as the scan)
+    M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
+             launch_ssd_recurrent(w.zx, w.u, bp, local, w.y, ssm_state, bf16_state, conv_state, dt_tap, st));
   } else {
-    M2_CUDA(cudaStreamWaitEvent(st, h->cum_ev, 0));
+    if (h->prof_on) {
+      M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(w.zx, bp, local, w.cumdt, dt_tap, st));
+    } else {
+      M2_CUDA(cudaStreamWaitEvent(st, h->cum_ev, 0));
+    }
+    M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
+             launch_ssd_chunk_state_tc(w.u, w.cumdt, local, w.states, h->err, st));
+    M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
+             launch_ssd_state_pass(w.states, w.cumdt, local, w.sin_img, ssm_state, bf16_state, w.zx, conv_state, st));
+    M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
+             launch_ssd_chunk_scan_tc(w.u, w.cumdt, w.sin_img, bp, local, w.y, h->err, st));
   }
-  M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
-           launch_ssd_chunk_state_tc(w.u, w.cumdt, local, w.states, h->err, st));
-  M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
-           launch_ssd_state_pass(w.states, w.cumdt, local, w.sin_img, ssm_state, h->cfg.ssm_dtype == M2_DTYPE_BF16,
-                                 w.zx, conv_state, st));
-  M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
-           launch_ssd_chunk_scan_tc(w.u, w.cumdt, w.sin_img, bp, local, w.y, h->err, st));
   if (w8a16) {
     // the bf16 normed output feeds out_proj (the e4m3 codes are written too, unused)
     M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.y, w.zx, bp, T, w.q2, w.o, st));
@@ -738,12 +754,15 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
   // stream.
   const bool fork = !h->prof_on && T > 0;
   const bool fork_decode = fork && Bt > 0;
+  const bool recur = T > 0 && max_seqlen(local) <= kRecMaxT;
   if (fork) {
     M2_CUDA(cudaEventRecord(h->fork_ev, st));
     M2_CUDA(cudaStreamWaitEvent(h->side, h->fork_ev, 0));
-    M2_CUDA(launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, h->side));
-    M2_CUDA(cudaEventRecord(h->cum_ev, h->side));
-    h->stats.kernel_launches += 1;
+    if (!recur) {
+      M2_CUDA(launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, h->side));
+      M2_CUDA(cudaEventRecord(h->cum_ev, h->side));
+      h->stats.kernel_launches += 1;
+    }
     if (fork_decode) {
       DecodeTaps dt{};
       if (h->taps_on) dt.o = h->taps.o, dt.y = h->taps.y;
@@ -756,18 +775,24 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
   }
   if (T > 0) {
     M2_STAGE(h, st, M2_STAGE_CONV, 1, launch_conv_silu_prefill(zx_pf, bp, conv_state, local, w.pf.u, st));
-    if (fork) {
-      M2_CUDA(cudaStreamWaitEvent(st, h->cum_ev, 0));
+    if (recur) {
+      M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
+               launch_ssd_recurrent(zx_pf, w.pf.u, bp, local, w.pf.y, ssm_state, bf16_state, conv_state, nullptr,
+                                    st));
     } else {
-      M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, st));
+      if (fork) {
+        M2_CUDA(cudaStreamWaitEvent(st, h->cum_ev, 0));
+      } else {
+        M2_STAGE(h, st, M2_STAGE_SSD_CUMSUM, 1, launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, st));
+      }
+      M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
+               launch_ssd_chunk_state_tc(w.pf.u, w.pf.cumdt, local, w.pf.states, h->err, st));
+      M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
+               launch_ssd_state_pass(w.pf.states, w.pf.cumdt, local, w.pf.sin_img, ssm_state, bf16_state, zx_pf,
+                                     conv_state, st));
+      M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
+               launch_ssd_chunk_scan_tc(w.pf.u, w.pf.cumdt, w.pf.sin_img, bp, local, w.pf.y, h->err, st));
     }
-    M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_STATE, 1,
-             launch_ssd_chunk_state_tc(w.pf.u, w.pf.cumdt, local, w.pf.states, h->err, st));
-    M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
-             launch_ssd_state_pass(w.pf.states, w.pf.cumdt, local, w.pf.sin_img, ssm_state, bf16_state, zx_pf,
-                                   conv_state, st));
-    M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
-             launch_ssd_chunk_scan_tc(w.pf.u, w.pf.cumdt, w.pf.sin_img, bp, local, w.pf.y, h->err, st));
     uint16_t* o_tap = (h->taps_on && h->taps.o) ? h->taps.o + (size_t)Bt * kI : nullptr;
     M2_STAGE(h, st, M2_STAGE_NORM_QUANT, 1, launch_gated_norm_quant(w.pf.y, zx_pf, bp, T, q2_pf, o_tap, st));
   }

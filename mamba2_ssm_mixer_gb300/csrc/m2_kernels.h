@@ -61,6 +61,16 @@ cudaError_t launch_ssd_state_pass(const float* states, const CumDt* cumdt, const
                                   void* ssm_state, bool bf16_state, const uint16_t* zx, uint16_t* conv_state,
                                   cudaStream_t st);
 
+// ssd_recurrent.cu: the whole SSD stage of a prefill whose sequences all have
+// at most kRecMaxT tokens, token by token (one CTA per sequence and head):
+// writes y, the final states to ssm_state (read first where the sequence has
+// initial state), each sequence's new conv window (conv_state may be null)
+// and dt as [T, 64] (dt_tok may be null).
+constexpr int kRecMaxT = 64;
+cudaError_t launch_ssd_recurrent(const uint16_t* zx, const uint16_t* u, const BlockParams& bp, const SeqInfo& si,
+                                 uint16_t* y, void* ssm_state, bool bf16_state, uint16_t* conv_state, float* dt_tok,
+                                 cudaStream_t st);
+
 // ssd_tc.cu (tensor-core chunk states and chunk scan)
 // Chunk states f32 [chunk][head][64][128].
 cudaError_t launch_ssd_chunk_state_tc(const uint16_t* u, const CumDt* cumdt, const SeqInfo& si, float* states,
