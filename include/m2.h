@@ -231,6 +231,9 @@ m2_status m2_prefill_workspace_size(const m2_handle* h, const int32_t* seqlens_h
 /*
  * Prefill of nseq packed sequences (varlen).  Chunks of chunk_size tokens
  * never cross a sequence boundary; the last chunk of a sequence is partial.
+ * When no sequence has more than 64 tokens the SSD recurrence is evaluated
+ * token by token in one kernel instead of chunk-wise (the same results up to
+ * f32 rounding order; the workspace size does not change).
  *   hidden       bf16 [sum(T), 2688] device
  *   seqlens_host int32 [nseq] host, each >= 1
  *   has_initial  uint8 [nseq] host or NULL (NULL = every sequence starts from
