@@ -950,7 +950,7 @@ def run_configs(args):
 def run_case(args):
     """One kernel family at its bench-workload shape, for profiler captures
     (ncu -k <kernel> -c <n>): --case in_proj | out_proj | decode | decode1 |
-    prefill | glue."""
+    prefill | prefill32 | glue."""
     import torch
 
     import mamba2_ssm_mixer_gb300 as m2
@@ -988,6 +988,22 @@ def run_case(args):
             m2.fp8_dequant(wq, 0.01, out=wd)
         torch.cuda.synchronize()
         m2.check_standalone()
+    elif args.case == "prefill32":
+        # one 32-token prefill from zero state (the token-by-token SSD path)
+        import synth
+        Wt = synth.make_weights(0)
+        blk = m2.Mamba2Mixer({k: (v.to(dev) if isinstance(v, torch.Tensor) else v)
+                              for k, v in _weights_torch(Wt).items()}, device=dev)
+        h = torch.from_numpy(synth.make_hidden(0, 32)).to(torch.bfloat16).to(dev)
+        conv = torch.zeros((1, CONV, 3), dtype=torch.bfloat16, device=dev)
+        ssm = torch.zeros((1, 64, 64, 128), dtype=torch.float32, device=dev)
+        out = torch.empty((32, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(blk.prefill_workspace_size([32]), dtype=torch.uint8, device=dev)
+        for _ in range(args.steps):
+            blk.prefill(h, [32], conv, ssm, out=out, workspace=ws)
+        torch.cuda.synchronize()
+        blk.check()
+        blk.close()
     elif args.case == "decode1":
         # one decode row from its own state (the single-row decode workload)
         import synth
@@ -1033,7 +1049,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "decode1", "prefill", "glue", "stack",
+    ap.add_argument("--case", choices=["in_proj", "out_proj", "decode", "decode1", "prefill", "prefill32", "glue", "stack",
                                        "decode_bf16", "arms", "configs"],
                     default=None,
                     help="run one kernel family at the workload shape (for profiler captures); prints nothing")
