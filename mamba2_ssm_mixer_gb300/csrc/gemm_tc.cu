@@ -883,13 +883,17 @@ cudaError_t launch_skinny(const void* X, const void* W, uint16_t* y, float* part
 // resident in one wave (CTAs per SM from the shared-memory footprint, with a
 // margin for cluster placement), at most 8 (the portable cluster size), and
 // at least two k-blocks per CTA.
-int fewrow_splits(int N, int kblocks, size_t smem) {
+int fewrow_splits(int N, int kblocks, size_t smem, int bnt) {
   const int nb = (N + kBM - 1) / kBM;
   int per_sm = (int)((228 * 1024) / (smem + 1024));
   if (per_sm < 1) per_sm = 1;
   int s = (int)(0.9 * per_sm * num_sms() / nb);
   if (s > 8) s = 8;
   if (s > kblocks / 2) s = kblocks / 2;
+  // from 33 rows on, each split's MMAs and exchange grow with the rows and two
+  // splits beat more for the 81 weight blocks of in_proj (measured in the
+  // decode call of 64 rows: 3 splits 80.2 us, 2 splits 78.4, 4 85.8)
+  if (bnt >= 64 && nb > 64 && s > 2) s = 2;
   return s < 1 ? 1 : s;
 }
 
@@ -905,7 +909,7 @@ cudaError_t launch_fewrow(const void* X, const void* W, uint16_t* y, int Mtok, i
   auto k = k_gemm_fewrow<BNT, STAGES, kBf16>;
   if ((e = set_smem(k, smem)) != cudaSuccess) return e;
   const int kblocks = (K * es + kBK - 1) / kBK;
-  const int S = fewrow_splits(N, kblocks, smem);
+  const int S = fewrow_splits(N, kblocks, smem, BNT);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(S, (N + kBM - 1) / kBM);
   cfg.blockDim = dim3(kThreads);
