@@ -650,11 +650,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = threadIdx.x; idx < rows * quads; idx += kThreads) {
       const int nl = r0 + idx % rows, m = 4 * (idx / rows);
       const uint32_t off = red_s + (uint32_t)((nl * RED_LD + m) * 4);
-      float4 acc = ld_dsmem_f32x4(cluster_map(off, 0));
-      for (int r = 1; r < S; ++r) {
-        const float4 v = ld_dsmem_f32x4(cluster_map(off, (uint32_t)r));
-        acc.x += v.x, acc.y += v.y, acc.z += v.z, acc.w += v.w;
-      }
+      // all ranks' loads first (independent remote reads in flight together),
+      // then the sums in rank order
+      float4 v[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < S) v[r] = ld_dsmem_f32x4(cluster_map(off, (uint32_t)r));
+      float4 acc = v[0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r)
+        if (r < S) acc.x += v[r].x, acc.y += v[r].y, acc.z += v[r].z, acc.w += v[r].w;
       const int n = n0 + nl;
       if (n < N) {
         uint16_t* yc = y + (size_t)m * N + n;
