@@ -9,8 +9,9 @@
 //   heads, S_c[n, p] = sum_t B[t, n] (w_t x[t, p]) with
 //   w_t = exp(cum_last - cum_t) dt_t is a 128 x 64 x 256 MMA; worker thread t
 //   scales its token row by w_t and splits it into a bf16 high part and a bf16
-//   remainder (two MMAs) so the chunk state keeps ~16 bits; head h's epilogue
-//   overlaps head h+1's staging.
+//   remainder (two MMAs) so the chunk state keeps ~16 bits.  A dedicated MMA
+//   warp issues each head's MMAs once all worker warps have staged it, so
+//   head h's MMAs run during head h+1's staging and head h-1's epilogue.
 // k_ssd_scan_tc   one CTA per (128-row half of the chunk, chunk, group),
 //   warp-specialised: warp 0 loads (TMA for the C, B and per-head x tiles,
 //   bulk copies of the cum/dt record and S_in image, one head ahead); warp 1
@@ -103,7 +104,7 @@ __device__ __forceinline__ void split2t(uint64_t v, uint32_t& hi, uint32_t& lo) 
 // chunk states
 // ---------------------------------------------------------------------------
 constexpr int kStWork = 256;             // 8 worker warps; worker thread t owns token row t
-constexpr int kStThr = kStWork + 32;     // + a loader warp
+constexpr int kStThr = kStWork + 64;     // + a loader warp + an MMA warp
 constexpr int kStSmB = 0;                // B [2 slices of 64 n][256 t][64] as TMA writes it    64 KB
 constexpr int kStSmX = 64 * 1024;        // x [256 t][64 p] as TMA writes it                    32 KB
 constexpr int kStSmW = 96 * 1024;        // w x [2 buffers] x (bf16 high, remainder) [256 t][64 p] 128 KB
@@ -112,6 +113,7 @@ constexpr int kStSmem = kStSmBar + 128 + 1024;
 
 struct StateBars {
   uint64_t b_full, x_full, x_empty, mma[2], drain;
+  uint64_t w_full[2], t_empty[2];   // operand k staged / accumulator k read
   uint32_t tslot;
   int abort;
 };
@@ -144,6 +146,10 @@ __global__ void __launch_bounds__(kStThr, 1)
     mbar_init(&sb->mma[0], 1);
     mbar_init(&sb->mma[1], 1);
     mbar_init(&sb->drain, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&sb->w_full[k], kStWork / 32);
+      mbar_init(&sb->t_empty[k], kStWork / 32);
+    }
     sb->abort = 0;
     fence_mbar_init();
     tma_prefetch(&tm_u);
@@ -179,6 +185,35 @@ __global__ void __launch_bounds__(kStThr, 1)
         if (issued >= 0) mbar_wait(&sb->x_full, issued & 1, nullptr, 100000000ull);
       }
     }
+  } else if (warp == kStWork / 32 + 1) {
+    // ------------------------------------------------ MMA issuer: head hh's
+    // MMAs run while the workers stage head hh+1 (the operand is double
+    // buffered) and drain head hh-1's accumulator
+    if (lane == 0) {
+      bool ok = wait_ab(&sb->b_full, 0, abort, err);
+      for (int hh = 0; hh < kHPG && ok; ++hh) {
+        const int k = hh & 1;
+        ok = wait_ab(&sb->w_full[k], (hh >> 1) & 1, abort, err) &&
+             wait_ab(&sb->t_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err);   // head hh-2 drained
+        if (!ok) break;
+        tc_fence_after();
+        // S[n, p] += sum_t B[t, n] (w x)[t, p]: 16 K-steps of 16 tokens
+        // (2048 bytes of both tiles); B's two 64-column slices are 32 KB apart
+        const uint32_t b0 = smem_u32(sB), h0 = smem_u32(smem + kStSmW + k * 64 * 1024), l0 = h0 + 32 * 1024;
+        const uint32_t d = tmem + (uint32_t)(k * 64);
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+          const uint64_t ad = desc_mnmajor_sw128(b0 + ks * 2048, 256 * 128);
+          mma_f16(d, ad, desc_mnmajor_sw128(h0 + ks * 2048, 1024), IDESC, ks != 0);
+          mma_f16(d, ad, desc_mnmajor_sw128(l0 + ks * 2048, 1024), IDESC, 1u);
+        }
+        mma_commit(&sb->mma[k]);
+      }
+      if (*abort) {   // no MMA may still be running when TMEM is freed
+        mma_commit(&sb->drain);
+        mbar_wait(&sb->drain, 0, nullptr, 100000000ull);
+      }
+    }
   } else {
     // ------------------------------------------------ workers (8 warps)
     const int quarter = warp & 3, side = warp >> 2;
@@ -200,6 +235,8 @@ __global__ void __launch_bounds__(kStThr, 1)
       tmem_ld_32x32b_x32(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(k * 64 + side * 32), r);
       tmem_ld_wait();
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sb->t_empty[k]);   // accumulator k may be overwritten
       if (ok && okm) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) out[(size_t)(side * 32 + j) * kN] = __uint_as_float(r[j]);
@@ -242,30 +279,12 @@ __global__ void __launch_bounds__(kStThr, 1)
         *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
       fence_proxy_async_smem();
-      asm volatile("bar.sync 1, %0;" ::"n"(kStWork) : "memory");
-      if (tid == 0) {
-        // S[n, p] += sum_t B[t, n] (w x)[t, p]: 16 K-steps of 16 tokens
-        // (2048 bytes of both tiles); B's two 64-column slices are 32 KB apart
-        tc_fence_after();
-        const uint32_t b0 = smem_u32(sB), h0 = smem_u32(sWh), l0 = smem_u32(sWl);
-        const uint32_t d = tmem + (uint32_t)(k * 64);
-#pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          const uint64_t ad = desc_mnmajor_sw128(b0 + ks * 2048, 256 * 128);
-          mma_f16(d, ad, desc_mnmajor_sw128(h0 + ks * 2048, 1024), IDESC, ks != 0);
-          mma_f16(d, ad, desc_mnmajor_sw128(l0 + ks * 2048, 1024), IDESC, 1u);
-        }
-        mma_commit(&sb->mma[k]);
-      }
       __syncwarp();
+      if (lane == 0) mbar_arrive(&sb->w_full[k]);   // this warp's rows of operand k are staged
       // head hh-1's accumulator: its MMA ran while this head was staged
       if (hh > 0) epilogue(hh - 1);
     }
     epilogue(kHPG - 1);
-    if (tid == 0 && *abort) {   // no MMA may still be running when TMEM is freed
-      mma_commit(&sb->drain);
-      mbar_wait(&sb->drain, 0, nullptr, 100000000ull);
-    }
   }
   __syncwarp();
   __syncthreads();
