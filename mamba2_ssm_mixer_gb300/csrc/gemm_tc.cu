@@ -895,9 +895,10 @@ int fewrow_splits(int N, int kblocks, size_t smem, int bnt) {
   int s = (int)(0.9 * per_sm * num_sms() / nb);
   if (s > 8) s = 8;
   if (s > kblocks / 2) s = kblocks / 2;
-  // from 33 rows on, each split's MMAs and exchange grow with the rows and two
-  // splits beat more for the 81 weight blocks of in_proj (measured in the
-  // decode call of 64 rows: 3 splits 80.2 us, 2 splits 78.4, 4 85.8)
+  // with two CTAs per SM, from 33 rows on, each split's MMAs and exchange
+  // grow with the rows and two splits beat more for the 81 weight blocks of
+  // in_proj (measured in the decode call of 64 rows with a 4-deep ring: 3
+  // splits 80.2 us, 2 splits 78.4, 4 85.8)
   if (bnt >= 64 && nb > 64 && s > 2) s = 2;
   return s < 1 ? 1 : s;
 }
@@ -938,8 +939,13 @@ cudaError_t fewrow_t(const void* X, const void* W, uint16_t* y, int Mtok, int N,
   const int bnt = (Mtok + 15) / 16 * 16;
   if (bnt <= 16) return launch_fewrow<16, 4, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
   if (bnt <= 32) return launch_fewrow<32, 4, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
-  if (bnt <= 64) return launch_fewrow<64, 4, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
-  if (bnt <= 128) return launch_fewrow<128, 3, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
+  // 33-64 rows: an 8-deep ring (192 KB, one CTA per SM), so in_proj's 81
+  // weight blocks run unsplit and out_proj's 21 split six ways; paged decode
+  // of 64 rows 77.0 -> 74.6 us against a 4-deep ring with 2 and 8 splits
+  if (bnt <= 64) return launch_fewrow<64, 8, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
+  // 65-128 rows: a 6-deep ring (192 KB, one CTA per SM); the 23-block stack's
+  // decode of 128 rows 2.96 -> 2.85 ms against a 3-deep ring
+  if (bnt <= 128) return launch_fewrow<128, 6, kBf16>(X, W, y, Mtok, N, K, scale, w_static, err, st);
   return cudaErrorInvalidValue;
 }
 
