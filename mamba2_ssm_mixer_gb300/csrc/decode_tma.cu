@@ -1,11 +1,10 @@
-// Paged decode of the mixer block, in two kernels organised for HBM bandwidth.
-//
-// k_decode_conv: per decode row, the conv window update + SiLU of all 6144
-//   xBC channels (bf16 u into the workspace) and, per head, dt and exp(dt A);
-//   the row's conv window in the pool shifts by one in place.
-// k_decode_stream: the single-step state update of each head, read from and
-//   written back to pool[slot] in place, y = S C + D x, gated group RMSNorm
-//   and e4m3 quant of out_proj's input:
+// Paged decode of the mixer block after in_proj, in one kernel organised for
+// HBM bandwidth.
+// k_decode_stream: per work item, the conv window update + SiLU of its xBC
+//   channels and dt, exp(dt A) of its heads (the row's conv window in the pool
+//   shifts by one in place), then the single-step state update of each head,
+//   read from and written back to pool[slot] in place, y = S C + D x, gated
+//   group RMSNorm and e4m3 quant of out_proj's input:
 //  - a work item is one (row, group); its 8 heads go to one CTA (HPC = 8,
 //    from a few rows up) or, for the smallest batches, to the 8 CTAs of a
 //    thread-block cluster, one head each (HPC = 1), so a single row spreads
@@ -14,11 +13,18 @@
 //  - in each CTA a producer thread streams its heads' states (64 x 128,
 //    contiguous in the pool: 32 KB in f32, 16 KB in bf16) into a
 //    shared-memory ring with cp.async.bulk (TMA, 1-D), items ahead, with an
-//    evict-first L2 policy (the rows pass through once), and each item's u,
-//    gate and dt slices into a small staging ring; the first state loads are
-//    issued before waiting on the previous kernel (no earlier kernel of the
-//    call writes the pool); 8 consumer warps update the state in shared
-//    memory and one thread writes it back with a bulk store;
+//    evict-first L2 policy (the rows pass through once), and each item's
+//    xBC, gate and dt inputs (of zx) into a small staging ring; the first
+//    state loads are issued before waiting on the previous kernel (no earlier
+//    kernel of the call writes the pool);
+//  - the consumer warps hold the conv windows and conv weights of their next
+//    item's channels in registers, loaded one item ahead (the first item's
+//    before the wait: in_proj writes neither), run the conv + SiLU in place
+//    in the staging slot, then update the state in shared memory; one thread
+//    writes it back with a bulk store.  With a cluster, every CTA computes
+//    the group's B and C channels (it needs them) and rank 0 writes their
+//    windows back after the item's exchange, by which time every rank has
+//    read the old ones;
 //  - the group's RMSNorm needs the sum of squares over all 8 heads: with a
 //    cluster, each CTA stores its partial into every CTA of the cluster
 //    (distributed shared memory) and arrives on their barriers; each then
@@ -94,14 +100,26 @@ __device__ __forceinline__ void st4(uint16_t* p, float4 v) {
   *reinterpret_cast<uint2*>(p) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
 }
 
-// One item's inputs as they sit in the workspace and zx (bulk-copied).
+// One item's inputs as they sit in zx (bulk-copied); the conv replaces the
+// xBC inputs with u in place.
 template <int HPC>
 struct __align__(16) Staging {
-  uint16_t ux[kP * HPC];   // u, the x channels of this CTA's heads (bf16)
-  uint16_t ub[kN];         // u, the group's B
-  uint16_t uc[kN];         // u, the group's C
+  uint16_t xc[kP * HPC];   // x of this CTA's heads: the new xBC inputs, then u (bf16)
+  uint16_t bc[kN];         // the group's B: input, then u
+  uint16_t cc[kN];         // the group's C: input, then u
   uint16_t z[kP * HPC];    // the gate (z of zx) of this CTA's channels
-  float4 dtA[HPC];         // (dt, exp(dt A), -, -) per head
+  uint16_t dtr[kHPG];      // the group's raw dt (dt of zx)
+};
+
+// Conv channel pairs of an item: this CTA's x channels, then the group's B
+// and C channels (xBC numbering).
+template <int HPC>
+struct ItemPairs {
+  static constexpr int kX = kP * HPC / 2;           // x pairs
+  static constexpr int kAll = kX + kN;              // + 64 B pairs + 64 C pairs
+  __device__ static int channel(int p, int h0, int g) {
+    return p < kX ? h0 * kP + 2 * p : (p < kX + kN / 2 ? kOffB + g * kN + 2 * (p - kX) : kOffC + g * kN + 2 * (p - kX - kN / 2));
+  }
 };
 
 template <typename S, int HPC>
@@ -110,6 +128,8 @@ struct __align__(16) Smem {
   static constexpr int kU = kHPG / HPC;                                      // CTAs per cluster
   S state[kStages][kP * kN];       // 96 KB ring
   Staging<HPC> stg[kStg];
+  float2 dtA[HPC];                 // (dt, exp(dt A)) of this CTA's heads, current item
+  uint32_t wbc[kU > 1 ? kN : 1][kW - 1];   // rank 0: the group's new B, C windows (pairs), until the exchange
   float ys[kP * HPC];
   float red[kConsumers / 32];
   float part[2][kU];               // the ranks' sums of squares, by item parity
@@ -122,66 +142,14 @@ struct __align__(16) Smem {
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// conv window update + SiLU and dt of the decode rows: 128 threads x 2
-// channels per CTA, grid (6144 / 256, Bt).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(128) k_decode_conv(const uint16_t* __restrict__ zx, const uint16_t* __restrict__ conv_w,
-                                                     const uint16_t* __restrict__ conv_b,
-                                                     const float* __restrict__ A_log, const float* __restrict__ dt_bias,
-                                                     uint16_t* __restrict__ conv_pool, int n_slots,
-                                                     const int32_t* __restrict__ slot_idx, uint16_t* __restrict__ u,
-                                                     float4* __restrict__ dtA, uint16_t* __restrict__ taps_u,
-                                                     float* __restrict__ taps_dt) {
-  pdl_wait();
-  pdl_trigger();
-  const int b = blockIdx.y, tid = threadIdx.x;
-  const int slot = slot_idx[b];
-  if (slot < 0 || slot >= n_slots) return;        // the state kernel flags and skips the row
-  bool hit = false;
-  for (int j = tid; j < b; j += blockDim.x) hit |= (slot_idx[j] == slot);
-  if (__syncthreads_or(hit)) return;              // a repeated slot: only its first row advances it
-  const uint16_t* zrow = zx + (size_t)b * kZ;
-  const int c = blockIdx.x * 256 + 2 * tid;
-  // the taps of channels c and c + 1: 6 bf16, [channel][tap], tap 0 oldest
-  uint32_t* tp = reinterpret_cast<uint32_t*>(conv_pool + ((size_t)slot * kConv + c) * (kW - 1));
-  const uint32_t w0 = tp[0], w1 = tp[1], w2 = tp[2];
-  const uint32_t xn = *reinterpret_cast<const uint32_t*>(zrow + kOffXBC + c);
-  const uint4 cw = *reinterpret_cast<const uint4*>(conv_w + (size_t)c * kW);
-  const uint16_t t0a = w0 & 0xFFFF, t1a = w0 >> 16, t2a = w1 & 0xFFFF;
-  const uint16_t t0b = w1 >> 16, t1b = w2 & 0xFFFF, t2b = w2 >> 16;
-  const uint16_t xa = xn & 0xFFFF, xb = xn >> 16;
-  float acc_a = conv_b ? bfbits2f(conv_b[c]) : 0.f;
-  float acc_b = conv_b ? bfbits2f(conv_b[c + 1]) : 0.f;
-  acc_a = fmaf(bfbits2f(cw.x & 0xFFFF), bfbits2f(t0a), acc_a);
-  acc_a = fmaf(bfbits2f(cw.x >> 16), bfbits2f(t1a), acc_a);
-  acc_a = fmaf(bfbits2f(cw.y & 0xFFFF), bfbits2f(t2a), acc_a);
-  acc_a = fmaf(bfbits2f(cw.y >> 16), bfbits2f(xa), acc_a);
-  acc_b = fmaf(bfbits2f(cw.z & 0xFFFF), bfbits2f(t0b), acc_b);
-  acc_b = fmaf(bfbits2f(cw.z >> 16), bfbits2f(t1b), acc_b);
-  acc_b = fmaf(bfbits2f(cw.w & 0xFFFF), bfbits2f(t2b), acc_b);
-  acc_b = fmaf(bfbits2f(cw.w >> 16), bfbits2f(xb), acc_b);
-  const uint32_t uu = (uint32_t)f2bfbits(silu_f(acc_a)) | ((uint32_t)f2bfbits(silu_f(acc_b)) << 16);
-  *reinterpret_cast<uint32_t*>(u + (size_t)b * kConv + c) = uu;
-  if (taps_u) *reinterpret_cast<uint32_t*>(taps_u + (size_t)b * kConv + c) = uu;
-  // the window shifts in: (t1, t2, x_new) per channel
-  tp[0] = (uint32_t)t1a | ((uint32_t)t2a << 16);
-  tp[1] = (uint32_t)xa | ((uint32_t)t1b << 16);
-  tp[2] = (uint32_t)t2b | ((uint32_t)xb << 16);
-  if (blockIdx.x == 0 && tid < kNH) {
-    const int h = tid;
-    const float dt = softplus_f(bfbits2f(zrow[kOffDt + h]) + dt_bias[h]);
-    dtA[(size_t)b * kNH + h] = make_float4(dt, expf(dt * -expf(A_log[h])), 0.f, 0.f);
-    if (taps_dt) taps_dt[(size_t)b * kNH + h] = dt;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// state update, y, gated norm and quant; cluster of 8 / HPC CTAs per item
+// conv, state update, y, gated norm and quant; cluster of 8 / HPC CTAs per item
 // ---------------------------------------------------------------------------
 template <typename S, int HPC>
 __global__ void __launch_bounds__(kThreadsT, 2)
-    k_decode_stream(const uint16_t* __restrict__ zx, const uint16_t* __restrict__ u, const float4* __restrict__ dtA,
-                    const float* __restrict__ Dp, const uint16_t* __restrict__ norm_w, float eps, float s_y,
+    k_decode_stream(const uint16_t* __restrict__ zx, const uint16_t* __restrict__ conv_w,
+                    const uint16_t* __restrict__ conv_b, const float* __restrict__ A_log,
+                    const float* __restrict__ dt_bias, const float* __restrict__ Dp,
+                    const uint16_t* __restrict__ norm_w, float eps, float s_y, uint16_t* __restrict__ conv_pool,
                     S* __restrict__ ssm_pool, int n_slots, const int32_t* __restrict__ slot_idx, int Bt,
                     uint8_t* __restrict__ q2, int* __restrict__ err, DecodeTaps taps,
                     const uint8_t* __restrict__ l2_prefetch, uint32_t l2_prefetch_bytes) {
@@ -259,12 +227,12 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         if (mbar_wait(&sm.sempty[ss], sphase ^ 1u, abort)) {
           Staging<HPC>& st = sm.stg[ss];
           mbar_expect_tx(&sm.sfull[ss], kStgBytes);
-          const uint16_t* ur = u + (size_t)b * kConv;
-          bulk_load(st.ux, ur + h0 * kP, kP * HPC * 2, &sm.sfull[ss], pol_stream);
-          bulk_load(st.ub, ur + kOffB + g * kN, kN * 2, &sm.sfull[ss], pol_stream);
-          bulk_load(st.uc, ur + kOffC + g * kN, kN * 2, &sm.sfull[ss], pol_stream);
-          bulk_load(st.z, zx + (size_t)b * kZ + h0 * kP, kP * HPC * 2, &sm.sfull[ss], pol_stream);
-          bulk_load(st.dtA, dtA + (size_t)b * kNH + h0, 16 * HPC, &sm.sfull[ss], pol_stream);
+          const uint16_t* zr = zx + (size_t)b * kZ;
+          bulk_load(st.xc, zr + kOffXBC + h0 * kP, kP * HPC * 2, &sm.sfull[ss], pol_stream);
+          bulk_load(st.bc, zr + kOffXBC + kOffB + g * kN, kN * 2, &sm.sfull[ss], pol_stream);
+          bulk_load(st.cc, zr + kOffXBC + kOffC + g * kN, kN * 2, &sm.sfull[ss], pol_stream);
+          bulk_load(st.z, zr + h0 * kP, kP * HPC * 2, &sm.sfull[ss], pol_stream);
+          bulk_load(st.dtr, zr + kOffDt + g * kHPG, kHPG * 2, &sm.sfull[ss], pol_stream);
           sissued[ss] = true;
           sissued_phase[ss] = sphase;
           if (++ss == kStg) ss = 0, sphase ^= 1u;
@@ -309,6 +277,31 @@ __global__ void __launch_bounds__(kThreadsT, 2)
     }
   } else {
     // ------------------------------------------------ consumer warps
+    using IP = ItemPairs<HPC>;
+    constexpr int kPPT = (IP::kAll + kConsumers - 1) / kConsumers;   // conv pairs per thread
+    // the next item's conv windows (3 words: taps 0-2 of two channels), conv
+    // weights and bias of this thread's pairs, loaded one item ahead
+    uint32_t win[kPPT][kW - 1], cbv[kPPT];
+    uint4 cwv[kPPT];
+    auto load_item = [&](int it) {
+      if (it >= items) return;
+      const int b = it / kG, g = it % kG, slot = slot_idx[b];
+      if (slot < 0 || slot >= n_slots) return;   // never read outside the pool
+      const int h0 = g * kHPG + rank * HPC;
+#pragma unroll
+      for (int j = 0; j < kPPT; ++j) {
+        const int pp = tid + j * kConsumers;
+        if (pp < IP::kAll) {
+          const int c = IP::channel(pp, h0, g);
+          const uint32_t* tp = reinterpret_cast<const uint32_t*>(conv_pool + ((size_t)slot * kConv + c) * (kW - 1));
+#pragma unroll
+          for (int k = 0; k < kW - 1; ++k) win[j][k] = tp[k];
+          cwv[j] = *reinterpret_cast<const uint4*>(conv_w + (size_t)c * kW);
+          cbv[j] = conv_b ? *reinterpret_cast<const uint32_t*>(conv_b + c) : 0u;
+        }
+      }
+    };
+    load_item(cluster);   // before the wait: no kernel of the call writes the windows or the weights
     pdl_wait();
     pdl_trigger();
     int stage = 0, ss = 0;
@@ -330,15 +323,63 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         if (tid == 0 && rank == 0 && dup) atomicOr(err, kErrDupSlot);
         if (tid == 0 && rank == 0 && bad && slot != -1) atomicOr(err, kErrSlot);
         for (int j = tid; j < kCh; j += kConsumers) q2c[j] = 0;
+        load_item(it + nclusters);
         continue;
       }
       if (!mbar_wait(&sm.sfull[ss], sphase, abort)) {
         if (tid == 0) atomicOr(err, kErrTimeout);
         *abort = 1;
       }
-      const Staging<HPC>& st = sm.stg[ss];
-      const uint2 bw = *reinterpret_cast<const uint2*>(st.ub + 4 * lane);
-      const uint2 cw = *reinterpret_cast<const uint2*>(st.uc + 4 * lane);
+      Staging<HPC>& st = sm.stg[ss];
+      // conv + SiLU of the item's channel pairs (as the prefill conv: bias,
+      // then taps oldest first, then the new input), u in place of the input;
+      // the window shifts in (t1, t2, x_new) per channel
+#pragma unroll
+      for (int j = 0; j < kPPT; ++j) {
+        const int pp = tid + j * kConsumers;
+        if (pp < IP::kAll) {
+          const int c = IP::channel(pp, h0, g);
+          uint16_t* xs = pp < IP::kX ? &st.xc[2 * pp]
+                                     : (pp < IP::kX + kN / 2 ? &st.bc[2 * (pp - IP::kX)] : &st.cc[2 * (pp - IP::kX - kN / 2)]);
+          const uint32_t xn = *reinterpret_cast<const uint32_t*>(xs);
+          const uint32_t w0 = win[j][0], w1 = win[j][1], w2 = win[j][2];
+          const uint4 cw = cwv[j];
+          const uint16_t t0a = w0 & 0xFFFF, t1a = w0 >> 16, t2a = w1 & 0xFFFF;
+          const uint16_t t0b = w1 >> 16, t1b = w2 & 0xFFFF, t2b = w2 >> 16;
+          const uint16_t xa = xn & 0xFFFF, xb = xn >> 16;
+          float acc_a = bfbits2f(cbv[j] & 0xFFFF), acc_b = bfbits2f(cbv[j] >> 16);
+          acc_a = fmaf(bfbits2f(cw.x & 0xFFFF), bfbits2f(t0a), acc_a);
+          acc_a = fmaf(bfbits2f(cw.x >> 16), bfbits2f(t1a), acc_a);
+          acc_a = fmaf(bfbits2f(cw.y & 0xFFFF), bfbits2f(t2a), acc_a);
+          acc_a = fmaf(bfbits2f(cw.y >> 16), bfbits2f(xa), acc_a);
+          acc_b = fmaf(bfbits2f(cw.z & 0xFFFF), bfbits2f(t0b), acc_b);
+          acc_b = fmaf(bfbits2f(cw.z >> 16), bfbits2f(t1b), acc_b);
+          acc_b = fmaf(bfbits2f(cw.w & 0xFFFF), bfbits2f(t2b), acc_b);
+          acc_b = fmaf(bfbits2f(cw.w >> 16), bfbits2f(xb), acc_b);
+          const uint32_t uu = (uint32_t)f2bfbits(silu_f(acc_a)) | ((uint32_t)f2bfbits(silu_f(acc_b)) << 16);
+          *reinterpret_cast<uint32_t*>(xs) = uu;
+          const uint32_t n0w = (uint32_t)t1a | ((uint32_t)t2a << 16), n1w = (uint32_t)xa | ((uint32_t)t1b << 16),
+                         n2w = (uint32_t)t2b | ((uint32_t)xb << 16);
+          const bool own = pp < IP::kX || kU == 1;   // x windows, or B/C without a cluster
+          if (own) {
+            uint32_t* tp = reinterpret_cast<uint32_t*>(conv_pool + ((size_t)slot * kConv + c) * (kW - 1));
+            tp[0] = n0w, tp[1] = n1w, tp[2] = n2w;
+          } else if (rank == 0) {
+            sm.wbc[pp - IP::kX][0] = n0w, sm.wbc[pp - IP::kX][1] = n1w, sm.wbc[pp - IP::kX][2] = n2w;
+          }
+          if (taps.u && (own || rank == 0)) *reinterpret_cast<uint32_t*>(taps.u + (size_t)b * kConv + c) = uu;
+        }
+      }
+      if (tid < HPC) {
+        const int h = h0 + tid;
+        const float dt = softplus_f(bfbits2f(st.dtr[rank * HPC + tid]) + dt_bias[h]);
+        sm.dtA[tid] = make_float2(dt, expf(dt * -expf(A_log[h])));
+        if (taps.dt) taps.dt[(size_t)b * kNH + h] = dt;
+      }
+      load_item(it + nclusters);
+      consumers_sync();   // every u and dt of the item is in shared memory
+      const uint2 bw = *reinterpret_cast<const uint2*>(st.bc + 4 * lane);
+      const uint2 cw = *reinterpret_cast<const uint2*>(st.cc + 4 * lane);
       const float4 bv = make_float4(__uint_as_float(bw.x << 16), __uint_as_float(bw.x & 0xFFFF0000u),
                                     __uint_as_float(bw.y << 16), __uint_as_float(bw.y & 0xFFFF0000u));
       const float4 cv = make_float4(__uint_as_float(cw.x << 16), __uint_as_float(cw.x & 0xFFFF0000u),
@@ -351,13 +392,13 @@ __global__ void __launch_bounds__(kThreadsT, 2)
           *abort = 1;
         }
         S* St = sm.state[stage];
-        const float dt = st.dtA[hh].x, dA = st.dtA[hh].y;
+        const float dt = sm.dtA[hh].x, dA = sm.dtA[hh].y;
         float part[kP / 8];
 #pragma unroll
         for (int i = 0; i < kP / 8; ++i) {
           const int p = warp + 8 * i;
           float4 s4 = ld4(St + p * kN + 4 * lane);
-          const float xd = dt * bfbits2f(st.ux[hh * kP + p]);
+          const float xd = dt * bfbits2f(st.xc[hh * kP + p]);
           s4.x = fmaf(dA, s4.x, xd * bv.x);
           s4.y = fmaf(dA, s4.y, xd * bv.y);
           s4.z = fmaf(dA, s4.z, xd * bv.z);
@@ -372,7 +413,7 @@ __global__ void __launch_bounds__(kThreadsT, 2)
           for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
           if (lane == 0) {
             const int p = warp + 8 * i;
-            sm.ys[hh * kP + p] = round_bf16(v + Dp[h] * bfbits2f(st.ux[hh * kP + p]));
+            sm.ys[hh * kP + p] = round_bf16(v + Dp[h] * bfbits2f(st.xc[hh * kP + p]));
           }
         }
         fence_async_smem();
@@ -420,6 +461,13 @@ __global__ void __launch_bounds__(kThreadsT, 2)
         if (!mbar_wait_cluster(&sm.xb[par], (uint32_t)(k >> 1) & 1u, abort)) {
           if (tid == 0) atomicOr(err, kErrTimeout);
           *abort = 1;
+        }
+        // every rank has read the group's old B, C windows (before its own
+        // arrival): rank 0 writes the new ones
+        if (rank == 0 && tid < kN) {
+          const int c = tid < kN / 2 ? kOffB + g * kN + 2 * tid : kOffC + g * kN + 2 * (tid - kN / 2);
+          uint32_t* tp = reinterpret_cast<uint32_t*>(conv_pool + ((size_t)slot * kConv + c) * (kW - 1));
+          tp[0] = sm.wbc[tid][0], tp[1] = sm.wbc[tid][1], tp[2] = sm.wbc[tid][2];
         }
 #pragma unroll
         for (int r = 0; r < kU; ++r) tot += sm.part[par][r];
@@ -488,8 +536,8 @@ int resident_clusters(size_t smem) {
 }  // namespace
 
 template <typename S, int HPC>
-static cudaError_t launch_state_t(const uint16_t* zx, const uint16_t* u, const float4* dtA, const BlockParams& bp,
-                                  S* ssm_pool, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
+static cudaError_t launch_state_t(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, S* ssm_pool,
+                                  int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
                                   const DecodeTaps& taps, const void* l2_prefetch, size_t l2_prefetch_bytes,
                                   cudaStream_t st) {
   constexpr int kU = kHPG / HPC;
@@ -515,8 +563,9 @@ static cudaError_t launch_state_t(const uint16_t* zx, const uint16_t* u, const f
   cfg.attrs = attr;
   cfg.numAttrs = kU > 1 ? 2 : 1;
   const uint32_t pf = (l2_prefetch && l2_prefetch_bytes < (1u << 31)) ? (uint32_t)(l2_prefetch_bytes & ~(size_t)15) : 0u;
-  return cudaLaunchKernelEx(&cfg, k, zx, u, dtA, bp.D, bp.norm_w, bp.eps, bp.s_y, ssm_pool, n_slots, slot_idx, Bt, q2,
-                            err, taps, static_cast<const uint8_t*>(pf ? l2_prefetch : nullptr), pf);
+  return cudaLaunchKernelEx(&cfg, k, zx, bp.conv_w, bp.conv_b, bp.A_log, bp.dt_bias, bp.D, bp.norm_w, bp.eps, bp.s_y,
+                            conv_pool, ssm_pool, n_slots, slot_idx, Bt, q2, err, taps,
+                            static_cast<const uint8_t*>(pf ? l2_prefetch : nullptr), pf);
 }
 
 // Heads per CTA of the state kernel for a batch of Bt rows: one for the
@@ -526,40 +575,33 @@ static cudaError_t launch_state_t(const uint16_t* zx, const uint16_t* u, const f
 int decode_heads_per_cta(int Bt) { return Bt <= 2 ? 1 : 8; }
 
 template <typename S>
-static cudaError_t launch_state_s(const uint16_t* zx, const uint16_t* u, const float4* dtA, const BlockParams& bp,
-                                  S* ssm_pool, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
+static cudaError_t launch_state_s(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, S* ssm_pool,
+                                  int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
                                   const DecodeTaps& taps, const void* l2_prefetch, size_t l2_prefetch_bytes,
                                   cudaStream_t st) {
   switch (decode_heads_per_cta(Bt)) {
     case 1:
-      return launch_state_t<S, 1>(zx, u, dtA, bp, ssm_pool, n_slots, slot_idx, Bt, q2, err, taps, l2_prefetch,
+      return launch_state_t<S, 1>(zx, bp, conv_pool, ssm_pool, n_slots, slot_idx, Bt, q2, err, taps, l2_prefetch,
                                   l2_prefetch_bytes, st);
     default:
-      return launch_state_t<S, 8>(zx, u, dtA, bp, ssm_pool, n_slots, slot_idx, Bt, q2, err, taps, l2_prefetch,
+      return launch_state_t<S, 8>(zx, bp, conv_pool, ssm_pool, n_slots, slot_idx, Bt, q2, err, taps, l2_prefetch,
                                   l2_prefetch_bytes, st);
   }
 }
 
-size_t decode_scratch_bytes(int Bt) { return (size_t)Bt * (kConv * 2 + kNH * 16); }
-
 cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, void* ssm_pool,
                                  bool bf16_state, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
-                                 const DecodeTaps& taps, void* scratch, cudaStream_t st, int* launches,
-                                 const void* l2_prefetch, size_t l2_prefetch_bytes) {
-  uint16_t* u = static_cast<uint16_t*>(scratch);
-  float4* dtA = reinterpret_cast<float4*>(static_cast<char*>(scratch) + (size_t)Bt * kConv * 2);
+                                 const DecodeTaps& taps, cudaStream_t st, int* launches, const void* l2_prefetch,
+                                 size_t l2_prefetch_bytes) {
   *launches = 0;
-  cudaError_t e = launch_pdl(k_decode_conv, dim3(kConv / 256, Bt), dim3(128), 0, st, zx, bp.conv_w, bp.conv_b,
-                             bp.A_log, bp.dt_bias, conv_pool, n_slots, slot_idx, u, (float4*)dtA, taps.u, taps.dt);
-  if (e != cudaSuccess) return e;
-  *launches = 1;
+  cudaError_t e;
   if (bf16_state)
-    e = launch_state_s(zx, u, dtA, bp, static_cast<uint16_t*>(ssm_pool), n_slots, slot_idx, Bt, q2, err, taps,
+    e = launch_state_s(zx, bp, conv_pool, static_cast<uint16_t*>(ssm_pool), n_slots, slot_idx, Bt, q2, err, taps,
                        l2_prefetch, l2_prefetch_bytes, st);
   else
-    e = launch_state_s(zx, u, dtA, bp, static_cast<float*>(ssm_pool), n_slots, slot_idx, Bt, q2, err, taps,
+    e = launch_state_s(zx, bp, conv_pool, static_cast<float*>(ssm_pool), n_slots, slot_idx, Bt, q2, err, taps,
                        l2_prefetch, l2_prefetch_bytes, st);
-  if (e == cudaSuccess) *launches = 2;
+  if (e == cudaSuccess) *launches = 1;
   return e;
 }
 

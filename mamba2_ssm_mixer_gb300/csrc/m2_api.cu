@@ -536,7 +536,6 @@ m2_status m2_prefill_q(m2_handle* h, const uint8_t* hidden_q, const int32_t* seq
 struct DecodeWs {
   uint8_t* q;
   uint16_t* zx;
-  void* dscratch;   // the decode rows' u and dt
   uint8_t* q2;
   uint16_t* o;   // W8A16 arm: the gated-norm output, out_proj's bf16 input
   void* gemm_ws;
@@ -549,7 +548,6 @@ static DecodeWs carve_decode(void* base, int Bt, bool w8a16) {
   DecodeWs w;
   w.q = w8a16 ? nullptr : c.take<uint8_t>((size_t)Bt * kH);
   w.zx = c.take<uint16_t>((size_t)Bt * kZ);
-  w.dscratch = c.take<char>(decode_scratch_bytes(Bt));
   w.q2 = c.take<uint8_t>((size_t)Bt * kI);
   w.o = w8a16 ? c.take<uint16_t>((size_t)Bt * kI) : nullptr;
   size_t g1 = w8a16 ? gemm_workspace_bytes_bf16(Bt, kZ, kH) : gemm_workspace_bytes(Bt, kZ, kH);
@@ -613,7 +611,7 @@ static m2_status decode_impl(m2_handle* h, const uint16_t* hidden, const uint8_t
   const size_t w2_bytes = (size_t)kH * kI * (w8a16 ? 2 : 1);
   M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, nl,
            launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, h->cfg.ssm_dtype == M2_DTYPE_BF16, n_slots, slot_idx,
-                                Bt, w.q2, h->err, dt, w.dscratch, st, &nl, w2, w2_bytes));
+                                Bt, w.q2, h->err, dt, st, &nl, w2, w2_bytes));
   if (w8a16) {
     M2_STAGE(h, st, M2_STAGE_DEC_OUT_PROJ, nl,
              gemm_bf16(w.o, h->out_proj_bf16, out, Bt, kH, kI, 1.0f, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
@@ -663,7 +661,6 @@ struct MixedWs {
   PrefillWs pf;   // prefill-only buffers (u, cum/dt, states, S_in, y) of T tokens
   uint8_t* q;     // [Bt + T, 2688]
   uint16_t* zx;   // [Bt + T, 10304]
-  void* dscratch; // the decode rows' u and dt
   uint8_t* q2;    // [Bt + T, 4096]
   void* gemm_ws;
   size_t gemm_ws_bytes;
@@ -676,7 +673,6 @@ static MixedWs carve_mixed(void* base, int Bt, int T, int chunks) {
   const size_t R = (size_t)Bt + T;
   w.q = c.take<uint8_t>(R * kH);
   w.zx = c.take<uint16_t>(R * kZ);
-  w.dscratch = c.take<char>(decode_scratch_bytes(Bt));
   w.q2 = c.take<uint8_t>(R * kI);
   w.pf = PrefillWs{};
   w.pf.u = c.take<uint16_t>((size_t)T * kConv);
@@ -768,7 +764,7 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
       if (h->taps_on) dt.o = h->taps.o, dt.y = h->taps.y;
       int dl = 0;
       M2_CUDA(launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err,
-                                   dt, w.dscratch, h->side, &dl));
+                                   dt, h->side, &dl));
       h->stats.kernel_launches += (uint64_t)dl;
       M2_CUDA(cudaEventRecord(h->join_ev, h->side));
     }
@@ -804,7 +800,7 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
     int dl = 0;
     M2_STAGE(h, st, M2_STAGE_DECODE_FUSED, dl,
              launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err,
-                                  dt, w.dscratch, st, &dl));
+                                  dt, st, &dl));
   }
   M2_STAGE(h, st, M2_STAGE_OUT_PROJ, nl,
            gemm_fp8(w.q2, h->out_proj, out, R, kH, kI, sc2, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));

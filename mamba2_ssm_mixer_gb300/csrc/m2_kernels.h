@@ -79,17 +79,15 @@ cudaError_t launch_ssd_chunk_scan_tc(const uint16_t* u, const CumDt* cumdt, cons
                                      const BlockParams& bp, const SeqInfo& si, uint16_t* y, int* err,
                                      cudaStream_t st);
 
-// decode_tma.cu: the conv window update + dt kernel, then the persistent,
-// TMA-streamed state kernel.  ssm_pool: f32 rows, or bf16 rows when
-// bf16_state (widened to f32 when read, rounded to bf16 when written back).
-// scratch: decode_scratch_bytes(Bt) bytes (u and dt of the rows), 16-byte
-// aligned.  l2_prefetch (may be null): l2_prefetch_bytes of a buffer the next
-// kernel reads (the out_proj weights), brought into L2 with an evict-last
-// policy.  *launches receives the number of kernels launched.
-size_t decode_scratch_bytes(int Bt);
+// decode_tma.cu: the persistent, TMA-streamed decode kernel (conv window
+// update, dt, state update, y, gated norm, quant).  ssm_pool: f32 rows, or
+// bf16 rows when bf16_state (widened to f32 when read, rounded to bf16 when
+// written back).  l2_prefetch (may be null): l2_prefetch_bytes of a buffer
+// the next kernel reads (the out_proj weights), brought into L2 with an
+// evict-last policy.  *launches receives the number of kernels launched.
 cudaError_t launch_decode_stream(const uint16_t* zx, const BlockParams& bp, uint16_t* conv_pool, void* ssm_pool,
                                  bool bf16_state, int n_slots, const int32_t* slot_idx, int Bt, uint8_t* q2, int* err,
-                                 const DecodeTaps& taps, void* scratch, cudaStream_t st, int* launches,
+                                 const DecodeTaps& taps, cudaStream_t st, int* launches,
                                  const void* l2_prefetch = nullptr, size_t l2_prefetch_bytes = 0);
 
 }  // namespace m2
