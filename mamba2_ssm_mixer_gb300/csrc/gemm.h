@@ -31,10 +31,11 @@ cudaError_t gemm_tc_fewrow(const uint8_t* X, const uint8_t* W, uint16_t* y, int 
                            bool w_static, int* err, cudaStream_t st);
 cudaError_t gemm_tc_fewrow_bf16(const uint16_t* X, const uint16_t* W, uint16_t* y, int Mtok, int N, int K, float scale,
                                 bool w_static, int* err, cudaStream_t st);
-cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
-                        cudaStream_t st);
+// More than 256 rows: the persistent CTA-pair kernel; w_static as above.
+cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale,
+                        bool w_static, int* err, cudaStream_t st);
 cudaError_t gemm_tc_big_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, int N, int K, float scale,
-                             int* err, cudaStream_t st);
+                             bool w_static, int* err, cudaStream_t st);
 constexpr int kSkinnyMaxRows = 256;
 
 // Failure-detection self-test: one CTA allocates TMEM, waits with the GEMMs'

@@ -30,7 +30,7 @@ cudaError_t gemm_fp8(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int
   }
   if (M <= kSkinnyMaxRows) return gemm_tc_skinny(A, B, y, M, N, K, scale, ws, ws_bytes, err, st, launches);
   *launches = 1;
-  return gemm_tc_big(A, B, y, M, N, K, scale, err, st);
+  return gemm_tc_big(A, B, y, M, N, K, scale, w_static, err, st);
 }
 
 cudaError_t gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, int N, int K, float scale, void* ws,
@@ -43,7 +43,7 @@ cudaError_t gemm_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, 
   }
   if (M <= kSkinnyMaxRows) return gemm_tc_skinny_bf16(A, B, y, M, N, K, scale, ws, ws_bytes, err, st, launches);
   *launches = 1;
-  return gemm_tc_big_bf16(A, B, y, M, N, K, scale, err, st);
+  return gemm_tc_big_bf16(A, B, y, M, N, K, scale, w_static, err, st);
 }
 
 }  // namespace m2

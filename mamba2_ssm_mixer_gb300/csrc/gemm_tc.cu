@@ -163,13 +163,16 @@ __device__ __forceinline__ void epilogue_rows(uint32_t tcol, uint8_t* bufs, int&
 // each CTA's TMEM.  Barriers: every load of a stage completes on the even
 // CTA's full[stage] (expecting both CTAs' bytes); the MMA commits arrive on
 // empty[stage] and tfull[acc] of both CTAs (multicast); both CTAs' epilogue
-// warps arrive on the even CTA's tempty[acc].
+// warps arrive on the even CTA's tempty[acc].  w_static: no kernel of the
+// stream writes B (the handle's weights), so the B slices of the first ring
+// stages are requested before waiting on the previous kernel (their bytes
+// are added to full[stage] then; its arrival comes with the A slice).
 // ---------------------------------------------------------------------------
 template <int BN, int STAGES, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, int tma_store, uint16_t* __restrict__ C, int M, int N,
-                int K, float scale, int* err) {
+                int K, float scale, int w_static, int* err) {
   static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN");
   static_assert(STAGES <= 8, "STAGES");
   constexpr int kPM = 2 * kBM;                        // rows of a pair tile
@@ -218,7 +221,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();                                     // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
-  pdl_wait();      // operands are produced by the previous kernel
+  // the first tile's B slices of the first ring stages, before the wait
+  const int npre = (w_static && pair < num_tiles) ? (kblocks < STAGES ? kblocks : STAGES) : 0;
+  if (warp == 0 && lane == 0) {
+    const int n0 = (pair / tiles_m) * BN + (int)rank * (BN / 2);
+    for (int s = 0; s < npre; ++s) {
+      if (rank == 0) mbar_add_tx(&ctl->full[s], 2 * B_BYTES);
+      tma_load_2d_pair(smem + s * STAGE_BYTES + A_BYTES, &tmB, cluster_map(smem_u32(&ctl->full[s]), 0),
+                       s * (kBK / ES), n0);
+    }
+  }
+  __syncwarp();
+  pdl_wait();      // A is produced by the previous kernel
   pdl_trigger();
 
   if (warp == 0) {
@@ -230,10 +244,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
       bool ok = true;
+      int nissued = 0;   // stages whose A slice has been requested
       for (int tile = pair; tile < num_tiles && ok; tile += npairs) {
         const int m0 = (tile % tiles_m) * kPM + (int)rank * kBM;
         const int n0 = (tile / tiles_m) * BN + (int)rank * (BN / 2);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = 0; kb < kblocks; ++kb, ++nissued) {
+          const bool pre = nissued < npre;   // its B slice is already on the way
           if (!mbar_wait(&ctl->empty[stage], phase ^ 1u, abort)) {
             raise_abort(ctl, err);
             ok = false;
@@ -241,9 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sA = smem + stage * STAGE_BYTES;
           const uint32_t full0 = cluster_map(smem_u32(&ctl->full[stage]), 0);
-          if (rank == 0) mbar_expect_tx(&ctl->full[stage], 2 * STAGE_BYTES);
+          if (rank == 0) mbar_expect_tx(&ctl->full[stage], pre ? 2 * A_BYTES : 2 * STAGE_BYTES);
           tma_load_2d_pair(sA, &tmA, full0, kb * (kBK / ES), m0);
-          tma_load_2d_pair(sA + A_BYTES, &tmB, full0, kb * (kBK / ES), n0);
+          if (!pre) tma_load_2d_pair(sA + A_BYTES, &tmB, full0, kb * (kBK / ES), n0);
           issued[stage] = true;
           issued_phase[stage] = phase;
           if (++stage == STAGES) stage = 0, phase ^= 1u;
@@ -251,10 +267,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (*abort) {
         // the even CTA's full barriers count both CTAs' copies: let those in
-        // flight land before the pair exits
+        // flight land before the pair exits (a stage whose B slice went out
+        // before the wait but whose A slice never did gets its arrival here)
         if (rank == 0)
-          for (int s = 0; s < STAGES; ++s)
+          for (int s = 0; s < STAGES; ++s) {
+            if (!issued[s] && s < npre) {
+              mbar_arrive(&ctl->full[s]);
+              issued[s] = true;
+              issued_phase[s] = 0;
+            }
             if (issued[s]) mbar_wait(&ctl->full[s], issued_phase[s], nullptr, 100000000ull);
+          }
       } else {
         // every stage's last MMA commit has arrived on this CTA's empty
         // barrier before the CTA may exit
@@ -836,8 +859,8 @@ int pair_clusters(size_t smem) {
 }
 
 template <int BN, int STAGES, bool kBf16>
-cudaError_t launch_pair(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, int* err,
-                        cudaStream_t st) {
+cudaError_t launch_pair(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, bool w_static,
+                        int* err, cudaStream_t st) {
   CUtensorMap ta, tb;
   cudaError_t e;
   constexpr int es = kBf16 ? 2 : 1;
@@ -865,7 +888,7 @@ cudaError_t launch_pair(const void* A, const void* B, uint16_t* y, int M, int N,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, k, ta, tb, tcm, tma_store, y, M, N, K, scale, err);
+  return cudaLaunchKernelEx(&cfg, k, ta, tb, tcm, tma_store, y, M, N, K, scale, (int)w_static, err);
 }
 
 template <int BNT, int STAGES, bool kBf16>
@@ -1011,11 +1034,11 @@ cudaError_t skinny_t(const void* X, const void* W, uint16_t* y, int Mtok, int N,
 }
 
 template <bool kBf16>
-cudaError_t big_t(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, int* err,
-                  cudaStream_t st) {
+cudaError_t big_t(const void* A, const void* B, uint16_t* y, int M, int N, int K, float scale, bool w_static,
+                  int* err, cudaStream_t st) {
   // 256 x 256 tiles on CTA pairs (N = 2688 leaves its last tile half
   // empty, which still beats narrower tiles' extra waves)
-  return launch_pair<256, 6, kBf16>(A, B, y, M, N, K, scale, err, st);
+  return launch_pair<256, 6, kBf16>(A, B, y, M, N, K, scale, w_static, err, st);
 }
 
 }  // namespace
@@ -1040,14 +1063,14 @@ cudaError_t gemm_tc_fewrow_bf16(const uint16_t* X, const uint16_t* W, uint16_t* 
   return fewrow_t<true>(X, W, y, Mtok, N, K, scale, w_static, err, st);
 }
 
-cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale, int* err,
-                        cudaStream_t st) {
-  return big_t<false>(A, B, y, M, N, K, scale, err, st);
+cudaError_t gemm_tc_big(const uint8_t* A, const uint8_t* B, uint16_t* y, int M, int N, int K, float scale,
+                        bool w_static, int* err, cudaStream_t st) {
+  return big_t<false>(A, B, y, M, N, K, scale, w_static, err, st);
 }
 
 cudaError_t gemm_tc_big_bf16(const uint16_t* A, const uint16_t* B, uint16_t* y, int M, int N, int K, float scale,
-                             int* err, cudaStream_t st) {
-  return big_t<true>(A, B, y, M, N, K, scale, err, st);
+                             bool w_static, int* err, cudaStream_t st) {
+  return big_t<true>(A, B, y, M, N, K, scale, w_static, err, st);
 }
 
 }  // namespace m2
