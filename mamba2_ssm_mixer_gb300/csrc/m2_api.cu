@@ -742,15 +742,32 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
   M2_STAGE(h, st, M2_STAGE_QUANT_IN, 1, launch_quant_e4m3(hidden, (size_t)R * kH, h->cfg.s_x, w.q, st));
   M2_STAGE(h, st, M2_STAGE_IN_PROJ, nl,
            gemm_fp8(w.q, h->in_proj, w.zx, R, kZ, kH, sc1, w.gemm_ws, w.gemm_ws_bytes, h->err, st, &nl, true));
-  // A second stream runs, beside the prefill rows' conv and scan, the
-  // prefill cumsum (it reads only the in_proj output) and then the decode
-  // rows' state stream (HBM-bound; the scan is latency-bound and its last
-  // waves leave SMs idle).  The chunk states wait for the cumsum, the out_proj
-  // for the decode rows.  Stage profiling keeps everything on the caller's
-  // stream.
+  // A second stream runs the prefill cumsum beside the conv (it reads only
+  // the in_proj output), and the decode rows' state kernel beside the chunk
+  // scan: that kernel is HBM-bound and the scan latency-bound, while next to
+  // the chunk states or the state pass the two contend (the chunk states'
+  // 230 KB CTAs wait for SMs the state kernel holds; the state pass is
+  // HBM-bound too).  Measured on the mixed step of 64 decode rows and 4 x 2048
+  // prefill tokens: started after the cumsum 0.470 ms, after the chunk states
+  // 0.473, after the state pass 0.457, after the scan 0.475.  With the
+  // token-by-token SSD path it starts at once.  The chunk states wait for the
+  // cumsum, the out_proj for the decode rows.  Stage profiling keeps
+  // everything on the caller's stream.
   const bool fork = !h->prof_on && T > 0;
   const bool fork_decode = fork && Bt > 0;
   const bool recur = T > 0 && max_seqlen(local) <= kRecMaxT;
+  // the decode rows' state kernel on the second stream, after the work that
+  // stream is already ordered behind
+  auto decode_on_side = [&]() -> cudaError_t {
+    DecodeTaps dt{};
+    if (h->taps_on) dt.o = h->taps.o, dt.y = h->taps.y;
+    int dl = 0;
+    cudaError_t e = launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2,
+                                         h->err, dt, h->side, &dl);
+    if (e != cudaSuccess) return e;
+    h->stats.kernel_launches += (uint64_t)dl;
+    return cudaEventRecord(h->join_ev, h->side);
+  };
   if (fork) {
     M2_CUDA(cudaEventRecord(h->fork_ev, st));
     M2_CUDA(cudaStreamWaitEvent(h->side, h->fork_ev, 0));
@@ -758,15 +775,8 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
       M2_CUDA(launch_ssd_cumsum(zx_pf, bp, local, w.pf.cumdt, nullptr, h->side));
       M2_CUDA(cudaEventRecord(h->cum_ev, h->side));
       h->stats.kernel_launches += 1;
-    }
-    if (fork_decode) {
-      DecodeTaps dt{};
-      if (h->taps_on) dt.o = h->taps.o, dt.y = h->taps.y;
-      int dl = 0;
-      M2_CUDA(launch_decode_stream(w.zx, bp, conv_pool, ssm_pool, bf16_state, n_slots, slot_idx, Bt, w.q2, h->err,
-                                   dt, h->side, &dl));
-      h->stats.kernel_launches += (uint64_t)dl;
-      M2_CUDA(cudaEventRecord(h->join_ev, h->side));
+    } else if (fork_decode) {
+      M2_CUDA(decode_on_side());
     }
   }
   if (T > 0) {
@@ -786,6 +796,11 @@ m2_status m2_mixed(m2_handle* h, const uint16_t* hidden, int Bt, uint16_t* conv_
       M2_STAGE(h, st, M2_STAGE_SSD_STATE_PASS, 1,
                launch_ssd_state_pass(w.pf.states, w.pf.cumdt, local, w.pf.sin_img, ssm_state, bf16_state, zx_pf,
                                      conv_state, st));
+      if (fork_decode) {
+        M2_CUDA(cudaEventRecord(h->fork_ev, st));
+        M2_CUDA(cudaStreamWaitEvent(h->side, h->fork_ev, 0));
+        M2_CUDA(decode_on_side());
+      }
       M2_STAGE(h, st, M2_STAGE_SSD_CHUNK_SCAN, 1,
                launch_ssd_chunk_scan_tc(w.pf.u, w.pf.cumdt, w.pf.sin_img, bp, local, w.pf.y, h->err, st));
     }
