@@ -106,14 +106,15 @@ __device__ __forceinline__ void split2t(uint64_t v, uint32_t& hi, uint32_t& lo) 
 constexpr int kStWork = 256;             // 8 worker warps; worker thread t owns token row t
 constexpr int kStThr = kStWork + 64;     // + a loader warp + an MMA warp
 constexpr int kStSmB = 0;                // B [2 slices of 64 n][256 t][64] as TMA writes it    64 KB
-constexpr int kStSmX = 64 * 1024;        // x [256 t][64 p] as TMA writes it                    32 KB
-constexpr int kStSmW = 96 * 1024;        // w x [2 buffers] x (bf16 high, remainder) [256 t][64 p] 128 KB
-constexpr int kStSmBar = 224 * 1024;
+constexpr int kStSmX = 64 * 1024;        // x [2 buffers][256 t][64 p] as TMA writes it         64 KB
+constexpr int kStSmW = 128 * 1024;       // w x [2 halves of 128 t] x (bf16 high, remainder) [128 t][64 p] 64 KB
+constexpr int kStSmBar = 192 * 1024;
 constexpr int kStSmem = kStSmBar + 128 + 1024;
 
 struct StateBars {
-  uint64_t b_full, x_full, x_empty, mma[2], drain;
-  uint64_t w_full[2], t_empty[2];   // operand k staged / accumulator k read
+  uint64_t b_full, x_full[2], x_empty[2], mma[2], drain;
+  uint64_t wf[2], we[2];            // operand half staged / read by the MMAs
+  uint64_t t_empty[2];              // accumulator k read
   uint32_t tslot;
   int abort;
 };
@@ -124,6 +125,17 @@ __device__ __forceinline__ uint32_t sw_row_chunk(int r, int c) {
   return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
 }
 
+// One CTA per (chunk, group): S[h][p][n] = sum_t w_t x_t[p] B_t[n] for the
+// group's 8 heads, w_t = exp(cum_last - cum_t) dt_t (zero past the chunk).
+// The loader TMA-loads the group's B tile once and each head's x tile into
+// one of two buffers, two heads ahead.  Worker thread t scales token row t of
+// x by w_t and splits it into a bf16 high part and remainder; the operand
+// lives in two halves of 128 tokens, each single-buffered, so the workers of
+// half j (warps 4j..4j+3) stage head h+1 there once the MMAs of head h have
+// read it.  The MMA warp issues each head's 16 K-steps (two MMAs each, high
+// and remainder) into one of two TMEM accumulators, the first 8 from half 0
+// and the last 8 from half 1, committing each half as it is read; the
+// workers drain accumulator k (head h-1) while head h's MMAs run.
 __global__ void __launch_bounds__(kStThr, 1)
     k_ssd_state_tc(const __grid_constant__ CUtensorMap tm_u, const CumDt* __restrict__ cumdt, const SeqInfo si,
                    float* __restrict__ states, int* err) {
@@ -132,7 +144,6 @@ __global__ void __launch_bounds__(kStThr, 1)
   StateBars* sb = reinterpret_cast<StateBars*>(smem + kStSmBar);
   volatile int* abort = &sb->abort;
   uint8_t* sB = smem + kStSmB;
-  uint8_t* sX = smem + kStSmX;
 
   const int c = blockIdx.x, g = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const ChunkPos cp = chunk_of(si, c);
@@ -141,15 +152,15 @@ __global__ void __launch_bounds__(kStThr, 1)
 
   if (tid == 0) {
     mbar_init(&sb->b_full, 1);
-    mbar_init(&sb->x_full, 1);
-    mbar_init(&sb->x_empty, kStWork / 32);
-    mbar_init(&sb->mma[0], 1);
-    mbar_init(&sb->mma[1], 1);
-    mbar_init(&sb->drain, 1);
     for (int k = 0; k < 2; ++k) {
-      mbar_init(&sb->w_full[k], kStWork / 32);
+      mbar_init(&sb->x_full[k], 1);
+      mbar_init(&sb->x_empty[k], kStWork / 32);
+      mbar_init(&sb->mma[k], 1);
+      mbar_init(&sb->wf[k], kStWork / 64);          // the 4 worker warps of a half
+      mbar_init(&sb->we[k], 1);
       mbar_init(&sb->t_empty[k], kStWork / 32);
     }
+    mbar_init(&sb->drain, 1);
     sb->abort = 0;
     fence_mbar_init();
     tma_prefetch(&tm_u);
@@ -172,41 +183,48 @@ __global__ void __launch_bounds__(kStThr, 1)
       mbar_expect_tx(&sb->b_full, 256 * 128 * 2);
       for (int a = 0; a < 2; ++a)
         tma_load_2d(sB + a * 256 * 128, &tm_u, &sb->b_full, kOffB + g * kN + a * 64, cp.t0);
-      int issued = -1;
+      int issued[2] = {-1, -1};   // last head whose x tile went into each buffer
       for (int hh = 0; hh < kHPG; ++hh) {
-        // the x tile is free once every worker has read head hh-1's rows
-        if (!wait_ab(&sb->x_empty, (hh & 1) ^ 1u, abort, err)) break;
-        mbar_expect_tx(&sb->x_full, 256 * 64 * 2);
-        tma_load_2d(sX, &tm_u, &sb->x_full, (g * kHPG + hh) * kP, cp.t0);
-        issued = hh;
+        const int xb = hh & 1;
+        // buffer xb is free once every worker has read head hh-2's rows
+        if (!wait_ab(&sb->x_empty[xb], ((hh >> 1) & 1) ^ 1u, abort, err)) break;
+        mbar_expect_tx(&sb->x_full[xb], 256 * 64 * 2);
+        tma_load_2d(smem + kStSmX + xb * 32 * 1024, &tm_u, &sb->x_full[xb], (g * kHPG + hh) * kP, cp.t0);
+        issued[xb] = hh;
       }
       if (*abort) {   // let copies in flight land before the CTA can exit
         mbar_wait(&sb->b_full, 0, nullptr, 100000000ull);
-        if (issued >= 0) mbar_wait(&sb->x_full, issued & 1, nullptr, 100000000ull);
+        for (int xb = 0; xb < 2; ++xb)
+          if (issued[xb] >= 0) mbar_wait(&sb->x_full[xb], (issued[xb] >> 1) & 1, nullptr, 100000000ull);
       }
     }
   } else if (warp == kStWork / 32 + 1) {
-    // ------------------------------------------------ MMA issuer: head hh's
-    // MMAs run while the workers stage head hh+1 (the operand is double
-    // buffered) and drain head hh-1's accumulator
+    // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       bool ok = wait_ab(&sb->b_full, 0, abort, err);
+      const uint32_t b0 = smem_u32(sB);
       for (int hh = 0; hh < kHPG && ok; ++hh) {
         const int k = hh & 1;
-        ok = wait_ab(&sb->w_full[k], (hh >> 1) & 1, abort, err) &&
-             wait_ab(&sb->t_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err);   // head hh-2 drained
-        if (!ok) break;
-        tc_fence_after();
-        // S[n, p] += sum_t B[t, n] (w x)[t, p]: 16 K-steps of 16 tokens
-        // (2048 bytes of both tiles); B's two 64-column slices are 32 KB apart
-        const uint32_t b0 = smem_u32(sB), h0 = smem_u32(smem + kStSmW + k * 64 * 1024), l0 = h0 + 32 * 1024;
+        if (!wait_ab(&sb->t_empty[k], ((hh >> 1) & 1) ^ 1u, abort, err)) break;   // head hh-2 drained
         const uint32_t d = tmem + (uint32_t)(k * 64);
+        // S[n, p] += sum_t B[t, n] (w x)[t, p]: 16 K-steps of 16 tokens (2048
+        // bytes of each tile), 8 per operand half; B's two 64-column slices
+        // are 32 KB apart
+        for (int half = 0; half < 2 && ok; ++half) {
+          ok = wait_ab(&sb->wf[half], hh & 1, abort, err);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t h0 = smem_u32(smem + kStSmW + half * 32 * 1024), l0 = h0 + 16 * 1024;
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          const uint64_t ad = desc_mnmajor_sw128(b0 + ks * 2048, 256 * 128);
-          mma_f16(d, ad, desc_mnmajor_sw128(h0 + ks * 2048, 1024), IDESC, ks != 0);
-          mma_f16(d, ad, desc_mnmajor_sw128(l0 + ks * 2048, 1024), IDESC, 1u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const int ks = half * 8 + kk;
+            const uint64_t ad = desc_mnmajor_sw128(b0 + ks * 2048, 256 * 128);
+            mma_f16(d, ad, desc_mnmajor_sw128(h0 + kk * 2048, 1024), IDESC, ks != 0);
+            mma_f16(d, ad, desc_mnmajor_sw128(l0 + kk * 2048, 1024), IDESC, 1u);
+          }
+          mma_commit(&sb->we[half]);   // this half of the operand may be restaged
         }
+        if (!ok) break;
         mma_commit(&sb->mma[k]);
       }
       if (*abort) {   // no MMA may still be running when TMEM is freed
@@ -217,12 +235,14 @@ __global__ void __launch_bounds__(kStThr, 1)
   } else {
     // ------------------------------------------------ workers (8 warps)
     const int quarter = warp & 3, side = warp >> 2;
-    const int t = tid;
+    const int t = tid, half = t >> 7, tl = t & 127;   // token row t = row tl of operand half `half`
     const CumDt* cd0 = cumdt + (size_t)c * kNH + g * kHPG;
     // this head's cum_t, cum_last and dt_t; the next head's are fetched one head ahead
     float ct_hi = cd0->hi[t], ct_lo = cd0->lo[t], ct_dt = cd0->dt[t];
     float cl_hi = cd0->hi[cp.n - 1], cl_lo = cd0->lo[cp.n - 1];
     bool ok = wait_ab(&sb->b_full, 0, abort, err);
+    uint8_t* sWh = smem + kStSmW + half * 32 * 1024;
+    uint8_t* sWl = sWh + 16 * 1024;
 
     auto epilogue = [&](int hd) {
       const int k = hd & 1;
@@ -244,9 +264,8 @@ __global__ void __launch_bounds__(kStThr, 1)
     };
 
     for (int hh = 0; hh < kHPG; ++hh) {
-      const int k = hh & 1;
-      uint8_t* sWh = smem + kStSmW + k * 64 * 1024;
-      uint8_t* sWl = sWh + 32 * 1024;
+      const int xb = hh & 1;
+      const uint8_t* sX = smem + kStSmX + xb * 32 * 1024;
       // w_t = exp(cum_last - cum_t) dt_t; zero past the chunk's end
       const float w = t < cp.n ? expf((cl_hi - ct_hi) + (cl_lo - ct_lo)) * ct_dt : 0.f;
       if (hh + 1 < kHPG) {
@@ -257,31 +276,35 @@ __global__ void __launch_bounds__(kStThr, 1)
         cl_hi = nx->hi[cp.n - 1];
         cl_lo = nx->lo[cp.n - 1];
       }
-      ok = wait_ab(&sb->x_full, hh & 1, abort, err) && ok;
+      ok = wait_ab(&sb->x_full[xb], (hh >> 1) & 1, abort, err) && ok;
       uint4 xv[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) xv[q] = *reinterpret_cast<const uint4*>(sX + sw_row_chunk(t, q));
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sb->x_empty);   // this warp's reads of the x tile are done
+      if (lane == 0) mbar_arrive(&sb->x_empty[xb]);   // this warp's reads of x buffer xb are done
       // row t of (w x), bf16 high part and remainder, in the x tile's own
-      // layout; buffer k was last read by head hh-2's MMA, which this thread
-      // saw finish in that head's epilogue
+      // layout, into operand half `half` once head hh-1's MMAs have read it
       const uint64_t w2 = pk2(w, w);
+      uint32_t hi[8][4], lo[8][4];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        uint32_t hi[4], lo[4];
         const uint32_t wd[4] = {xv[q].x, xv[q].y, xv[q].z, xv[q].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          split2t(mul2(w2, pk2(__uint_as_float(wd[e] << 16), __uint_as_float(wd[e] & 0xFFFF0000u))), hi[e], lo[e]);
-        const uint32_t off = sw_row_chunk(t, q);
-        *reinterpret_cast<uint4*>(sWh + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          split2t(mul2(w2, pk2(__uint_as_float(wd[e] << 16), __uint_as_float(wd[e] & 0xFFFF0000u))), hi[q][e],
+                  lo[q][e]);
+      }
+      ok = wait_ab(&sb->we[half], (hh & 1) ^ 1u, abort, err) && ok;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const uint32_t off = sw_row_chunk(tl, q);
+        *reinterpret_cast<uint4*>(sWh + off) = make_uint4(hi[q][0], hi[q][1], hi[q][2], hi[q][3]);
+        *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lo[q][0], lo[q][1], lo[q][2], lo[q][3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sb->w_full[k]);   // this warp's rows of operand k are staged
-      // head hh-1's accumulator: its MMA ran while this head was staged
+      if (lane == 0) mbar_arrive(&sb->wf[half]);   // this warp's rows of operand half `half` are staged
+      // head hh-1's accumulator: its MMAs ran while this head was staged
       if (hh > 0) epilogue(hh - 1);
     }
     epilogue(kHPG - 1);
