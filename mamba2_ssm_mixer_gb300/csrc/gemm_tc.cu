@@ -343,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = pair; tile < num_tiles; tile += npairs) {
       const int m0 = (tile % tiles_m) * kPM + (int)rank * kBM, n0 = (tile / tiles_m) * BN;
-      if (!mbar_wait(&ctl->tfull[acc], acc_phase, abort)) {
+      // one decision per warp: the TMEM loads below are warp-collective
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->tfull[acc], acc_phase, abort))) {
         raise_abort(ctl, err);
         break;
       }
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int quarter = warp & 3;
-    if (kb1 > kb0 && mbar_wait(&ctl->tfull[0], 0, abort)) {
+    if (__all_sync(0xffffffffu, kb1 > kb0 && mbar_wait(&ctl->tfull[0], 0, abort))) {   // warp-uniform: TMEM loads
       tc_fence_after();
       const int n = n0 + quarter * 32 + lane;
 #pragma unroll 1
@@ -642,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- epilogue warps 2..5: accumulator rows -> own exchange buffer
       const int quarter = warp & 3;
       float* dst = red + (quarter * 32 + lane) * RED_LD;
-      if (nk > 0 && mbar_wait(&ctl->tfull[0], 0, abort)) {
+      if (__all_sync(0xffffffffu, nk > 0 && mbar_wait(&ctl->tfull[0], 0, abort))) {   // warp-uniform: TMEM loads
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < BNT; c += 16) {
